@@ -1,0 +1,268 @@
+/*
+ * spec.h -- C ABI of the batch-invariant speculative-verification library
+ * (libspec.so, CUDA sm_103a).
+ *
+ * Contract.  Greedy speculative decoding returns the same tokens as ordinary
+ * one-token-at-a-time decoding only if the target model computes, for every
+ * query row, the same logits whether the row is evaluated alone (width 1), in
+ * a verify block of width 2-8, or in a ragged batch of several sequences
+ * (ramgpt.org, "When Lossless Speculation Stops Being Lossless on Blackwell",
+ * sections "The Hidden Contract Behind Lossless Speculation" and "A Better
+ * Backend Test Matrix").  Every floating-point entry point below computes each
+ * output element with a sequence of operations fixed by the reduction length
+ * (K for the matmul, the row's own KV length for attention, H for norms) and
+ * by nothing else: not by the number of columns, rows or sequences in the
+ * call, nor by where in the call the row sits.  Results are therefore
+ * bit-identical across widths and batch compositions.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated.  The
+ *    library allocates no device memory and keeps no per-call state; scratch
+ *    is caller-supplied workspace sized by the matching *_workspace() call.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and may be captured in a CUDA graph.
+ *  - The returned status reports errors the host can see: bad shapes, NULL or
+ *    misaligned pointers, short workspace, launch failure.  On any status
+ *    other than SPEC_OK nothing was launched, and spec_last_error() gives a
+ *    one-line reason (thread-local).
+ *  - Errors only the device can see (a token id out of range, a NaN logit, a
+ *    block-table entry that is negative, a sequence longer than the declared
+ *    bound) are OR-ed into the caller's int32 word `dev_err` (may be NULL) as
+ *    SPEC_DEVERR_* bits.  Kernels never trap and never wait without a bound.
+ *  - bf16 / fp16 values are passed as their 16-bit patterns (uint16_t).
+ *  - KV caches are paged: [num_pages][Hkv][16][D], 16 tokens per page; token j
+ *    of sequence s lives in page block_table[s * max_blocks + j / 16], slot
+ *    j % 16.
+ *  - Ragged batches: sequence s owns rows cu_rows[s] .. cu_rows[s+1]-1
+ *    (cu_rows has S+1 entries, cu_rows[0] = 0, cu_rows[S] = R); its rows sit
+ *    at absolute positions ctx_start[s], ctx_start[s]+1, ...
+ */
+#ifndef SPEC_H
+#define SPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *spec_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* bad shape, NULL or misaligned pointer */
+    SPEC_ERR_UNSUPPORTED = 2, /* valid request this build does not support */
+    SPEC_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than *_workspace() */
+    SPEC_ERR_CUDA = 4         /* a CUDA runtime call failed */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_F16 = 1, SPEC_BF16 = 2 } spec_dtype;
+
+/* bits OR-ed into *dev_err by kernels */
+#define SPEC_DEVERR_TOKEN_RANGE 0x1 /* a token id outside [0, V) */
+#define SPEC_DEVERR_NAN 0x2         /* a NaN logit (it never wins an argmax) */
+#define SPEC_DEVERR_BLOCK_TABLE 0x4 /* a needed block-table entry is negative or >= num_pages */
+#define SPEC_DEVERR_LENGTH 0x8      /* a sequence exceeds max_kv_len / max_blocks * 16 */
+#define SPEC_DEVERR_TIMEOUT 0x10    /* a bounded wait on an mbarrier ran out */
+#define SPEC_DEVERR_LAYOUT 0x20     /* cu_rows not non-decreasing or cu_rows[S] != R */
+
+const char *spec_status_string(spec_status st);
+const char *spec_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * K1  block-4-bit dequantising matmul
+ *
+ *   y[j][n] (+)= sum_k x[j][k] * d[n][k/32] * (nib(n, k) - 8)
+ *
+ * ramgpt.org, "When Lossless Speculation Stops Being Lossless on Blackwell",
+ * section "Quantized Matrix Multiplication Shows the Same Class of Failure":
+ * a batched product must equal the concatenation of single-column products.
+ * tokenstrom.com, "'Lossless,' but not quite", section "Why the math checks
+ * out and the text still flips": the mat-vec's warp split (and so its partial-
+ * sum order) changed with the number of tokens.  Here the K-split, each lane's
+ * partial-sum order and the combine order are functions of K alone.
+ *
+ *   wq   uint8 [N][K/2]: two 4-bit codes per byte, even k in the low nibble,
+ *        code = q + 8 for q in [-8, 7].  16-byte aligned.
+ *   ws   fp16 bits [N][K/32]: one scale per 32 consecutive k.  16-byte aligned.
+ *   x    bf16 bits [n_cols][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned.
+ *   y    [n_cols][ldy] of y_dt (SPEC_F32 or SPEC_BF16), ldy >= N.
+ *        accumulate != 0 adds into y (SPEC_F32 only): y = fp32(y + result).
+ *   K % 256 == 0, N >= 1, n_cols >= 0 (0 launches nothing).
+ * ---------------------------------------------------------------------- */
+spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
+                         const uint16_t *x, int n_cols, int ldx,
+                         void *y, spec_dtype y_dt, int ldy, int accumulate,
+                         int32_t *dev_err, spec_stream_t stream);
+
+/* The same product computed by a kernel whose split of K and whose CTA shape
+ * are chosen per call from n_cols and the problem size for speed: NOT batch
+ * invariant.  It exists to measure what width-1 speed the invariant kernel
+ * gives up (the pages' prior-art kernels pick geometry by width; tokenstrom.com,
+ * section "Why the math checks out and the text still flips").  Same argument
+ * rules as spec_qmatmul; y_dt must be SPEC_F32 and accumulate 0. */
+spec_status spec_qmatmul_noninvariant(const uint8_t *wq, const uint16_t *ws, int N, int K,
+                                      const uint16_t *x, int n_cols, int ldx,
+                                      float *y, int ldy, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * K2 + K3  split-KV causal attention for verify blocks (paged KV cache)
+ *
+ * ramgpt.org, section "Flash Attention Changes Geometry With Batch Width":
+ * the tile geometry chosen by query width changed the KV traversal and the
+ * combine order.  Here the KV sequence is cut into chunks of a constant 256
+ * keys; row r (position p) gets one partial (max, sum, weighted values) per
+ * chunk c <= p / 256 computed over keys [256c, min(256c + 255, p)] in
+ * ascending order, and the partials are combined in ascending c.  Nothing
+ * depends on the other rows of the call.
+ *
+ *   q        [R][Hq][D] of qkv_dt (SPEC_F16 or SPEC_BF16), 16-byte aligned
+ *   k_cache, v_cache  [num_pages][Hkv][16][D] of qkv_dt, 16-byte aligned
+ *   block_table int32 [S][max_blocks]
+ *   ctx_start int32 [S]: tokens already cached before the block; the block's
+ *            own K/V must already be in the cache (positions ctx_start[s] ..
+ *            ctx_start[s] + rows - 1).  Row i attends to keys 0 .. ctx_start+i.
+ *   cu_rows  int32 [S+1]
+ *   max_kv_len  host bound on ctx_start[s] + rows of s (sizes the grid)
+ *   out      [R][Hq][D] of out_dt (SPEC_F32 or SPEC_BF16)
+ *   scale    multiplies q.k before the softmax
+ *   D in {64, 128}; Hq % Hkv == 0; Hq / Hkv <= 16.
+ * ---------------------------------------------------------------------- */
+size_t spec_flash_decode_workspace(int R, int Hq, int D, int max_kv_len);
+spec_status spec_flash_decode(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, float scale,
+                              const void *k_cache, const void *v_cache, int num_pages,
+                              const int32_t *block_table, int max_blocks,
+                              const int32_t *ctx_start, const int32_t *cu_rows, int S, int R,
+                              int max_kv_len, void *out, spec_dtype out_dt,
+                              void *workspace, size_t ws_bytes, int32_t *dev_err,
+                              spec_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * K4  ragged greedy verification
+ *
+ * proofoftech.org, "'Lossless' speculative decoding isn't free", opening
+ * section: the target checks the drafts in one pass, accepts the prefix it
+ * agrees with and corrects the first token it does not.  ramgpt.org, section
+ * "The Hidden Contract Behind Lossless Speculation": greedy choice = the
+ * maximum-logit token.
+ *
+ *   logits  [R][V] of dt (SPEC_F32 or SPEC_BF16), 16-byte aligned, V % 8 == 0
+ *   drafts  int32 [R - S]: sequence s's L_s = rows_s - 1 drafts start at
+ *           drafts[cu_rows[s] - s]
+ *   argmax_out int32 [R]: lowest index of each row's maximum
+ *   accepted   int32 [S]: first i < L_s with draft_i != argmax[r0 + i], else L_s
+ *   correction int32 [S]: argmax[r0 + accepted[s]]
+ *   ctx_new    int32 [S]: ctx_start[s] + accepted[s] + 1
+ *   Integer results are exact; NaN logits never win and set SPEC_DEVERR_NAN.
+ * ---------------------------------------------------------------------- */
+size_t spec_verify_greedy_workspace(int R, int V);
+spec_status spec_verify_greedy(const void *logits, spec_dtype dt, int V,
+                               const int32_t *cu_rows, int S, int R,
+                               const int32_t *drafts, const int32_t *ctx_start,
+                               int32_t *argmax_out, int32_t *accepted, int32_t *correction,
+                               int32_t *ctx_new, void *workspace, size_t ws_bytes,
+                               int32_t *dev_err, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * K5  KV-cache realignment after ragged acceptance
+ *
+ * proofoftech.org, section "Batching breaks the implementation": after
+ * sequences accept different numbers of drafts their positions and KV state
+ * must be realigned exactly.  Rows 0 .. accepted[s] of sequence s are kept:
+ * staged row cu_rows[s] + i is written to the cache slot of position
+ * ctx_start[s] + i.  Rejected rows never reach the cache.
+ *
+ *   k_stage, v_stage  [R][Hkv][D] 16-bit elements, or both NULL when the block
+ *            was already written into the cache in place (then only the index
+ *            outputs are produced and the cache is not touched)
+ *   cu_kept  int32 [S+1]: exclusive prefix sum of accepted[s] + 1
+ *   kept_src int32 [R], dst_slot int64 [R]: for kept token j (j < cu_kept[S])
+ *            its staging row and its cache slot page * 16 + slot
+ *   D % 8 == 0.
+ * ---------------------------------------------------------------------- */
+spec_status spec_kv_compact(const void *k_stage, const void *v_stage, void *k_cache, void *v_cache,
+                            int Hkv, int D, int num_pages, const int32_t *block_table, int max_blocks,
+                            const int32_t *ctx_start, const int32_t *accepted,
+                            const int32_t *cu_rows, int S, int R,
+                            int32_t *cu_kept, int32_t *kept_src, int64_t *dst_slot,
+                            int32_t *dev_err, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Decoder glue for the end-to-end generation workload.  Each is a per-row
+ * operation with a fixed reduction order over the row, hence width-invariant.
+ * The pages run real decoders but name none of these steps; they are the
+ * textbook definitions (RMSNorm, rotate-half RoPE, SwiGLU).
+ * ---------------------------------------------------------------------- */
+
+/* h[r][:] = float(emb[tokens[r]][:]); emb bf16 [V][H]; h fp32 [R][H]. */
+spec_status spec_embed(const uint16_t *emb, int V, int H, const int32_t *tokens, int R,
+                       float *h, int32_t *dev_err, spec_stream_t stream);
+
+/* If delta != NULL first h += delta (fp32, in place).  Then
+ * out[r][:] = bf16(h[r][:] / sqrt(mean(h[r]^2) + eps) * w[:]).
+ * h, delta fp32 [R][H]; w fp32 [H]; out bf16 [R][H]; H % 4 == 0. */
+spec_status spec_add_rmsnorm(float *h, const float *delta, const float *w, int R, int H, float eps,
+                             uint16_t *out, spec_stream_t stream);
+
+/* Fill tab[p][i] = (cos, sin)(p * theta^(-2i/D)) for p < max_pos, i < D/2,
+ * fp32 [max_pos][D/2][2]; angles evaluated in double. */
+spec_status spec_rope_table(float *tab, int max_pos, int D, float theta, spec_stream_t stream);
+
+/* Split qkv rows fp32 [R][(Hq + 2 Hkv) D] = [q | k | v]; rotate q and k
+ * (rotate-half) at each row's position; write q bf16 [R][Hq][D] and write k, v
+ * (bf16) either into the paged cache at the row's position (k_stage == NULL) or
+ * into staging rows k_stage/v_stage [R][Hkv][D]. */
+spec_status spec_rope_append(const float *qkv, int R, int Hq, int Hkv, int D,
+                             const float *rope_tab, int max_pos,
+                             const int32_t *cu_rows, const int32_t *ctx_start, int S,
+                             uint16_t *q_out, uint16_t *k_cache, uint16_t *v_cache, int num_pages,
+                             const int32_t *block_table, int max_blocks,
+                             uint16_t *k_stage, uint16_t *v_stage,
+                             int32_t *dev_err, spec_stream_t stream);
+
+/* out[r][i] = bf16(silu(gu[r][i]) * gu[r][F + i]); gu fp32 [R][2F]; out bf16 [R][F]. */
+spec_status spec_swiglu(const float *gu, int R, int F, uint16_t *out, spec_stream_t stream);
+
+/* out[i] = bf16(in[i]) for i < n (round to nearest even). */
+spec_status spec_cast_bf16(const float *in, size_t n, uint16_t *out, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * n-gram drafting on the device (tokenstrom.com, section "Why the math
+ * checks out and the text still flips", and ramgpt.org, section "Flash
+ * Attention Changes Geometry With Batch Width", both run n-gram speculation;
+ * neither gives the rule, so this is a reading).  For each sequence s with
+ * history hist[s][0 .. hist_len[s]-1] (row stride hist_cap): find the most
+ * recent earlier occurrence of the last n tokens (n = 3, then 2, then 1),
+ * propose the up to W tokens that followed it (never past the end of the
+ * history) and fill the remaining slots from pad[s][slot].
+ *   drafts        int32 [S][W]
+ *   matched_n     int32 [S] or NULL: the n that matched (0: none)
+ *   block_tokens  int32 [S][W + 1] or NULL: the next verify block, i.e. the
+ *                 last history token followed by the W drafts
+ * ---------------------------------------------------------------------- */
+spec_status spec_ngram_draft(const int32_t *hist, int hist_cap, const int32_t *hist_len, int S, int W,
+                             const int32_t *pad, int32_t *drafts, int32_t *matched_n,
+                             int32_t *block_tokens, spec_stream_t stream);
+
+/* Commit one verify step to the device-side histories: append drafts[s][0 ..
+ * accepted[s]-1] and correction[s] to hist[s], advance hist_len[s] by
+ * accepted[s] + 1 and copy ctx[s] = ctx_new[s].  A history that would overflow
+ * hist_cap is left unchanged and sets SPEC_DEVERR_LENGTH. */
+spec_status spec_commit_accepted(int32_t *hist, int hist_cap, int32_t *hist_len, const int32_t *drafts, int W,
+                                 const int32_t *accepted, const int32_t *correction, const int32_t *ctx_new,
+                                 int32_t *ctx, int S, int32_t *dev_err, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Test hook: spec_qmatmul with an explicit column-tile width nt in {1, 2, 4}
+ * (columns per CTA = 8 nt).  The result of every column must not depend on
+ * nt; the tests use this to show it.  y_dt is SPEC_F32.
+ * ---------------------------------------------------------------------- */
+spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,
+                                  int n_cols, int ldx, float *y, int ldy, int nt, spec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_H */

@@ -1,0 +1,202 @@
+"""ctypes binding of libspec.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls, takes torch
+tensors (device memory) and plain ints, passes their data pointers and the
+current CUDA stream, and raises ``SpecError`` on any status other than SPEC_OK.
+There is no fallback: if the library is missing or fails to load, the import
+of this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+SPEC_F32, SPEC_F16, SPEC_BF16 = 0, 1, 2
+DEVERR = {"TOKEN_RANGE": 0x1, "NAN": 0x2, "BLOCK_TABLE": 0x4, "LENGTH": 0x8, "TIMEOUT": 0x10, "LAYOUT": 0x20}
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {_status_name(status)}: {msg}")
+        self.status = status
+
+
+_vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+# name -> (restype, argtypes)
+_SIGS = {
+    "spec_status_string": (ctypes.c_char_p, [_i32]),
+    "spec_last_error": (ctypes.c_char_p, []),
+    "spec_qmatmul": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _vp]),
+    "spec_qmatmul_noninvariant": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _vp]),
+    "spec_qmatmul_debug_nt": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _vp]),
+    "spec_flash_decode_workspace": (_sz, [_i32, _i32, _i32, _i32]),
+    "spec_flash_decode": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32,
+                                 _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
+    "spec_verify_greedy_workspace": (_sz, [_i32, _i32]),
+    "spec_verify_greedy": (_i32, [_vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "spec_kv_compact": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp,
+                               _vp, _vp, _vp]),
+    "spec_embed": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp]),
+    "spec_add_rmsnorm": (_i32, [_vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp]),
+    "spec_rope_table": (_i32, [_vp, _i32, _i32, _f32, _vp]),
+    "spec_rope_append": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp,
+                                _i32, _vp, _vp, _vp, _vp]),
+    "spec_swiglu": (_i32, [_vp, _i32, _i32, _vp, _vp]),
+    "spec_cast_bf16": (_i32, [_vp, _sz, _vp, _vp]),
+    "spec_ngram_draft": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "spec_commit_accepted": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libspec.so (building it first when it is absent and nvcc is present)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise ImportError(f"libspec.so is not built ({path}); run __graft_entry__.build()")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _status_name(st: int) -> str:
+    try:
+        return load().spec_status_string(st).decode()
+    except Exception:
+        return str(st)
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise SpecError(fn, st, load().spec_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    if torch.cuda.is_available():
+        return torch.cuda.current_stream().cuda_stream
+    return None
+
+
+def _dt(t: torch.Tensor) -> int:
+    return {torch.float32: SPEC_F32, torch.float16: SPEC_F16, torch.bfloat16: SPEC_BF16,
+            torch.int16: SPEC_BF16, torch.uint16: SPEC_BF16}[t.dtype]
+
+
+# ---------------------------------------------------------------------------
+# wrappers (names follow the C ABI)
+# ---------------------------------------------------------------------------
+def spec_qmatmul(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate=0, dev_err=None, stream=None):
+    _check("spec_qmatmul", load().spec_qmatmul(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx, _ptr(y), y_dt, ldy,
+                                               int(accumulate), _ptr(dev_err), _stream(stream)))
+
+
+def spec_qmatmul_noninvariant(wq, ws, N, K, x, n_cols, ldx, y, ldy, stream=None):
+    _check("spec_qmatmul_noninvariant", load().spec_qmatmul_noninvariant(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols,
+                                                                         ldx, _ptr(y), ldy, _stream(stream)))
+
+
+def spec_qmatmul_debug_nt(wq, ws, N, K, x, n_cols, ldx, y, ldy, nt, stream=None):
+    _check("spec_qmatmul_debug_nt", load().spec_qmatmul_debug_nt(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx,
+                                                                 _ptr(y), ldy, nt, _stream(stream)))
+
+
+def spec_flash_decode_workspace(R, Hq, D, max_kv_len) -> int:
+    return int(load().spec_flash_decode_workspace(R, Hq, D, max_kv_len))
+
+
+def spec_flash_decode(q, qkv_dt, Hq, Hkv, D, scale, k_cache, v_cache, num_pages, block_table, max_blocks, ctx_start,
+                      cu_rows, S, R, max_kv_len, out, out_dt, workspace, ws_bytes, dev_err=None, stream=None):
+    _check("spec_flash_decode", load().spec_flash_decode(
+        _ptr(q), qkv_dt, Hq, Hkv, D, float(scale), _ptr(k_cache), _ptr(v_cache), num_pages, _ptr(block_table),
+        max_blocks, _ptr(ctx_start), _ptr(cu_rows), S, R, max_kv_len, _ptr(out), out_dt, _ptr(workspace),
+        int(ws_bytes), _ptr(dev_err), _stream(stream)))
+
+
+def spec_verify_greedy_workspace(R, V) -> int:
+    return int(load().spec_verify_greedy_workspace(R, V))
+
+
+def spec_verify_greedy(logits, dt, V, cu_rows, S, R, drafts, ctx_start, argmax_out, accepted, correction, ctx_new,
+                       workspace, ws_bytes, dev_err=None, stream=None):
+    _check("spec_verify_greedy", load().spec_verify_greedy(
+        _ptr(logits), dt, V, _ptr(cu_rows), S, R, _ptr(drafts), _ptr(ctx_start), _ptr(argmax_out), _ptr(accepted),
+        _ptr(correction), _ptr(ctx_new), _ptr(workspace), int(ws_bytes), _ptr(dev_err), _stream(stream)))
+
+
+def spec_kv_compact(k_stage, v_stage, k_cache, v_cache, Hkv, D, num_pages, block_table, max_blocks, ctx_start,
+                    accepted, cu_rows, S, R, cu_kept, kept_src, dst_slot, dev_err=None, stream=None):
+    _check("spec_kv_compact", load().spec_kv_compact(
+        _ptr(k_stage), _ptr(v_stage), _ptr(k_cache), _ptr(v_cache), Hkv, D, num_pages, _ptr(block_table), max_blocks,
+        _ptr(ctx_start), _ptr(accepted), _ptr(cu_rows), S, R, _ptr(cu_kept), _ptr(kept_src), _ptr(dst_slot),
+        _ptr(dev_err), _stream(stream)))
+
+
+def spec_embed(emb, V, H, tokens, R, h, dev_err=None, stream=None):
+    _check("spec_embed", load().spec_embed(_ptr(emb), V, H, _ptr(tokens), R, _ptr(h), _ptr(dev_err), _stream(stream)))
+
+
+def spec_add_rmsnorm(h, delta, w, R, H, eps, out, stream=None):
+    _check("spec_add_rmsnorm", load().spec_add_rmsnorm(_ptr(h), _ptr(delta), _ptr(w), R, H, float(eps), _ptr(out),
+                                                       _stream(stream)))
+
+
+def spec_rope_table(tab, max_pos, D, theta, stream=None):
+    _check("spec_rope_table", load().spec_rope_table(_ptr(tab), max_pos, D, float(theta), _stream(stream)))
+
+
+def spec_rope_append(qkv, R, Hq, Hkv, D, rope_tab, max_pos, cu_rows, ctx_start, S, q_out, k_cache, v_cache,
+                     num_pages, block_table, max_blocks, k_stage=None, v_stage=None, dev_err=None, stream=None):
+    _check("spec_rope_append", load().spec_rope_append(
+        _ptr(qkv), R, Hq, Hkv, D, _ptr(rope_tab), max_pos, _ptr(cu_rows), _ptr(ctx_start), S, _ptr(q_out),
+        _ptr(k_cache), _ptr(v_cache), num_pages, _ptr(block_table), max_blocks, _ptr(k_stage), _ptr(v_stage),
+        _ptr(dev_err), _stream(stream)))
+
+
+def spec_swiglu(gu, R, F, out, stream=None):
+    _check("spec_swiglu", load().spec_swiglu(_ptr(gu), R, F, _ptr(out), _stream(stream)))
+
+
+def spec_cast_bf16(inp, n, out, stream=None):
+    _check("spec_cast_bf16", load().spec_cast_bf16(_ptr(inp), int(n), _ptr(out), _stream(stream)))
+
+
+def spec_ngram_draft(hist, hist_cap, hist_len, S, W, pad, drafts, matched_n=None, block_tokens=None, stream=None):
+    _check("spec_ngram_draft", load().spec_ngram_draft(_ptr(hist), hist_cap, _ptr(hist_len), S, W, _ptr(pad),
+                                                       _ptr(drafts), _ptr(matched_n), _ptr(block_tokens),
+                                                       _stream(stream)))
+
+
+def spec_commit_accepted(hist, hist_cap, hist_len, drafts, W, accepted, correction, ctx_new, ctx, S, dev_err=None,
+                         stream=None):
+    _check("spec_commit_accepted", load().spec_commit_accepted(
+        _ptr(hist), hist_cap, _ptr(hist_len), _ptr(drafts), W, _ptr(accepted), _ptr(correction), _ptr(ctx_new),
+        _ptr(ctx), S, _ptr(dev_err), _stream(stream)))

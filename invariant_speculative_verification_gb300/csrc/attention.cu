@@ -1,0 +1,523 @@
+// K2 + K3: batch-invariant split-KV causal attention over a paged KV cache.
+//
+// ramgpt.org, "When Lossless Speculation Stops Being Lossless on Blackwell",
+// section "Flash Attention Changes Geometry With Batch Width": choosing tile
+// geometry by query width changed the KV traversal and the combine order.
+// Here every row's reduction structure is fixed by its own position p:
+//  * keys are cut into chunks of CHUNK = 256 (a constant), chunk c covers keys
+//    [256c, 256c + 255]; row p has partials for chunks 0 .. p / 256;
+//  * inside a chunk, keys are visited in sub-tiles of 64 in ascending order
+//    with an online softmax (running max m, sum l, weighted values o);
+//  * K3 combines a row's chunk partials in ascending chunk order.
+// The other rows of the call only decide which warp or CTA runs a row and how
+// many fully masked sub-tiles it also visits; a fully masked sub-tile leaves
+// (m, l, o) bit-unchanged (rescale factor exactly 1, probabilities exactly 0).
+//
+// K2 (attn_partial_kernel): one CTA per (chunk, kv head, sequence).  A
+// producer thread streams the chunk's K and V pages with 4-D TMA boxes
+// (128B swizzle) into a ring of 64-key slots; four consumer warps each own a
+// 16-row M-tile of (query row, grouped head) pairs and run S = Q K^T and
+// O += P V on mma.sync m16n8k16 with fp32 accumulation.  P enters the PV
+// product as a hi + lo pair of 16-bit values so its rounding error is ~2^-17.
+// K3 (attn_combine_kernel): one warp per (row, head).
+#include "common.cuh"
+
+namespace {
+
+constexpr int CHUNK = 256;
+constexpr int SUB = 64;
+constexpr int PAGE = 16;
+constexpr int NCONS = 4;
+constexpr int THREADS = (NCONS + 1) * 32;
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int D>
+struct ACfg {
+    static constexpr int HALVES = D / 64;                 // 64-wide d boxes per key row
+    static constexpr int KV_BYTES = HALVES * SUB * 128;   // one of K or V for a slot
+    static constexpr int SLOT = 2 * KV_BYTES;
+    static constexpr int NSLOT = (D == 128) ? 3 : 5;
+    static constexpr int SMEM = 1024 + NSLOT * SLOT + 2 * NSLOT * 8;
+};
+
+template <bool BF16>
+__device__ __forceinline__ void mma16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                      uint32_t b1, const float (&c)[4]) {
+    if (BF16)
+        dev::mma_bf16(d, a0, a1, a2, a3, b0, b1, c);
+    else
+        dev::mma_f16(d, a0, a1, a2, a3, b0, b1, c);
+}
+
+// pack two fp32 into the 16-bit pair (lo half = a) with round to nearest even,
+// and return the residuals a - hi, b - hi (exact in fp32)
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_hi(float a, float b, float &ra, float &rb) {
+    if (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        float2 f = __bfloat1622float2(h);
+        ra = a - f.x;
+        rb = b - f.y;
+        return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(a, b);
+        float2 f = __half22float2(h);
+        ra = a - f.x;
+        rb = b - f.y;
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(THREADS, 1)
+attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                    const uint16_t *__restrict__ q, int Hq, int Hkv, float scale_log2, int num_pages,
+                    const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_start,
+                    const int32_t *__restrict__ cu_rows, int R, int max_kv_len, int nc_max,
+                    float2 *__restrict__ part_ml, float *__restrict__ part_o, int32_t *dev_err) {
+    using C = ACfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NSLOT * C::SLOT);
+    uint64_t *empty = full + C::NSLOT;
+
+    const int c = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = cu_rows[s];
+    const int rows = cu_rows[s + 1] - r0;
+    const int ctx = ctx_start[s];
+    const int len = ctx + rows;
+    if (rows <= 0 || ctx < 0) return;
+    if (r0 < 0 || r0 + rows > R) {  // rows outside the workspace the host sized
+        if (threadIdx.x == 0 && c == 0 && kvh == 0) dev::report(dev_err, SPEC_DEVERR_LAYOUT);
+        return;
+    }
+    if (len > max_kv_len || len > max_blocks * PAGE) {
+        if (threadIdx.x == 0 && c == 0 && kvh == 0) dev::report(dev_err, SPEC_DEVERR_LENGTH);
+        return;
+    }
+    const int kbeg = c * CHUNK;
+    if (kbeg >= len) return;
+    const int kend = min(kbeg + CHUNK, len);
+    const int nsub = (kend - kbeg + SUB - 1) / SUB;
+    const int G = Hq / Hkv;
+    const int i0 = max(0, kbeg - ctx);  // first row whose position reaches this chunk
+    const int mrows = (rows - i0) * G;
+    const int rounds = (mrows + 16 * NCONS - 1) / (16 * NCONS);
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < C::NSLOT; ++b) {
+            dev::mbar_init(&full[b], 1);
+            dev::mbar_init(&empty[b], NCONS);
+        }
+        dev::fence_barrier_init();
+    }
+    __syncthreads();
+    const int total = rounds * nsub;
+
+    if (warp == NCONS) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            dev::prefetch_tmap(&tk);
+            dev::prefetch_tmap(&tv);
+            const int32_t *bt = block_table + (size_t)s * max_blocks;
+            int issued = 0;
+            for (int it = 0; it < total; ++it) {
+                const int b = it % C::NSLOT;
+                if (it >= C::NSLOT && !dev::mbar_wait(&empty[b], ((it / C::NSLOT) - 1) & 1)) {
+                    dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                    break;
+                }
+                const int sub = it % nsub;
+                const int key0 = kbeg + sub * SUB;
+                const int pg0 = key0 / PAGE;
+                const int pg1 = min(pg0 + SUB / PAGE, (len + PAGE - 1) / PAGE);
+                uint8_t *kdst = smem + b * C::SLOT;
+                uint8_t *vdst = kdst + C::KV_BYTES;
+                dev::mbar_arrive_expect_tx(&full[b], (uint32_t)((pg1 - pg0) * C::HALVES * 2 * 2048));
+                for (int pg = pg0; pg < pg1; ++pg) {
+                    int phys = bt[pg];
+                    if (phys < 0 || phys >= num_pages) {
+                        dev::report(dev_err, SPEC_DEVERR_BLOCK_TABLE);
+                        phys = 0;
+                    }
+                    const int off = (pg - pg0) * 2048;
+#pragma unroll
+                    for (int hh = 0; hh < C::HALVES; ++hh) {
+                        dev::tma_load_4d(kdst + hh * SUB * 128 + off, &tk, hh * 64, 0, kvh, phys, &full[b]);
+                        dev::tma_load_4d(vdst + hh * SUB * 128 + off, &tv, hh * 64, 0, kvh, phys, &full[b]);
+                    }
+                }
+                issued = it + 1;
+            }
+            for (int it = (issued > C::NSLOT ? issued - C::NSLOT : 0); it < issued; ++it)
+                if (!dev::mbar_wait(&full[it % C::NSLOT], (it / C::NSLOT) & 1))
+                    dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int g = lane >> 2, t = lane & 3;
+    int it = 0;
+    bool ok = true;
+    for (int ro = 0; ro < rounds; ++ro) {
+        const int mt = ro * NCONS + warp;
+        const bool active = (mt * 16 < mrows);
+        // rows of this lane: m0 = 16 mt + g, m1 = m0 + 8
+        int pos[2];
+        bool valid[2];
+        size_t qoff[2];
+        int orow[2], ohead[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int m = mt * 16 + g + 8 * h;
+            valid[h] = active && m < mrows;
+            const int i = i0 + (valid[h] ? m / G : 0);
+            const int gg = valid[h] ? m % G : 0;
+            pos[h] = ctx + i;
+            orow[h] = r0 + i;
+            ohead[h] = kvh * G + gg;
+            qoff[h] = ((size_t)orow[h] * Hq + ohead[h]) * D;
+        }
+        // Q fragments for all k-steps (A operand): row m0 / m1, d = 16 kk + 2t (+8)
+        uint32_t qa[D / 16][4];
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int d0 = 16 * kk + 2 * t;
+            qa[kk][0] = valid[0] ? *reinterpret_cast<const uint32_t *>(q + qoff[0] + d0) : 0u;
+            qa[kk][1] = valid[1] ? *reinterpret_cast<const uint32_t *>(q + qoff[1] + d0) : 0u;
+            qa[kk][2] = valid[0] ? *reinterpret_cast<const uint32_t *>(q + qoff[0] + d0 + 8) : 0u;
+            qa[kk][3] = valid[1] ? *reinterpret_cast<const uint32_t *>(q + qoff[1] + d0 + 8) : 0u;
+        }
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+        float o[D / 8][4];
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+
+        for (int sub = 0; sub < nsub; ++sub, ++it) {
+            const int b = it % C::NSLOT;
+            if (ok && !dev::mbar_wait(&full[b], (it / C::NSLOT) & 1)) {
+                dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                ok = false;  // keep walking the loop so named barriers stay matched
+            }
+            const int key0 = kbeg + sub * SUB;
+            uint8_t *kslot = smem + b * C::SLOT;
+            uint8_t *vslot = kslot + C::KV_BYTES;
+            const int nvalid = len - key0;  // keys of this slot inside the sequence
+            if (nvalid < SUB) {
+                // V rows past the sequence end hold stale or unloaded data: zero them so
+                // that 0-probability keys contribute exactly 0 to P V
+                const int tid = threadIdx.x;
+                for (int idx = tid; idx < C::HALVES * (SUB - nvalid) * 8; idx += NCONS * 32) {
+                    const int hh = idx / ((SUB - nvalid) * 8);
+                    const int rem = idx % ((SUB - nvalid) * 8);
+                    const int key = nvalid + rem / 8, ch = rem % 8;
+                    *reinterpret_cast<uint4 *>(vslot + hh * SUB * 128 + key * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                }
+                dev::fence_proxy_async();
+                asm volatile("bar.sync 1, %0;" ::"n"(NCONS * 32) : "memory");
+            }
+            if (active && ok) {
+                const uint32_t kb = dev::smem_u32(kslot), vb = dev::smem_u32(vslot);
+                // ---- S = Q K^T (16 rows x 64 keys) ----
+                float sc[8][4];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int hh = (16 * kk) / 64;
+                    const int cbase = ((16 * kk) % 64) / 8;
+#pragma unroll
+                    for (int jp = 0; jp < 4; ++jp) {
+                        const int mi = lane >> 3;
+                        const int key = 8 * (2 * jp + (mi >> 1)) + (lane & 7);
+                        const int ch = cbase + (mi & 1);
+                        uint32_t b0, b1, b2, b3;
+                        dev::ldmatrix_x4(b0, b1, b2, b3, kb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
+                        mma16<BF16>(sc[2 * jp], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1, sc[2 * jp]);
+                        mma16<BF16>(sc[2 * jp + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3,
+                                    sc[2 * jp + 1]);
+                    }
+                }
+                // ---- mask, scale to log2 units, online softmax ----
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = e >> 1;
+                        const int key = key0 + 8 * j + 2 * t + (e & 1);
+                        const bool vis = valid[h] && key <= pos[h];
+                        const float v = vis ? sc[j][e] * scale_log2 : -INFINITY;
+                        sc[j][e] = v;
+                        mx[h] = fmaxf(mx[h], v);
+                    }
+                }
+                float alpha[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                    const float mnew = fmaxf(m_run[h], mx[h]);
+                    alpha[h] = (mnew == m_run[h]) ? 1.0f : exp2f(m_run[h] - mnew);
+                    m_run[h] = mnew;
+                }
+                float rs[2] = {0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = e >> 1;
+                        const float p = (m_run[h] == -INFINITY) ? 0.f : exp2f(sc[j][e] - m_run[h]);
+                        sc[j][e] = p;
+                        rs[h] += p;
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 1);
+                    rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 2);
+                    l_run[h] = l_run[h] * alpha[h] + rs[h];
+                }
+#pragma unroll
+                for (int nd = 0; nd < D / 8; ++nd) {
+                    o[nd][0] *= alpha[0];
+                    o[nd][1] *= alpha[0];
+                    o[nd][2] *= alpha[1];
+                    o[nd][3] *= alpha[1];
+                }
+                // ---- O += P V with P = hi + lo ----
+#pragma unroll
+                for (int kk = 0; kk < SUB / 16; ++kk) {
+                    uint32_t ph[4], pl[4];
+                    float r00, r01, r10, r11, r20, r21, r30, r31;
+                    ph[0] = pack_hi<BF16>(sc[2 * kk][0], sc[2 * kk][1], r00, r01);
+                    ph[1] = pack_hi<BF16>(sc[2 * kk][2], sc[2 * kk][3], r10, r11);
+                    ph[2] = pack_hi<BF16>(sc[2 * kk + 1][0], sc[2 * kk + 1][1], r20, r21);
+                    ph[3] = pack_hi<BF16>(sc[2 * kk + 1][2], sc[2 * kk + 1][3], r30, r31);
+                    pl[0] = pack2<BF16>(r00, r01);
+                    pl[1] = pack2<BF16>(r10, r11);
+                    pl[2] = pack2<BF16>(r20, r21);
+                    pl[3] = pack2<BF16>(r30, r31);
+#pragma unroll
+                    for (int ndp = 0; ndp < D / 16; ++ndp) {
+                        const int mi = lane >> 3;
+                        const int key = 16 * kk + 8 * (mi & 1) + (lane & 7);
+                        const int dch = 2 * ndp + (mi >> 1);     // 8-wide d chunk
+                        const int hh = dch / 8, ch = dch % 8;
+                        uint32_t b0, b1, b2, b3;
+                        dev::ldmatrix_x4_trans(b0, b1, b2, b3, vb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
+                        mma16<BF16>(o[2 * ndp], ph[0], ph[1], ph[2], ph[3], b0, b1, o[2 * ndp]);
+                        mma16<BF16>(o[2 * ndp], pl[0], pl[1], pl[2], pl[3], b0, b1, o[2 * ndp]);
+                        mma16<BF16>(o[2 * ndp + 1], ph[0], ph[1], ph[2], ph[3], b2, b3, o[2 * ndp + 1]);
+                        mma16<BF16>(o[2 * ndp + 1], pl[0], pl[1], pl[2], pl[3], b2, b3, o[2 * ndp + 1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(&empty[b]);
+        }
+        // ---- write this chunk's partial for the lane's rows ----
+        if (active && ok) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (!valid[h]) continue;
+                const size_t pidx = ((size_t)orow[h] * Hq + ohead[h]) * nc_max + c;
+                if (t == 0) part_ml[pidx] = make_float2(m_run[h], l_run[h]);
+                float *op = part_o + pidx * D;
+#pragma unroll
+                for (int nd = 0; nd < D / 8; ++nd)
+                    *reinterpret_cast<float2 *>(op + 8 * nd + 2 * t) = make_float2(o[nd][2 * h], o[nd][2 * h + 1]);
+            }
+        }
+    }
+}
+
+// K3: out = (sum_c o_c 2^(m_c - m)) / (sum_c l_c 2^(m_c - m)), c ascending
+template <int D, bool OUT_BF16>
+__global__ void __launch_bounds__(128)
+attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__restrict__ cu_rows, int S, int R, int Hq,
+                    int nc_max, const float2 *__restrict__ part_ml, const float *__restrict__ part_o, void *out,
+                    int max_kv_len) {
+    const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (wid >= R * Hq) return;
+    const int r = wid / Hq, h = wid % Hq;
+    int lo = 0, hi = S;  // sequence of row r: largest s with cu_rows[s] <= r
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu_rows[mid] <= r) lo = mid; else hi = mid;
+    }
+    const int p = ctx_start[lo] + (r - cu_rows[lo]);
+    constexpr int PER = D / 32;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    if (p < 0 || p >= max_kv_len) {
+        // the partial kernel rejected this sequence (length error); emit zeros
+    } else {
+        const int nc = p / CHUNK + 1;
+        const float2 *ml = part_ml + ((size_t)r * Hq + h) * nc_max;
+        float m = -INFINITY;
+        for (int c = 0; c < nc; ++c) m = fmaxf(m, ml[c].x);
+        float l = 0.f;
+        for (int c = 0; c < nc; ++c) {
+            const float w = exp2f(ml[c].x - m);
+            l += ml[c].y * w;
+            const float *op = part_o + (((size_t)r * Hq + h) * nc_max + c) * D + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] += op[e] * w;
+        }
+        const float inv = 1.0f / l;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] *= inv;
+    }
+    const size_t ob = ((size_t)r * Hq + h) * D + lane * PER;
+    if (OUT_BF16) {
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(out) + ob;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[e] = __float2bfloat16_rn(acc[e]);
+    } else {
+        float *o = reinterpret_cast<float *>(out) + ob;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[e] = acc[e];
+    }
+}
+
+template <int D, bool BF16>
+spec_status launch_partial(const CUtensorMap &tk, const CUtensorMap &tv, const void *q, int Hq, int Hkv, float scale,
+                           int num_pages, const int32_t *bt, int max_blocks, const int32_t *ctx, const int32_t *cu,
+                           int S, int R, int max_kv_len, int nc_max, float2 *ml, float *po, int32_t *dev_err,
+                           cudaStream_t st) {
+    using C = ACfg<D>;
+    auto kern = attn_partial_kernel<D, BF16>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return spec::cuda_status(e, "cudaFuncSetAttribute(attn smem)");
+        configured = true;
+    }
+    dim3 grid(nc_max, Hkv, S);
+    kern<<<grid, THREADS, C::SMEM, st>>>(tk, tv, reinterpret_cast<const uint16_t *>(q), Hq, Hkv, scale * LOG2E,
+                                         num_pages, bt, max_blocks, ctx, cu, R, max_kv_len, nc_max, ml, po, dev_err);
+    return spec::cuda_status(cudaGetLastError(), "attn partial launch");
+}
+
+}  // namespace
+
+namespace spec {
+size_t attn_workspace_bytes(int R, int Hq, int D, int max_kv_len) {
+    const size_t nc = (size_t)((max_kv_len + CHUNK - 1) / CHUNK);
+    const size_t pairs = (size_t)R * Hq * nc;
+    size_t ml = pairs * sizeof(float2);
+    ml = (ml + 255) & ~size_t(255);
+    return ml + pairs * D * sizeof(float);
+}
+
+// Launch K2 and K3; the caller has validated every argument.
+spec_status attn_run(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, float scale, const void *k_cache,
+                     const void *v_cache, int num_pages, const int32_t *block_table, int max_blocks,
+                     const int32_t *ctx_start, const int32_t *cu_rows, int S, int R, int max_kv_len, void *out,
+                     spec_dtype out_dt, void *workspace, int32_t *dev_err, cudaStream_t stream) {
+    const int nc_max = (max_kv_len + CHUNK - 1) / CHUNK;
+    const size_t pairs = (size_t)R * Hq * nc_max;
+    size_t mlb = (pairs * sizeof(float2) + 255) & ~size_t(255);
+    float2 *ml = reinterpret_cast<float2 *>(workspace);
+    float *po = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + mlb);
+
+    CUtensorMap tk, tv;
+    uint64_t dims[4] = {(uint64_t)D, (uint64_t)PAGE, (uint64_t)Hkv, (uint64_t)num_pages};
+    uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)PAGE * D * 2, (uint64_t)Hkv * PAGE * D * 2};
+    uint32_t box[4] = {64, PAGE, 1, 1};
+    if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, k_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, v_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return SPEC_ERR_CUDA;
+    const bool bf = (qkv_dt == SPEC_BF16);
+    spec_status st;
+    if (D == 128)
+        st = bf ? launch_partial<128, true>(tk, tv, q, Hq, Hkv, scale, num_pages, block_table, max_blocks, ctx_start,
+                                            cu_rows, S, R, max_kv_len, nc_max, ml, po, dev_err, stream)
+                : launch_partial<128, false>(tk, tv, q, Hq, Hkv, scale, num_pages, block_table, max_blocks,
+                                             ctx_start, cu_rows, S, R, max_kv_len, nc_max, ml, po, dev_err, stream);
+    else
+        st = bf ? launch_partial<64, true>(tk, tv, q, Hq, Hkv, scale, num_pages, block_table, max_blocks, ctx_start,
+                                           cu_rows, S, R, max_kv_len, nc_max, ml, po, dev_err, stream)
+                : launch_partial<64, false>(tk, tv, q, Hq, Hkv, scale, num_pages, block_table, max_blocks, ctx_start,
+                                            cu_rows, S, R, max_kv_len, nc_max, ml, po, dev_err, stream);
+    if (st != SPEC_OK) return st;
+    const int warps = R * Hq;
+    dim3 grid((warps + 3) / 4);
+    const bool obf = (out_dt == SPEC_BF16);
+    if (D == 128) {
+        if (obf)
+            attn_combine_kernel<128, true><<<grid, 128, 0, stream>>>(ctx_start, cu_rows, S, R, Hq, nc_max, ml, po, out,
+                                                                     max_kv_len);
+        else
+            attn_combine_kernel<128, false><<<grid, 128, 0, stream>>>(ctx_start, cu_rows, S, R, Hq, nc_max, ml, po,
+                                                                      out, max_kv_len);
+    } else {
+        if (obf)
+            attn_combine_kernel<64, true><<<grid, 128, 0, stream>>>(ctx_start, cu_rows, S, R, Hq, nc_max, ml, po, out,
+                                                                    max_kv_len);
+        else
+            attn_combine_kernel<64, false><<<grid, 128, 0, stream>>>(ctx_start, cu_rows, S, R, Hq, nc_max, ml, po, out,
+                                                                     max_kv_len);
+    }
+    return cuda_status(cudaGetLastError(), "attn combine launch");
+}
+
+spec_status attn_check(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, const void *k_cache,
+                       const void *v_cache, int num_pages, const int32_t *block_table, int max_blocks,
+                       const int32_t *ctx_start, const int32_t *cu_rows, int S, int R, int max_kv_len, const void *out,
+                       spec_dtype out_dt) {
+    SPEC_CHECK_ARG(qkv_dt == SPEC_F16 || qkv_dt == SPEC_BF16, "flash_decode: qkv_dt must be SPEC_F16 or SPEC_BF16");
+    SPEC_CHECK_ARG(out_dt == SPEC_F32 || out_dt == SPEC_BF16, "flash_decode: out_dt must be SPEC_F32 or SPEC_BF16");
+    SPEC_CHECK_ARG(D == 64 || D == 128, "flash_decode: D must be 64 or 128 (D=%d)", D);
+    SPEC_CHECK_ARG(Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0 && Hq / Hkv <= 16,
+                   "flash_decode: need Hq %% Hkv == 0 and Hq / Hkv <= 16 (Hq=%d Hkv=%d)", Hq, Hkv);
+    SPEC_CHECK_ARG(S >= 0 && R >= 0 && num_pages >= 1 && max_blocks >= 1 && max_kv_len >= 1,
+                   "flash_decode: bad sizes (S=%d R=%d num_pages=%d max_blocks=%d max_kv_len=%d)", S, R, num_pages,
+                   max_blocks, max_kv_len);
+    SPEC_CHECK_ARG(S <= 65535 && Hkv <= 65535, "flash_decode: S and Hkv must be <= 65535");
+    SPEC_CHECK_ARG(q && k_cache && v_cache && block_table && ctx_start && cu_rows && out, "flash_decode: NULL pointer");
+    SPEC_CHECK_ARG(aligned16(q) && aligned16(k_cache) && aligned16(v_cache),
+                   "flash_decode: q, k_cache and v_cache must be 16-byte aligned");
+    return SPEC_OK;
+}
+}  // namespace spec
+
+extern "C" size_t spec_flash_decode_workspace(int R, int Hq, int D, int max_kv_len) {
+    if (R <= 0 || Hq <= 0 || D <= 0 || max_kv_len <= 0) return 0;
+    return spec::attn_workspace_bytes(R, Hq, D, max_kv_len);
+}
+
+extern "C" spec_status spec_flash_decode(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, float scale,
+                                         const void *k_cache, const void *v_cache, int num_pages,
+                                         const int32_t *block_table, int max_blocks, const int32_t *ctx_start,
+                                         const int32_t *cu_rows, int S, int R, int max_kv_len, void *out,
+                                         spec_dtype out_dt, void *workspace, size_t ws_bytes, int32_t *dev_err,
+                                         spec_stream_t stream) {
+    spec_status st = spec::attn_check(q, qkv_dt, Hq, Hkv, D, k_cache, v_cache, num_pages, block_table, max_blocks,
+                                      ctx_start, cu_rows, S, R, max_kv_len, out, out_dt);
+    if (st != SPEC_OK) return st;
+    if (S == 0 || R == 0) return SPEC_OK;
+    const size_t need = spec::attn_workspace_bytes(R, Hq, D, max_kv_len);
+    if (!workspace || ws_bytes < need || !spec::aligned16(workspace))
+        return spec::fail(SPEC_ERR_WORKSPACE, "flash_decode: workspace needs %zu bytes (16-byte aligned), got %zu",
+                          need, ws_bytes);
+    return spec::attn_run(q, qkv_dt, Hq, Hkv, D, scale, k_cache, v_cache, num_pages, block_table, max_blocks,
+                          ctx_start, cu_rows, S, R, max_kv_len, out, out_dt, workspace, dev_err,
+                          (cudaStream_t)stream);
+}

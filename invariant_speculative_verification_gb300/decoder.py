@@ -1,0 +1,214 @@
+"""End-to-end greedy generation on a random-init decoder, driven entirely by
+libspec kernels: the target forward (int4 linears, RMSNorm, RoPE, paged
+attention, SwiGLU), greedy verification, KV realignment, n-gram drafting and
+the history update all run on the device; one speculative step needs no host
+round trip and is captured in a CUDA graph.
+
+The model is the workload's stand-in: the pages run real decoders with real
+weights, which are out of reach here (ramgpt.org, "When Lossless Speculation
+Stops Being Lossless on Blackwell", section "Why Tiny Numerical Differences Can
+Change Entire Answers": byte-identical speculative vs non-speculative output is
+the user-facing test).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+def _dev(a: np.ndarray, device) -> torch.Tensor:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a.copy()).to(device)
+
+
+class Decoder:
+    """Device-resident decoder: weights, paged KV cache, activation buffers.
+
+    ``weights`` is a ``synth.DecoderWeights``-like object (cfg, emb, layers, lm,
+    final_norm) in storage formats.  Each sequence owns max_len / 16 private
+    pages; the block table is contiguous per sequence.
+    """
+
+    def __init__(self, weights, n_seqs: int, max_len: int, max_rows: int, device="cuda"):
+        cfg = weights.cfg
+        self.cfg, self.S, self.device = cfg, n_seqs, device
+        self.H, self.Hq, self.Hkv, self.D, self.F, self.V = (cfg.hidden, cfg.heads, cfg.kv_heads, cfg.head_dim,
+                                                             cfg.ffn, cfg.vocab)
+        self.nqkv = (self.Hq + 2 * self.Hkv) * self.D
+        self.max_len = max_len
+        self.max_blocks = (max_len + 15) // 16
+        self.pages = n_seqs * self.max_blocks
+        self.emb = _dev(weights.emb, device)
+        self.layers = []
+        for lay in weights.layers:
+            self.layers.append({k: (tuple(_dev(a, device) for a in v) if isinstance(v, tuple) else _dev(v, device))
+                                for k, v in lay.items()})
+        self.lm = tuple(_dev(a, device) for a in weights.lm)
+        self.final_norm = _dev(weights.final_norm, device)
+        self.block_table = torch.arange(self.pages, dtype=torch.int32, device=device).view(n_seqs, self.max_blocks)
+        shape = (self.pages, self.Hkv, 16, self.D)
+        self.k_cache = [torch.zeros(shape, dtype=torch.int16, device=device) for _ in range(cfg.layers)]
+        self.v_cache = [torch.zeros(shape, dtype=torch.int16, device=device) for _ in range(cfg.layers)]
+        self.rope = torch.empty((max_len, self.D // 2, 2), dtype=torch.float32, device=device)
+        L.spec_rope_table(self.rope, max_len, self.D, cfg.rope_theta)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=device)
+        self._alloc(max_rows)
+
+    def _alloc(self, R):
+        d, H, F = self.device, self.H, self.F
+        self.max_rows = R
+        self.h = torch.zeros((R, H), dtype=torch.float32, device=d)
+        self.a = torch.zeros((R, max(H, F)), dtype=torch.int16, device=d)
+        self.qkv = torch.zeros((R, self.nqkv), dtype=torch.float32, device=d)
+        self.q = torch.zeros((R, self.Hq, self.D), dtype=torch.int16, device=d)
+        self.attn = torch.zeros((R, self.Hq * self.D), dtype=torch.int16, device=d)
+        self.gu = torch.zeros((R, 2 * F), dtype=torch.float32, device=d)
+        self.logits = torch.zeros((R, self.V), dtype=torch.float32, device=d)
+        self.ws_bytes = L.spec_flash_decode_workspace(R, self.Hq, self.D, self.max_len)
+        self.attn_ws = torch.empty(self.ws_bytes // 4 + 64, dtype=torch.float32, device=d)
+
+    # ------------------------------------------------------------------
+    def embed(self, tokens, R):
+        L.spec_embed(self.emb, self.V, self.H, tokens, R, self.h, self.dev_err)
+
+    def layer(self, li, R, cu_rows, ctx, S, max_kv_len=None):
+        lay, H, F, D = self.layers[li], self.H, self.F, self.D
+        max_kv_len = max_kv_len or self.max_len
+        L.spec_add_rmsnorm(self.h, None, lay["norm1"], R, H, self.cfg.eps, self.a)
+        L.spec_qmatmul(lay["qkv"][0], lay["qkv"][1], self.nqkv, H, self.a, R, self.a.shape[1], self.qkv, L.SPEC_F32,
+                       self.nqkv, 0, self.dev_err)
+        L.spec_rope_append(self.qkv, R, self.Hq, self.Hkv, D, self.rope, self.max_len, cu_rows, ctx, S, self.q,
+                           self.k_cache[li], self.v_cache[li], self.pages, self.block_table, self.max_blocks,
+                           None, None, self.dev_err)
+        L.spec_flash_decode(self.q, L.SPEC_BF16, self.Hq, self.Hkv, D, 1.0 / math.sqrt(D), self.k_cache[li],
+                            self.v_cache[li], self.pages, self.block_table, self.max_blocks, ctx, cu_rows, S, R,
+                            max_kv_len, self.attn, L.SPEC_BF16, self.attn_ws, self.ws_bytes, self.dev_err)
+        L.spec_qmatmul(lay["o"][0], lay["o"][1], H, self.Hq * D, self.attn, R, self.Hq * D, self.h, L.SPEC_F32, H, 1,
+                       self.dev_err)
+        L.spec_add_rmsnorm(self.h, None, lay["norm2"], R, H, self.cfg.eps, self.a)
+        L.spec_qmatmul(lay["gu"][0], lay["gu"][1], 2 * F, H, self.a, R, self.a.shape[1], self.gu, L.SPEC_F32, 2 * F,
+                       0, self.dev_err)
+        L.spec_swiglu(self.gu, R, F, self.a)
+        L.spec_qmatmul(lay["down"][0], lay["down"][1], H, F, self.a, R, self.a.shape[1], self.h, L.SPEC_F32, H, 1,
+                       self.dev_err)
+
+    def head(self, R):
+        L.spec_add_rmsnorm(self.h, None, self.final_norm, R, self.H, self.cfg.eps, self.a)
+        L.spec_qmatmul(self.lm[0], self.lm[1], self.V, self.H, self.a, R, self.a.shape[1], self.logits, L.SPEC_F32,
+                       self.V, 0, self.dev_err)
+
+    def forward(self, tokens, cu_rows, ctx, S, R, max_kv_len=None):
+        """Logits (fp32 [R][V], in self.logits) for a ragged verify batch whose rows
+        sit at positions ctx[s] + i; writes the rows' K/V into the cache."""
+        assert R <= self.max_rows
+        self.embed(tokens, R)
+        for li in range(self.cfg.layers):
+            self.layer(li, R, cu_rows, ctx, S, max_kv_len)
+        self.head(R)
+        return self.logits[:R]
+
+
+def max_len_for(P: int, n_new: int, W: int) -> int:
+    """KV positions a Generator needs for prompts of P tokens, n_new new tokens and W drafts."""
+    return P + (n_new + 1) * (W + 1) + 2 * W + 16
+
+
+class Generator:
+    """Greedy generation for S sequences, W drafts per step (W = 0: ordinary
+    width-1 decoding).  All per-step state lives on the device."""
+
+    def __init__(self, dec: Decoder, prompts: np.ndarray, W: int, pads: np.ndarray, n_new: int):
+        self.dec, self.W = dec, W
+        S, P = prompts.shape
+        assert S == dec.S
+        d = dec.device
+        self.S, self.P, self.n_new = S, P, n_new
+        # a sequence may gain W + 1 tokens per step while the slowest gains one
+        self.cap = P + (n_new + 1) * (W + 1) + 8
+        assert dec.max_len >= self.cap + W + 1, "decoder max_len too small for this generation"
+        self.R = S * (W + 1)
+        hist = np.zeros((S, self.cap), np.int32)
+        hist[:, :P] = prompts
+        self.hist = torch.from_numpy(hist).to(d)
+        self.hist_len = torch.full((S,), P, dtype=torch.int32, device=d)
+        self.ctx = torch.full((S,), P - 1, dtype=torch.int32, device=d)
+        self.ctx_new = torch.zeros(S, dtype=torch.int32, device=d)
+        self.cu = torch.arange(0, self.R + 1, W + 1, dtype=torch.int32, device=d)
+        self.block = torch.zeros(self.R, dtype=torch.int32, device=d)
+        self.drafts = torch.zeros(max(S * W, 1), dtype=torch.int32, device=d)
+        self.argmax = torch.zeros(self.R, dtype=torch.int32, device=d)
+        self.accepted = torch.zeros(S, dtype=torch.int32, device=d)
+        self.correction = torch.zeros(S, dtype=torch.int32, device=d)
+        self.cu_kept = torch.zeros(S + 1, dtype=torch.int32, device=d)
+        self.kept_src = torch.zeros(self.R, dtype=torch.int32, device=d)
+        self.dst_slot = torch.zeros(self.R, dtype=torch.int64, device=d)
+        self.vws_bytes = L.spec_verify_greedy_workspace(self.R, dec.V)
+        self.vws = torch.empty(self.vws_bytes // 8 + 2, dtype=torch.int64, device=d)
+        self.pads = torch.from_numpy(np.ascontiguousarray(pads, np.int32)).to(d)   # [n_pad][S][W]
+        self.pad_step = torch.zeros((S, max(W, 1)), dtype=torch.int32, device=d)
+        self.steps = 0
+        self.graph = None
+        # prefill the first P-1 prompt tokens of every sequence (same kernels, one ragged batch)
+        pre = torch.from_numpy(np.ascontiguousarray(prompts[:, :P - 1].reshape(-1), np.int32)).to(d)
+        cu = torch.arange(0, S * (P - 1) + 1, P - 1, dtype=torch.int32, device=d)
+        zero = torch.zeros(S, dtype=torch.int32, device=d)
+        dec.forward(pre, cu, zero, S, S * (P - 1))
+
+    def _step_body(self):
+        dec, W, S, R = self.dec, self.W, self.S, self.R
+        L.spec_ngram_draft(self.hist, self.cap, self.hist_len, S, W, self.pad_step, self.drafts, None, self.block)
+        logits = dec.forward(self.block, self.cu, self.ctx, S, R)
+        L.spec_verify_greedy(logits, L.SPEC_F32, dec.V, self.cu, S, R, self.drafts if W else None, self.ctx,
+                             self.argmax, self.accepted, self.correction, self.ctx_new, self.vws, self.vws_bytes,
+                             dec.dev_err)
+        # the block's K/V were written into the cache in place: realignment is index-only
+        L.spec_kv_compact(None, None, None, None, dec.Hkv, dec.D, dec.pages, dec.block_table, dec.max_blocks,
+                          self.ctx, self.accepted, self.cu, S, R, self.cu_kept, self.kept_src, self.dst_slot,
+                          dec.dev_err)
+        L.spec_commit_accepted(self.hist, self.cap, self.hist_len, self.drafts, W, self.accepted, self.correction,
+                               self.ctx_new, self.ctx, S, dec.dev_err)
+
+    def set_pads(self, step):
+        if self.W:
+            self.pad_step.copy_(self.pads[step % self.pads.shape[0]])
+
+    def step(self, use_graph=False):
+        self.set_pads(self.steps)
+        if use_graph and self.steps > 0:
+            # the first step runs eagerly, so every kernel is configured before capture
+            if self.graph is None:
+                self._capture()
+            self.graph.replay()
+        else:
+            self._step_body()
+        self.steps += 1
+
+    def _capture(self):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        # every call in the step is capture-safe: no allocation, no synchronisation
+        with torch.cuda.graph(g, stream=s):
+            self._step_body()
+        torch.cuda.current_stream().wait_stream(s)
+        self.graph = g
+
+    def done(self) -> bool:
+        return int(self.hist_len.min().item()) >= self.P + self.n_new
+
+    def run(self, use_graph=False, max_steps=None):
+        max_steps = max_steps or (self.n_new + 1)
+        while not self.done() and self.steps < max_steps:
+            self.step(use_graph)
+        torch.cuda.synchronize()
+        return self.tokens()
+
+    def tokens(self) -> np.ndarray:
+        h = self.hist.cpu().numpy()
+        return h[:, self.P:self.P + self.n_new]

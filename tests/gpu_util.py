@@ -1,0 +1,42 @@
+"""Small helpers shared by the GPU tests: numpy <-> device tensors (same bytes)."""
+import numpy as np
+import torch
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    """Upload a numpy array to cuda:0 keeping its bytes (uint16 -> int16, uint8 -> uint8)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    elif a.dtype == np.uint32:
+        a = a.view(np.int32)
+    elif a.dtype == np.uint64:
+        a = a.view(np.int64)
+    return torch.from_numpy(a.copy()).to("cuda")
+
+
+def host(t: torch.Tensor, dtype=None) -> np.ndarray:
+    a = t.detach().cpu().numpy()
+    if dtype is not None:
+        a = a.view(dtype)
+    return a
+
+
+def bits_equal(a: torch.Tensor, b: torch.Tensor) -> bool:
+    """Bitwise equality of two tensors of the same shape and dtype."""
+    if a.shape != b.shape or a.dtype != b.dtype:
+        return False
+    ai = a.contiguous().view(torch.int32) if a.element_size() == 4 else a.contiguous().view(torch.int16)
+    bi = b.contiguous().view(torch.int32) if b.element_size() == 4 else b.contiguous().view(torch.int16)
+    return bool(torch.equal(ai, bi))
+
+
+def rel_err_rows(got: np.ndarray, ref: np.ndarray) -> float:
+    """max over rows of max|got - ref| / max|ref| of that row (rows = last axis vectors)."""
+    got = got.reshape(-1, got.shape[-1]).astype(np.float64)
+    ref = ref.reshape(-1, ref.shape[-1]).astype(np.float64)
+    scale = np.maximum(np.abs(ref).max(axis=1), 1e-30)
+    return float((np.abs(got - ref).max(axis=1) / scale).max())
+
+
+TOL = 2e-3  # max abs error relative to the output row's max-abs (fp32-accumulated 16-bit math)

@@ -1,0 +1,88 @@
+"""The C ABI library builds, loads without a GPU, exports every symbol the
+header declares, and rejects bad arguments on the host before touching the
+device."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "spec.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    import invariant_speculative_verification_gb300 as L
+    lib = L.load()
+    names = declared_functions()
+    assert len(names) >= 15
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    import invariant_speculative_verification_gb300 as L
+    lib = L.load()
+    assert lib.spec_status_string(0) == b"SPEC_OK"
+    assert lib.spec_status_string(3) == b"SPEC_ERR_WORKSPACE"
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-NULL pointer value; never dereferenced by the host checks
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(K=100), "K >= 256"),
+    (dict(K=512 + 32), "multiple of 256"),
+    (dict(ldx=500), "ldx"),
+    (dict(x=FAKE + 4), "16-byte aligned"),
+    (dict(y_dt=1), "y_dt"),
+])
+def test_qmatmul_host_validation(kw, msg):
+    import invariant_speculative_verification_gb300 as L
+    a = dict(wq=FAKE, ws=FAKE, N=64, K=512, x=FAKE, n_cols=1, ldx=512, y=FAKE, y_dt=0, ldy=64)
+    a.update(kw)
+    if "ldx" not in kw:
+        a["ldx"] = max(a["K"], 8) if a["K"] % 8 == 0 else 512
+    with pytest.raises(L.SpecError) as e:
+        L.spec_qmatmul(a["wq"], a["ws"], a["N"], a["K"], a["x"], a["n_cols"], a["ldx"], a["y"], a["y_dt"], a["ldy"],
+                       stream=0)
+    assert msg in str(e.value) and e.value.status == 1
+
+
+def test_flash_decode_host_validation_and_workspace():
+    import invariant_speculative_verification_gb300 as L
+    ws = L.spec_flash_decode_workspace(10, 8, 128, 1000)
+    assert ws >= 10 * 8 * 4 * (128 + 2) * 4
+    args = [FAKE, 2, 8, 2, 128, 1.0, FAKE, FAKE, 16, FAKE, 8, FAKE, FAKE, 2, 10, 1000, FAKE, 0, FAKE, ws]
+    bad_d = list(args)
+    bad_d[4] = 96
+    with pytest.raises(L.SpecError, match="D must be"):
+        L.spec_flash_decode(*bad_d, stream=0)
+    bad_g = list(args)
+    bad_g[3] = 3
+    with pytest.raises(L.SpecError, match="Hq"):
+        L.spec_flash_decode(*bad_g, stream=0)
+    short = list(args)
+    short[19] = ws - 1
+    with pytest.raises(L.SpecError) as e:
+        L.spec_flash_decode(*short, stream=0)
+    assert e.value.status == 3
+
+
+def test_verify_and_compact_host_validation():
+    import invariant_speculative_verification_gb300 as L
+    with pytest.raises(L.SpecError, match="multiple of 8"):
+        L.spec_verify_greedy(FAKE, 0, 1001, FAKE, 2, 10, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, stream=0)
+    with pytest.raises(L.SpecError, match="both or neither"):
+        L.spec_kv_compact(FAKE, None, FAKE, FAKE, 8, 128, 16, FAKE, 8, FAKE, FAKE, FAKE, 2, 10, FAKE, FAKE, FAKE,
+                          stream=0)
+
+
+def test_zero_sized_calls_launch_nothing():
+    import invariant_speculative_verification_gb300 as L
+    L.spec_qmatmul(FAKE, FAKE, 64, 512, FAKE, 0, 512, FAKE, 0, 64, stream=0)
+    L.spec_verify_greedy(FAKE, 0, 1000, FAKE, 0, 0, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, stream=0)

@@ -1,0 +1,144 @@
+"""K1 (spec_qmatmul): parity with the oracle and bit-exact batch invariance.
+
+Batch invariance test shape from ramgpt.org, "When Lossless Speculation Stops
+Being Lossless on Blackwell", sections "Quantized Matrix Multiplication Shows
+the Same Class of Failure" (batched product vs a sequence of single-column
+products) and "A Better Backend Test Matrix" (widths 2, 3, 4, 5 and 8).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_util import TOL, bits_equal, dev, host, rel_err_rows
+
+pytestmark = pytest.mark.gpu
+
+WIDTHS = [1, 2, 3, 4, 5, 8]
+
+
+def _lib():
+    import invariant_speculative_verification_gb300 as L
+    return L
+
+
+def run(case_or_w, x_dev, n_cols, N, K, ldx=None, out_dt=0, y=None, accumulate=0, ldy=None):
+    L = _lib()
+    wq, ws = case_or_w
+    ldx = K if ldx is None else ldx
+    ldy = N if ldy is None else ldy
+    if y is None:
+        y = torch.zeros((max(n_cols, 1), ldy), dtype=torch.float32 if out_dt == 0 else torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.spec_qmatmul(wq, ws, N, K, x_dev, n_cols, ldx, y, out_dt, ldy, accumulate, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return y
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    case = synth.qmatmul_case(1001, 512, 512, 8)
+    return case, (dev(case.wq), dev(case.ws)), dev(case.x)
+
+
+def test_parity_tiny_all_widths(tiny):
+    case, w, x = tiny
+    ref = oracle.qmatmul(case.wq, case.ws, case.x, 512, 512)
+    for n in WIDTHS:
+        y = run(w, x, n, 512, 512)
+        assert rel_err_rows(host(y)[:n], ref[:n]) <= TOL
+
+
+def test_width_n_equals_n_width1_calls_bitwise(tiny):
+    case, w, x = tiny
+    singles = torch.cat([run(w, x[j:j + 1], 1, 512, 512) for j in range(8)])
+    for n in range(1, 9):
+        y = run(w, x, n, 512, 512)
+        assert bits_equal(y[:n], singles[:n]), f"width {n}"
+
+
+@pytest.mark.parametrize("N,K", [(200, 768), (1000, 2048), (96, 5120), (130, 17408)])
+def test_ragged_rows_and_ksplits_parity_and_invariance(N, K):
+    case = synth.qmatmul_case(7000 + N, N, K, 5)
+    w, x = (dev(case.wq), dev(case.ws)), dev(case.x)
+    y = run(w, x, 5, N, K)
+    ref = oracle.qmatmul(case.wq, case.ws, case.x, N, K)
+    assert rel_err_rows(host(y), ref) <= TOL
+    for j in range(5):
+        assert bits_equal(run(w, x[j:j + 1], 1, N, K)[0], y[j])
+
+
+def test_column_placement_and_tile_width_do_not_change_bits(tiny):
+    case, w, x = tiny
+    L = _lib()
+    probe = x[3:4]
+    ref = run(w, probe, 1, 512, 512)[0]
+    g = np.random.default_rng(5)
+    for n_cols in (8, 16, 37, 80):
+        xs = dev(synth.activations_bf16(int(g.integers(1 << 30)), n_cols, 512))
+        for pos in sorted({0, n_cols // 2, n_cols - 1, min(7, n_cols - 1)}):
+            xs[pos] = probe[0]
+            y = run(w, xs, n_cols, 512, 512)
+            assert bits_equal(y[pos], ref), (n_cols, pos)
+            for nt in (1, 2, 4):
+                yy = torch.zeros((n_cols, 512), dtype=torch.float32, device="cuda")
+                L.spec_qmatmul_debug_nt(w[0], w[1], 512, 512, xs, n_cols, 512, yy, 512, nt)
+                torch.cuda.synchronize()
+                assert bits_equal(yy, y), (n_cols, nt)
+
+
+def test_padding_columns_and_ldx_do_not_leak(tiny):
+    case, w, x = tiny
+    ldx = 640
+    xp = torch.full((3, ldx), 0x7FC0, dtype=torch.int16, device="cuda")  # NaN in the padding
+    xp[:, :512] = x[:3]
+    y = run(w, xp, 3, 512, 512, ldx=ldx)
+    assert torch.isfinite(y).all()
+    assert bits_equal(y, run(w, x[:3], 3, 512, 512))
+
+
+def test_bf16_output_and_accumulate(tiny):
+    case, w, x = tiny
+    y32 = run(w, x, 4, 512, 512)
+    ybf = run(w, x, 4, 512, 512, out_dt=2)
+    assert torch.equal(ybf, y32.to(torch.bfloat16))
+    base = torch.randn(4, 512, device="cuda")
+    acc = base.clone()
+    run(w, x, 4, 512, 512, y=acc, accumulate=1)
+    assert bits_equal(acc, base + y32)
+
+
+def test_zero_columns_is_a_noop(tiny):
+    case, w, x = tiny
+    y = torch.full((1, 512), 7.0, device="cuda")
+    run(w, x, 0, 512, 512, y=y)
+    assert bool((y == 7.0).all())
+
+
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408), (5120, 5120)])
+def test_dense_sweep_shapes_sampled_parity_and_invariance(N, K):
+    """Full-size shapes of a 27B-class decoder: parity on sampled output rows,
+    bitwise width-n == n width-1 calls on every output."""
+    case = synth.qmatmul_case(1002 + K % 97, N, K, 8)
+    w, x = (dev(case.wq), dev(case.ws)), dev(case.x)
+    singles = torch.cat([run(w, x[j:j + 1], 1, N, K) for j in range(8)])
+    for n in WIDTHS:
+        y = run(w, x, n, N, K)
+        assert bits_equal(y[:n], singles[:n]), f"width {n}"
+    rows = np.random.default_rng(3).choice(N, 48, replace=False)
+    ref = oracle.qmatmul_rows(case.wq, case.ws, case.x, K, rows)      # [8][48]
+    got = host(singles)[:, rows]
+    full_scale = np.abs(host(singles)).max(axis=1, keepdims=True)     # row max over all N outputs
+    assert float((np.abs(got - ref) / full_scale).max()) <= TOL
+
+
+def test_noninvariant_variant_matches_oracle(tiny):
+    case, w, x = tiny
+    L = _lib()
+    y = torch.zeros((8, 512), dtype=torch.float32, device="cuda")
+    L.spec_qmatmul_noninvariant(w[0], w[1], 512, 512, x, 8, 512, y, 512)
+    torch.cuda.synchronize()
+    ref = oracle.qmatmul(case.wq, case.ws, case.x, 512, 512)
+    assert rel_err_rows(host(y), ref) <= TOL
