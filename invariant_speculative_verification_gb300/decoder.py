@@ -64,7 +64,8 @@ class Decoder:
         d, H, F = self.device, self.H, self.F
         self.max_rows = R
         self.h = torch.zeros((R, H), dtype=torch.float32, device=d)
-        self.a = torch.zeros((R, max(H, F)), dtype=torch.int16, device=d)
+        self.a = torch.zeros((R, H), dtype=torch.int16, device=d)       # normed rows entering a matmul
+        self.act = torch.zeros((R, F), dtype=torch.int16, device=d)     # SwiGLU output rows
         self.qkv = torch.zeros((R, self.nqkv), dtype=torch.float32, device=d)
         self.q = torch.zeros((R, self.Hq, self.D), dtype=torch.int16, device=d)
         self.attn = torch.zeros((R, self.Hq * self.D), dtype=torch.int16, device=d)
@@ -81,7 +82,7 @@ class Decoder:
         lay, H, F, D = self.layers[li], self.H, self.F, self.D
         max_kv_len = max_kv_len or self.max_len
         L.spec_add_rmsnorm(self.h, None, lay["norm1"], R, H, self.cfg.eps, self.a)
-        L.spec_qmatmul(lay["qkv"][0], lay["qkv"][1], self.nqkv, H, self.a, R, self.a.shape[1], self.qkv, L.SPEC_F32,
+        L.spec_qmatmul(lay["qkv"][0], lay["qkv"][1], self.nqkv, H, self.a, R, H, self.qkv, L.SPEC_F32,
                        self.nqkv, 0, self.dev_err)
         L.spec_rope_append(self.qkv, R, self.Hq, self.Hkv, D, self.rope, self.max_len, cu_rows, ctx, S, self.q,
                            self.k_cache[li], self.v_cache[li], self.pages, self.block_table, self.max_blocks,
@@ -92,15 +93,15 @@ class Decoder:
         L.spec_qmatmul(lay["o"][0], lay["o"][1], H, self.Hq * D, self.attn, R, self.Hq * D, self.h, L.SPEC_F32, H, 1,
                        self.dev_err)
         L.spec_add_rmsnorm(self.h, None, lay["norm2"], R, H, self.cfg.eps, self.a)
-        L.spec_qmatmul(lay["gu"][0], lay["gu"][1], 2 * F, H, self.a, R, self.a.shape[1], self.gu, L.SPEC_F32, 2 * F,
+        L.spec_qmatmul(lay["gu"][0], lay["gu"][1], 2 * F, H, self.a, R, H, self.gu, L.SPEC_F32, 2 * F,
                        0, self.dev_err)
-        L.spec_swiglu(self.gu, R, F, self.a)
-        L.spec_qmatmul(lay["down"][0], lay["down"][1], H, F, self.a, R, self.a.shape[1], self.h, L.SPEC_F32, H, 1,
+        L.spec_swiglu(self.gu, R, F, self.act)
+        L.spec_qmatmul(lay["down"][0], lay["down"][1], H, F, self.act, R, F, self.h, L.SPEC_F32, H, 1,
                        self.dev_err)
 
     def head(self, R):
         L.spec_add_rmsnorm(self.h, None, self.final_norm, R, self.H, self.cfg.eps, self.a)
-        L.spec_qmatmul(self.lm[0], self.lm[1], self.V, self.H, self.a, R, self.a.shape[1], self.logits, L.SPEC_F32,
+        L.spec_qmatmul(self.lm[0], self.lm[1], self.V, self.H, self.a, R, self.H, self.logits, L.SPEC_F32,
                        self.V, 0, self.dev_err)
 
     def forward(self, tokens, cu_rows, ctx, S, R, max_kv_len=None):
