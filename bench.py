@@ -162,6 +162,8 @@ def qgemv_sweep(torch, L, hbm_peak):
             ws.append(ws[0].clone())
         x = torch.from_numpy(synth.activations_bf16(7, 8, K).view(np.int16)).to(dev)
         y = torch.zeros((8, N), dtype=torch.float32, device=dev)
+        wsb = L.spec_qmatmul_workspace(N, K, 8)
+        wsp = torch.zeros(wsb // 4 + 64, dtype=torch.int32, device=dev)
         res = {}
 
         def timed(n, fn_one, reps=3):
@@ -190,27 +192,32 @@ def qgemv_sweep(torch, L, hbm_peak):
             return best
 
         def inv(i, n):
-            L.spec_qmatmul(wq[i], ws[i], N, K, x, n, K, y, L.SPEC_F32, N, 0, None)
-
-        def noninv(i, n):
-            L.spec_qmatmul_noninvariant(wq[i], ws[i], N, K, x, n, K, y, N)
+            L.spec_qmatmul(wq[i], ws[i], N, K, x, n, K, y, L.SPEC_F32, N, 0, wsp, wsb, None)
 
         for n in SWEEP_WIDTHS:
             t = timed(n, inv)
             algo = 0.5625 * N * K + 2 * n * K + 4 * n * N
             res[str(n)] = {"us": round(t * 1e6, 2), "GBps": round(algo / t / 1e9, 1),
                            "frac": round(algo / t / 1e9 / hbm_peak, 3)}
-        t1n = timed(1, noninv)
+        # the fastest non-invariant variant at width 1: K-segment length picked per call
         algo1 = 0.5625 * N * K + 2 * K + 4 * N
-        res["noninvariant_w1"] = {"us": round(t1n * 1e6, 2), "GBps": round(algo1 / t1n / 1e9, 1)}
+        best = None
+        for seg in (0, 1, 2, 4, 8):
+            def noninv(i, n, _seg=seg):
+                L.spec_qmatmul_noninvariant(wq[i], ws[i], N, K, x, n, K, y, N, _seg, wsp, wsb)
+            tn = timed(1, noninv)
+            if best is None or tn < best[0]:
+                best = (tn, seg)
+        res["noninvariant_w1"] = {"us": round(best[0] * 1e6, 2), "GBps": round(algo1 / best[0] / 1e9, 1),
+                                  "seg_stages": best[1]}
         res["w1_vs_noninvariant"] = round(res["1"]["us"] / res["noninvariant_w1"]["us"], 3)
         # bitwise invariance: width n == n width-1 calls
         singles = torch.zeros((8, N), dtype=torch.float32, device=dev)
         for j in range(8):
-            L.spec_qmatmul(wq[0], ws[0], N, K, x[j:j + 1], 1, K, singles[j:j + 1], L.SPEC_F32, N, 0, None)
+            L.spec_qmatmul(wq[0], ws[0], N, K, x[j:j + 1], 1, K, singles[j:j + 1], L.SPEC_F32, N, 0, wsp, wsb, None)
         for n in range(1, 9):
             yy = torch.zeros((n, N), dtype=torch.float32, device=dev)
-            L.spec_qmatmul(wq[0], ws[0], N, K, x, n, K, yy, L.SPEC_F32, N, 0, None)
+            L.spec_qmatmul(wq[0], ws[0], N, K, x, n, K, yy, L.SPEC_F32, N, 0, wsp, wsb, None)
             torch.cuda.synchronize()
             inv_cases += 1
             inv_pass += int(torch.equal(yy.view(torch.int32), singles[:n].view(torch.int32)))
@@ -427,10 +434,12 @@ def qmatmul_step_roofline(torch, L, w, hbm_peak, peak_kind):
     x = torch.from_numpy(synth.activations_bf16(3, n, max(H, F)).view(np.int16)).to(dev)
     y = torch.zeros((n, cfg.vocab), dtype=torch.float32, device=dev)
     algo = sum(0.5625 * N * K + 2 * n * K + 4 * n * N for _, _, N, K in mats)
+    wsb = max(L.spec_qmatmul_workspace(N, K, n) for _, _, N, K in mats)
+    wsp = torch.zeros(wsb // 4 + 64, dtype=torch.int32, device=dev)
 
     def body():
         for wq, ws, N, K in mats:
-            L.spec_qmatmul(wq, ws, N, K, x, n, x.shape[1], y, L.SPEC_F32, N, 0, None)
+            L.spec_qmatmul(wq, ws, N, K, x, n, x.shape[1], y, L.SPEC_F32, N, 0, wsp, wsb, None)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())

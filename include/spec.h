@@ -89,22 +89,41 @@ const char *spec_last_error(void);
  *   x    bf16 bits [n_cols][ldx], ldx >= K, ldx % 8 == 0, 16-byte aligned.
  *   y    [n_cols][ldy] of y_dt (SPEC_F32 or SPEC_BF16), ldy >= N.
  *        accumulate != 0 adds into y (SPEC_F32 only): y = fp32(y + result).
+ *   workspace  at least spec_qmatmul_workspace(N, K, n_cols) bytes, 16-byte
+ *        aligned, zero-filled before its first use (cudaMemset once).  Every
+ *        call that returns SPEC_OK and reports no SPEC_DEVERR_TIMEOUT leaves it
+ *        zero-filled again, so one workspace serves any sequence of calls on
+ *        one stream; calls that overlap on the GPU need separate workspaces.
  *   K % 256 == 0, N >= 1, n_cols >= 0 (0 launches nothing).
+ *   The kernel is launched with programmatic dependent launch: it may start
+ *   reading wq and ws while the preceding kernel on the stream is still
+ *   running (weights are treated as constant inputs); x, y and the workspace
+ *   are touched only after that kernel has finished.
+ *
+ * Arithmetic of one output element (fixed by K): K is cut into segments of
+ * 512 (the last may be 256); within a segment each 32-k block's partial is
+ * one chain of two m16n8k16 MMAs, scaled by its fp16 scale into an fp32
+ * accumulator in ascending block order; segment partials are added in
+ * ascending segment order.
  * ---------------------------------------------------------------------- */
+size_t spec_qmatmul_workspace(int N, int K, int n_cols);
 spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
                          const uint16_t *x, int n_cols, int ldx,
                          void *y, spec_dtype y_dt, int ldy, int accumulate,
+                         void *workspace, size_t ws_bytes,
                          int32_t *dev_err, spec_stream_t stream);
 
-/* The same product computed by a kernel whose split of K and whose CTA shape
- * are chosen per call from n_cols and the problem size for speed: NOT batch
- * invariant.  It exists to measure what width-1 speed the invariant kernel
- * gives up (the pages' prior-art kernels pick geometry by width; tokenstrom.com,
- * section "Why the math checks out and the text still flips").  Same argument
- * rules as spec_qmatmul; y_dt must be SPEC_F32 and accumulate 0. */
+/* The same product with a K-segment length of seg_stages x 256 chosen per
+ * call (seg_stages = 0: picked from the problem size and the GPU for speed),
+ * so its reduction order depends on the call: NOT batch invariant.  It exists
+ * to measure what width-1 speed the invariant kernel gives up (the pages'
+ * prior-art kernels pick geometry by width; tokenstrom.com, "'Lossless,' but
+ * not quite", section "Why the math checks out and the text still flips").
+ * Same argument rules as spec_qmatmul; y is fp32, no accumulate. */
 spec_status spec_qmatmul_noninvariant(const uint8_t *wq, const uint16_t *ws, int N, int K,
                                       const uint16_t *x, int n_cols, int ldx,
-                                      float *y, int ldy, spec_stream_t stream);
+                                      float *y, int ldy, int seg_stages,
+                                      void *workspace, size_t ws_bytes, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * K2 + K3  split-KV causal attention for verify blocks (paged KV cache)
@@ -255,11 +274,13 @@ spec_status spec_commit_accepted(int32_t *hist, int hist_cap, int32_t *hist_len,
 
 /* ------------------------------------------------------------------------
  * Test hook: spec_qmatmul with an explicit column-tile width nt in {1, 2, 4}
- * (columns per CTA = 8 nt).  The result of every column must not depend on
+ * (columns per pass = 8 nt; the workspace must hold T * (1 + ceil(K/512))
+ * * 128 * 8 nt floats after 256-byte-rounded T int counters, T = ceil(N/128)).  The result of every column must not depend on
  * nt; the tests use this to show it.  y_dt is SPEC_F32.
  * ---------------------------------------------------------------------- */
 spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,
-                                  int n_cols, int ldx, float *y, int ldy, int nt, spec_stream_t stream);
+                                  int n_cols, int ldx, float *y, int ldy, int nt,
+                                  void *workspace, size_t ws_bytes, spec_stream_t stream);
 
 #ifdef __cplusplus
 }

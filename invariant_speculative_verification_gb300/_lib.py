@@ -31,9 +31,10 @@ _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_s
 _SIGS = {
     "spec_status_string": (ctypes.c_char_p, [_i32]),
     "spec_last_error": (ctypes.c_char_p, []),
-    "spec_qmatmul": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _vp]),
-    "spec_qmatmul_noninvariant": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _vp]),
-    "spec_qmatmul_debug_nt": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _vp]),
+    "spec_qmatmul_workspace": (_sz, [_i32, _i32, _i32]),
+    "spec_qmatmul": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
+    "spec_qmatmul_noninvariant": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _sz, _vp]),
+    "spec_qmatmul_debug_nt": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _sz, _vp]),
     "spec_flash_decode_workspace": (_sz, [_i32, _i32, _i32, _i32]),
     "spec_flash_decode": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32,
                                  _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
@@ -114,19 +115,27 @@ def _dt(t: torch.Tensor) -> int:
 # ---------------------------------------------------------------------------
 # wrappers (names follow the C ABI)
 # ---------------------------------------------------------------------------
-def spec_qmatmul(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate=0, dev_err=None, stream=None):
+def spec_qmatmul_workspace(N, K, n_cols) -> int:
+    return int(load().spec_qmatmul_workspace(N, K, n_cols))
+
+
+def spec_qmatmul(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, workspace, ws_bytes, dev_err=None,
+                 stream=None):
     _check("spec_qmatmul", load().spec_qmatmul(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx, _ptr(y), y_dt, ldy,
-                                               int(accumulate), _ptr(dev_err), _stream(stream)))
+                                               int(accumulate), _ptr(workspace), int(ws_bytes), _ptr(dev_err),
+                                               _stream(stream)))
 
 
-def spec_qmatmul_noninvariant(wq, ws, N, K, x, n_cols, ldx, y, ldy, stream=None):
-    _check("spec_qmatmul_noninvariant", load().spec_qmatmul_noninvariant(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols,
-                                                                         ldx, _ptr(y), ldy, _stream(stream)))
+def spec_qmatmul_noninvariant(wq, ws, N, K, x, n_cols, ldx, y, ldy, seg_stages, workspace, ws_bytes, stream=None):
+    _check("spec_qmatmul_noninvariant", load().spec_qmatmul_noninvariant(
+        _ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx, _ptr(y), ldy, int(seg_stages), _ptr(workspace),
+        int(ws_bytes), _stream(stream)))
 
 
-def spec_qmatmul_debug_nt(wq, ws, N, K, x, n_cols, ldx, y, ldy, nt, stream=None):
+def spec_qmatmul_debug_nt(wq, ws, N, K, x, n_cols, ldx, y, ldy, nt, workspace, ws_bytes, stream=None):
     _check("spec_qmatmul_debug_nt", load().spec_qmatmul_debug_nt(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx,
-                                                                 _ptr(y), ldy, nt, _stream(stream)))
+                                                                 _ptr(y), ldy, nt, _ptr(workspace), int(ws_bytes),
+                                                                 _stream(stream)))
 
 
 def spec_flash_decode_workspace(R, Hq, D, max_kv_len) -> int:

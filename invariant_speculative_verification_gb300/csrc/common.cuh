@@ -180,6 +180,12 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     return v;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue now / wait until the preceding kernel has finished and its writes
+// are visible.  Both are no-ops when the launch did not enable it.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void report(int32_t *dev_err, int32_t bits) {
     if (dev_err) atomicOr(dev_err, bits);
 }

@@ -2,27 +2,37 @@
 //
 //   y[j][n] = sum_k x[j][k] * d[n][k/32] * (nib(n, k) - 8)
 //
-// Why it is width-invariant.  Output element (n, j) is computed as follows and
-// nothing in the sequence depends on how many columns the call has or where
-// column j sits:
-//  * K is cut into `ksplit(K)` segments of whole 256-k stages (a function of
-//    K alone).  Segment s is reduced by CTA rank s of a thread-block cluster.
-//  * Inside a segment, for every 32-k block b in ascending order, one warp
-//    computes the block partial P_b = sum_{k in b} q x with two chained
-//    m16n8k16 bf16 MMAs (C starts at +0), then acc = fma(d_b, P_b, acc).
-//    The MMA instruction stream is identical for every call; column j's value
-//    depends only on A (the weights), on B column j and on C column j.
-//    Unused columns are zero, never a different instruction.
-//  * The cluster's segment partials are summed in ascending rank order.
-// Which CTA, warp or column tile handles column j is a scheduling choice and
-// may depend on n_cols; the arithmetic applied to column j never does.
+// Per-element arithmetic (identical for every call, whatever n_cols is and
+// wherever column j sits):
+//  * K is cut into segments of 512 (when K / 256 is odd the last segment is
+//    256 long).  The cut depends on K only.
+//  * Inside a segment, for every 32-k block b in ascending order, the block
+//    partial P_b is one chain of two m16n8k16 bf16 MMAs whose A operand is the
+//    code c = q + 8 plus 128 (exactly representable) and whose C operand starts
+//    at -136 * sum_{k in b} x[j][k] (column j's block sum in fp32, its four
+//    8-k chunks summed in k order and then in chunk order), so P_b = sum q x up
+//    to MMA rounding; then s = fma(d_b, P_b, s) with s starting at +0.
+//  * The segment sums are folded in ascending order: y = ((s_0 + s_1) + s_2)...
+// The MMA instruction stream is the same for every column tile and column j's
+// result depends only on A, on B column j and on C column j; unused columns
+// are zero, never a different instruction.  Which CTA, warp or column tile
+// handles a column, and where a CTA's share of the work starts and ends, is
+// scheduling that may depend on the call; the arithmetic above never does.
 //
-// Data movement: TMA (cp.async.bulk.tensor) streams, per 256-k stage, a
-// 64-row x 128-byte weight tile (128B swizzle), the 64 x 8 fp16 scales and
-// the 4 x 64-k activation tiles of the CTA's column group into a ring of
-// shared-memory stages guarded by mbarriers; a producer warp issues the
-// copies, four consumer warps (16 rows each) read weights with ldmatrix,
-// dequantise nibbles to bf16 in registers and feed mma.sync.
+// Execution: a persistent grid of one CTA per SM, each with eight consumer
+// warps (16 weight rows each, 128 rows per tile) and one producer warp.  The
+// (128-row tile x K-segment) units are dealt out in equal contiguous ranges
+// (stream-K), so every SM streams the same number of bytes.  The producer's
+// lane 0 issues TMA (cp.async.bulk.tensor) copies of each 512-k stage -- the
+// int4 codes (two 128-row x 128-byte boxes, 128B swizzle) and the fp16 scales
+// -- into a ring of mbarrier-guarded stages; the producer warp reads the
+// stage's activation columns from L2 with vector loads, writes them in the
+// MMA B-fragment order and writes the block sums, so consumers issue only
+// ldmatrix, 4 LOP3 per 8 weights, lds and mma.sync.  A tile covered by one CTA is folded in registers and written
+// directly.  A tile shared by several CTAs is finished through the workspace:
+// the CTA holding its first segment stores its fold so far, the others store
+// their segment sums, and the last CTA to finish (atomic counter) folds the
+// rest in segment order, writes y and resets the counter.
 //
 // The weight format (int4 block 32, fp16 scale, even k in the low nibble) is
 // the stand-in for the block-quantised formats named in ramgpt.org, "When
@@ -32,226 +42,382 @@
 
 namespace {
 
-constexpr int BM = 64;                        // weight rows per CTA
-constexpr int KST = 256;                      // k per pipeline stage
-constexpr int W_BYTES = BM * KST / 2;         // 8192: int4 codes of one stage
-constexpr int S_BYTES = BM * (KST / 32) * 2;  // 1024: fp16 scales of one stage
-constexpr int NCONS = 4;                      // consumer warps
-constexpr int THREADS = (NCONS + 1) * 32;     // + one producer warp
-constexpr int SMEM_BUDGET = 100 * 1024;       // two CTAs per SM
+constexpr int KST = 512;                     // k per stage (= one K-segment on the invariant path)
+constexpr int SEG_ST = 1;                    // stages per K-segment (invariant path)
+constexpr int BM = 128;                      // weight rows per tile
+constexpr int NCW = 8;                       // consumer warps (16 rows each)
+constexpr int NXW = 2;                       // activation warps (alternate stages)
+constexpr int THREADS = (NCW + 1 + NXW) * 32;  // + TMA warp
+constexpr int W_BOX = BM * 128;              // one 128-row x 128-byte code box (256 k)
+constexpr int W_BYTES = 2 * W_BOX;           // 32768
+constexpr int S_BYTES = BM * (KST / 32) * 2; // 4096
+constexpr int MAX_NT = 4;                    // column tiles per pass (32 columns)
+constexpr int SMEM_BUDGET = 226 * 1024;
 
 template <int NT>
 struct Cfg {
-    static constexpr int X_BOX = 8 * NT * 128;          // one 64-k activation box
-    static constexpr int X_BYTES = 4 * X_BOX;           // 4 boxes per stage
-    static constexpr int STAGE = W_BYTES + X_BYTES + S_BYTES;
-    static constexpr int NST = (SMEM_BUDGET / STAGE) < 2 ? 2 : (SMEM_BUDGET / STAGE);
-    static constexpr int SMEM = 1024 + NST * STAGE + 2 * NST * 8;
-    static_assert(W_BYTES % 1024 == 0 && X_BOX % 1024 == 0 && STAGE % 1024 == 0, "1024-byte swizzle alignment");
-    static_assert(8 * NT * BM * 4 <= STAGE * NST, "partial tile fits in the stage ring");
+    static constexpr int X_BOX = 8 * NT * 128;            // 64 k of the stage's activation columns
+    static constexpr int X_BYTES = 8 * X_BOX;
+    static constexpr int CI_BYTES = 16 * 8 * NT * 4;       // [16 blocks][8 NT slots] fp32
+    static constexpr int RAW = W_BYTES + X_BYTES + S_BYTES + CI_BYTES;
+    static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
+    static constexpr int NS = (SMEM_BUDGET / STAGE) > 6 ? 6 : (SMEM_BUDGET / STAGE);
+    static constexpr int SMEM = 1024 + NS * STAGE + 3 * NS * 8 + 64;
+    static_assert(NS >= 2, "at least two stages");
+    static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// K-split as a function of K alone: segments of >= 4 stages, at most 8.
-__host__ __device__ inline int ksplit_of(int K) {
-    int nst = K / KST;
-    int s = nst / 4;
-    return s < 1 ? 1 : (s > 8 ? 8 : s);
+// stages of 512 k (the last one may be half empty); segments of seg_st stages
+__host__ __device__ inline int n_stages(int K) { return (K + KST - 1) / KST; }
+__host__ __device__ inline int n_segments(int K, int seg_st) { return (n_stages(K) + seg_st - 1) / seg_st; }
+
+struct Sched {
+    int G;          // CTAs
+    long long U;    // units = tiles * ks
+    int ks, tiles, seg_st;
+    __device__ long long begin(int c) const { return (long long)c * U / G; }
+    __device__ int cta_of(long long u) const { return (int)(((u + 1) * G - 1) / U); }
+};
+
+// nibble codes (k = 8t .. 8t+7 of a block) -> (128 + code_m, 128 + code_{m+4}), exact
+__device__ __forceinline__ void codes_to_bf16(uint32_t w, uint32_t (&o)[4]) {
+    o[0] = dev::lop3_and_or(w, 0x000F000Fu, 0x43004300u);
+    o[1] = dev::lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);
+    o[2] = dev::lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);
+    o[3] = dev::lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);
 }
 
-// nibble codes of one 32-bit word (8 codes, k = 8t .. 8t+7 of a block) to
-// four bf16x2 registers holding (q_m, q_{m+4}) for m = 0..3
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&o)[4]) {
-    const uint32_t MASK = 0x000F000Fu, MAGIC = 0x43004300u;  // bf16 128.0 in each half
-    const __nv_bfloat162 OFF = __floats2bfloat162_rn(136.0f, 136.0f);
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        uint32_t v = dev::lop3_and_or(w >> (4 * m), MASK, MAGIC);  // (128 + code) per half, exact
-        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&v);
-        h = __hsub2(h, OFF);                                         // code - 8 = q, exact
-        o[m] = *reinterpret_cast<uint32_t *>(&h);
-    }
+__device__ __forceinline__ void named_sync_consumers() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
 }
 
 template <int NT, bool OUT_BF16>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ts,
-           const __grid_constant__ CUtensorMap tx, int N, int K, int n_cols, void *__restrict__ y, int ldy,
-           int accumulate, int ksplit, int32_t *dev_err) {
+           const uint16_t *__restrict__ x, int ldx, int N, int K, int n_cols, int col0, void *__restrict__ y, int ldy,
+           int accumulate, Sched sch, float *__restrict__ wsp_prefix, float *__restrict__ wsp_seg,
+           int *__restrict__ counters, int32_t *dev_err) {
     using C = Cfg<NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE);
-    uint64_t *empty = full + C::NST;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NS * C::STAGE);
+    uint64_t *ready = full + C::NS;
+    uint64_t *empty = ready + C::NS;
+    int *flag = reinterpret_cast<int *>(empty + C::NS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = blockIdx.x * BM;
-    const int seg = blockIdx.y;
-    const int col0 = blockIdx.z * 8 * NT;
-    const int nst_total = K / KST;
-    const int st_begin = seg * nst_total / ksplit;
-    const int nst = (seg + 1) * nst_total / ksplit - st_begin;
+    const int nst_total = n_stages(K);
+    const int seg_st = sch.seg_st, ks = sch.ks;
+    const long long ua = sch.begin(blockIdx.x), ub = sch.begin(blockIdx.x + 1);
+    constexpr int TILE_ELEMS = BM * 8 * NT;     // one tile's values for this pass
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::NST; ++s) {
+        for (int s = 0; s < C::NS; ++s) {
             dev::mbar_init(&full[s], 1);
-            dev::mbar_init(&empty[s], NCONS);
+            dev::mbar_init(&ready[s], 1);
+            dev::mbar_init(&empty[s], NCW);
         }
         dev::fence_barrier_init();
     }
     __syncthreads();
+    // The weights and scales are constant inputs: the TMA warp starts streaming
+    // them at once, overlapping the tail of the preceding kernel on the stream.
+    // Activations are read, and anything global is written, only after that
+    // kernel has finished (pdl_wait).
+    dev::pdl_launch_dependents();
 
-    float acc[NT][4];
-#pragma unroll
-    for (int c = 0; c < NT; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+    // stage sequence of this CTA: units ua..ub-1, each 1 or 2 stages
+    auto unit_stages = [&](long long u) { return min(seg_st, nst_total - (int)(u % ks) * seg_st); };
 
-    if (warp == NCONS) {
-        // ---------------- producer ----------------
+    if (warp == NCW) {
+        // ============================ TMA warp ============================
+        // lane 0 streams the codes (two 128-row x 128-byte boxes per 512-k stage)
+        // and the scales of every stage of this CTA, NS stages ahead of the
+        // consumers, reusing a slot once its consumers have released it.
         if (lane == 0) {
             dev::prefetch_tmap(&tw);
-            dev::prefetch_tmap(&tx);
             dev::prefetch_tmap(&ts);
-            int issued = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int s = i % C::NST;
-                if (i >= C::NST && !dev::mbar_wait(&empty[s], ((i / C::NST) - 1) & 1)) {
+            long long iu = ua;
+            int ist = 0;
+            for (int issued = 0; iu < ub; ++issued) {
+                const int s = issued % C::NS;
+                if (issued >= C::NS && !dev::mbar_wait(&empty[s], ((issued / C::NS) - 1) & 1)) {
                     dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     break;
                 }
+                const int tile = (int)(iu / ks);
+                const int k0 = ((int)(iu % ks) * seg_st + ist) * KST;
                 uint8_t *base = smem + s * C::STAGE;
-                const int k0 = (st_begin + i) * KST;
-                dev::mbar_arrive_expect_tx(&full[s], C::STAGE);
-                dev::tma_load_2d(base, &tw, k0 / 2, row0, &full[s]);
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    dev::tma_load_2d(base + W_BYTES + b * C::X_BOX, &tx, k0 + 64 * b, col0, &full[s]);
-                dev::tma_load_2d(base + W_BYTES + C::X_BYTES, &ts, k0 / 32, row0, &full[s]);
-                issued = i + 1;
-            }
-            // never leave copies in flight: wait (bounded) for every issued stage
-            for (int i = (issued > C::NST ? issued - C::NST : 0); i < issued; ++i)
-                if (!dev::mbar_wait(&full[i % C::NST], (i / C::NST) & 1)) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
-        }
-    } else {
-        // ---------------- consumers ----------------
-        const int r = lane >> 2, t = lane & 3;
-        const int wrow = warp * 16;
-        // B-fragment column of this lane: MMA column slot g = lane/4 carries
-        // activation column pi(g) = (g & 1) * 4 + g / 2 (bank-conflict-free rows)
-        const int g = lane >> 2;
-        const int xcol = (g & 1) * 4 + (g >> 1);
-        for (int i = 0; i < nst; ++i) {
-            const int s = i % C::NST;
-            if (!dev::mbar_wait(&full[s], (i / C::NST) & 1)) {
-                dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
-                break;
-            }
-            uint8_t *base = smem + s * C::STAGE;
-            const uint32_t wbase = dev::smem_u32(base);
-            const uint32_t xbase = wbase + W_BYTES;
-            const uint32_t sbase = xbase + C::X_BYTES;
-            uint32_t sr[4], sr8[4];
-            dev::lds128(sr[0], sr[1], sr[2], sr[3], sbase + (wrow + r) * 16);
-            dev::lds128(sr8[0], sr8[1], sr8[2], sr8[3], sbase + (wrow + r + 8) * 16);
-#pragma unroll
-            for (int bp = 0; bp < 4; ++bp) {
-                uint32_t wv[4];
-                {
-                    const int m = lane >> 3, rr = lane & 7;
-                    const int row = wrow + (m & 1) * 8 + rr;
-                    const int blk = 2 * bp + (m >> 1);
-                    dev::ldmatrix_x4(wv[0], wv[1], wv[2], wv[3], wbase + row * 128 + ((blk ^ (row & 7)) << 4));
+                dev::mbar_arrive_expect_tx(&full[s], W_BYTES + S_BYTES);
+                dev::tma_load_2d(base, &tw, k0 / 2, tile * BM, &full[s]);
+                dev::tma_load_2d(base + W_BOX, &tw, k0 / 2 + 128, tile * BM, &full[s]);
+                dev::tma_load_2d(base + W_BYTES + C::X_BYTES, &ts, k0 / 32, tile * BM, &full[s]);
+                if (++ist == unit_stages(iu)) {
+                    ist = 0;
+                    ++iu;
                 }
+            }
+        }
+        return;
+    }
+    if (warp > NCW) {
+        // ======================== activation warps ========================
+        // warp NCW + 1 + h prepares stages i with i % NXW == h: it reads the
+        // stage's activation columns from L2 (all loads of a group in flight),
+        // writes them in B-fragment order with their block sums, waits for the
+        // stage's TMA bytes, then hands the stage to the consumers.
+        const int h = warp - NCW - 1;
+        dev::pdl_wait();   // x may be the preceding kernel's output
+        bool ok = true;
+        long long pu = ua;
+        int pst = 0;
+        for (int i = 0; pu < ub; ++i) {
+            const int k0 = ((int)(pu % ks) * seg_st + pst) * KST;
+            if (++pst == unit_stages(pu)) {
+                pst = 0;
+                ++pu;
+            }
+            if (i % NXW != h) continue;
+            const int s = i % C::NS;
+            bool slot_free = (i < C::NS);   // the slot's previous stage must be released before writing
+            uint8_t *xs = smem + s * C::STAGE + W_BYTES;
+            float *ci = reinterpret_cast<float *>(smem + s * C::STAGE + W_BYTES + C::X_BYTES + S_BYTES);
+            // (block, column) pairs p = lane + 32 j; each is four 16-byte chunks of k = 32 blk .. +31;
+            // chunk sums in k order, block sum = chunk sums in order
+            constexpr int PAIRS = 16 * 8 * NT / 32;   // per lane
+            constexpr int GROUP = 4;                  // pairs whose loads are in flight together
+#pragma unroll 1
+            for (int j0 = 0; j0 < PAIRS; j0 += GROUP) {
+                uint4 v[GROUP][4];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int blk = 2 * bp + h;
-                    uint32_t ar[4], ar8[4];
-                    dequant_word(wv[2 * h], ar);       // row r
-                    dequant_word(wv[2 * h + 1], ar8);  // row r + 8
-                    const uint32_t s2 = sr[blk >> 1], s28 = sr8[blk >> 1];
-                    const float d_r = __half2float(__ushort_as_half((unsigned short)((blk & 1) ? (s2 >> 16) : (s2 & 0xFFFF))));
-                    const float d_r8 = __half2float(__ushort_as_half((unsigned short)((blk & 1) ? (s28 >> 16) : (s28 & 0xFFFF))));
+                for (int jj = 0; jj < GROUP; ++jj) {
+                    const int p = lane + 32 * (j0 + jj);
+                    const int blk = p / (8 * NT), c = p % (8 * NT);
+                    const int col = col0 + c, kb = k0 + 32 * blk;
 #pragma unroll
-                    for (int ct = 0; ct < NT; ++ct) {
-                        const int xrow = ct * 8 + xcol;
-                        const int chunk = ((blk & 1) * 4 + t) ^ (xrow & 7);
-                        uint32_t e01, e23, e45, e67;
-                        dev::lds128(e01, e23, e45, e67, xbase + (blk >> 1) * C::X_BOX + xrow * 128 + (chunk << 4));
-                        const uint32_t b00 = dev::prmt(e01, e45, 0x5410), b01 = dev::prmt(e01, e45, 0x7632);
-                        const uint32_t b10 = dev::prmt(e23, e67, 0x5410), b11 = dev::prmt(e23, e67, 0x7632);
-                        const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-                        float p[4];
-                        dev::mma_bf16(p, ar[0], ar8[0], ar[1], ar8[1], b00, b01, zero);
-                        dev::mma_bf16(p, ar[2], ar8[2], ar[3], ar8[3], b10, b11, p);
-                        acc[ct][0] = fmaf(d_r, p[0], acc[ct][0]);
-                        acc[ct][1] = fmaf(d_r, p[1], acc[ct][1]);
-                        acc[ct][2] = fmaf(d_r8, p[2], acc[ct][2]);
-                        acc[ct][3] = fmaf(d_r8, p[3], acc[ct][3]);
+                    for (int q = 0; q < 4; ++q) {
+                        v[jj][q] = make_uint4(0, 0, 0, 0);
+                        if (col < n_cols && kb + 8 * q < K)
+                            v[jj][q] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)col * ldx + kb + 8 * q));
                     }
                 }
+                if (!slot_free) {   // loads are in flight; now wait for the consumers' release
+                    int got = 1;
+                    if (lane == 0 && ok) got = dev::mbar_wait(&empty[s], ((i / C::NS) - 1) & 1) ? 1 : 0;
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got && ok) {
+                        if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                        ok = false;
+                    }
+                    slot_free = true;
+                }
+#pragma unroll
+                for (int jj = 0; jj < GROUP; ++jj) {
+                    const int p = lane + 32 * (j0 + jj);
+                    const int blk = p / (8 * NT), c = p % (8 * NT);
+                    uint8_t *row = xs + (blk >> 1) * C::X_BOX + c * 128;
+                    float sum = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t w4[4] = {v[jj][q].x, v[jj][q].y, v[jj][q].z, v[jj][q].w};
+                        float cs = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            cs += __uint_as_float(w4[e] << 16);
+                            cs += __uint_as_float(w4[e] & 0xFFFF0000u);
+                        }
+                        sum = (q == 0) ? cs : sum + cs;
+                        uint4 o;
+                        o.x = dev::prmt(w4[0], w4[2], 0x5410);   // (x0, x4)
+                        o.y = dev::prmt(w4[0], w4[2], 0x7632);   // (x1, x5)
+                        o.z = dev::prmt(w4[1], w4[3], 0x5410);   // (x2, x6)
+                        o.w = dev::prmt(w4[1], w4[3], 0x7632);   // (x3, x7)
+                        const int chunk = (((blk & 1) * 4 + q) ^ (c & 7)) << 4;
+                        *reinterpret_cast<uint4 *>(row + chunk) = o;
+                    }
+                    // MMA column slot g carries activation column pi(g) = (g & 1) * 4 + g / 2
+                    const int cc = c & 7, slot = (cc & 3) * 2 + (cc >> 2);
+                    ci[blk * 8 * NT + (c & ~7) + slot] = -136.0f * sum;
+                }
+            }
+            int got = 1;
+            if (lane == 0 && ok) got = dev::mbar_wait(&full[s], (i / C::NS) & 1) ? 1 : 0;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got && ok) {
+                if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                ok = false;
             }
             __syncwarp();
-            if (lane == 0) dev::mbar_arrive(&empty[s]);
+            if (lane == 0) dev::mbar_arrive(&ready[s]);
         }
+        return;
     }
 
-    // ---------------- segment partial -> shared tile [8NT cols][64 rows] ----------------
-    __syncthreads();
-    float *part = reinterpret_cast<float *>(smem);
-    if (warp < NCONS) {
-        const int r = lane >> 2, t = lane & 3;
-        const int wrow = warp * 16;
+    // ============================ consumers ============================
+    dev::pdl_wait();   // y (accumulate), the workspace and y writes follow the preceding kernel
+    const int r = lane >> 2, t = lane & 3;
+    const int wrow = warp * 16;
+    const int g = lane >> 2;
+    const int xcol = (g & 1) * 4 + (g >> 1);   // activation column of this lane's B fragment
+    float yrun[NT][4];
+    int i = 0;
+    bool ok = true;
+    long long u = ua;
+    while (u < ub) {
+        const int tile = (int)(u / ks);
+        const long long tile_u0 = (long long)tile * ks;
+        const long long u_end = min(ub, tile_u0 + ks);     // this CTA's units of this tile
+        const bool head = (u == tile_u0);
+        const bool whole = head && (u_end == tile_u0 + ks);
 #pragma unroll
-        for (int ct = 0; ct < NT; ++ct) {
-            // C slot 2t <-> column t, slot 2t+1 <-> column t + 4 (see xcol)
-            part[(ct * 8 + t) * BM + wrow + r] = acc[ct][0];
-            part[(ct * 8 + t + 4) * BM + wrow + r] = acc[ct][1];
-            part[(ct * 8 + t) * BM + wrow + r + 8] = acc[ct][2];
-            part[(ct * 8 + t + 4) * BM + wrow + r + 8] = acc[ct][3];
-        }
-    }
-    if (ksplit > 1)
-        dev::cluster_sync();
-    else
-        __syncthreads();
-
-    // ---------------- fixed-order combine of the segments and store ----------------
-    const int rank = (ksplit > 1) ? (int)dev::cluster_ctarank() : 0;
-    const int elems = 8 * NT * BM;
-    for (int e = rank * THREADS + threadIdx.x; e < elems; e += ksplit * THREADS) {
-        float v;
-        if (ksplit > 1) {
-            const uint32_t local = dev::smem_u32(part + e);
-            v = dev::ld_shared_cluster_f32(dev::map_shared_rank(local, 0));
-            for (int q = 1; q < ksplit; ++q) v += dev::ld_shared_cluster_f32(dev::map_shared_rank(local, q));
-        } else {
-            v = part[e];
-        }
-        const int col = col0 + e / BM, row = row0 + e % BM;
-        if (col < n_cols && row < N) {
-            if (OUT_BF16) {
-                reinterpret_cast<__nv_bfloat16 *>(y)[(size_t)col * ldy + row] = __float2bfloat16_rn(v);
+        for (int ct = 0; ct < NT; ++ct) yrun[ct][0] = yrun[ct][1] = yrun[ct][2] = yrun[ct][3] = 0.f;
+        for (; u < u_end; ++u) {
+            const int seg = (int)(u - tile_u0);
+            const int nstg = unit_stages(u);
+            float acc[NT][4];
+#pragma unroll
+            for (int ct = 0; ct < NT; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
+            for (int st = 0; st < nstg; ++st, ++i) {
+                const int s = i % C::NS;
+                if (ok && !dev::mbar_wait(&ready[s], (i / C::NS) & 1)) {
+                    dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                    ok = false;
+                }
+                const uint32_t wbase = dev::smem_u32(smem + s * C::STAGE);
+                const uint32_t xbase = wbase + W_BYTES;
+                const uint32_t sbase = xbase + C::X_BYTES;
+                const uint32_t cbase = sbase + S_BYTES;
+                constexpr int BP_UNROLL = NT > 4 ? 1 : 8;
+#pragma unroll BP_UNROLL
+                for (int bp = 0; bp < 8; ++bp) {
+                    uint32_t wv[4];
+                    {
+                        // blocks 2bp, 2bp+1: box bp/4 (256 k each), 16-byte chunk (2bp + m/2) % 8
+                        const int m = lane >> 3, rr = lane & 7;
+                        const int row = wrow + (m & 1) * 8 + rr;
+                        const int blk = 2 * bp + (m >> 1);
+                        dev::ldmatrix_x4(wv[0], wv[1], wv[2], wv[3],
+                                         wbase + (blk >> 3) * W_BOX + row * 128 + (((blk & 7) ^ (row & 7)) << 4));
+                    }
+                    uint32_t s2, s28;   // the two fp16 scales of blocks 2bp, 2bp+1 for rows r and r+8
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2) : "r"(sbase + (wrow + r) * 32 + bp * 4));
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s28) : "r"(sbase + (wrow + r + 8) * 32 + bp * 4));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int blk = 2 * bp + h;
+                        uint32_t ar[4], ar8[4];
+                        codes_to_bf16(wv[2 * h], ar);
+                        codes_to_bf16(wv[2 * h + 1], ar8);
+                        const float d_r = __half2float(__ushort_as_half((unsigned short)(s2 >> (16 * h))));
+                        const float d_r8 = __half2float(__ushort_as_half((unsigned short)(s28 >> (16 * h))));
+#pragma unroll
+                        for (int ct = 0; ct < NT; ++ct) {
+                            const int xrow = ct * 8 + xcol;
+                            const int chunk = ((blk & 1) * 4 + t) ^ (xrow & 7);
+                            uint32_t b00, b01, b10, b11;
+                            dev::lds128(b00, b01, b10, b11, xbase + (blk >> 1) * C::X_BOX + xrow * 128 + (chunk << 4));
+                            float c0, c1;
+                            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                                         : "=f"(c0), "=f"(c1)
+                                         : "r"(cbase + (blk * 8 * NT + ct * 8 + 2 * t) * 4));
+                            const float cinit[4] = {c0, c1, c0, c1};
+                            float p[4];
+                            dev::mma_bf16(p, ar[0], ar8[0], ar[1], ar8[1], b00, b01, cinit);
+                            dev::mma_bf16(p, ar[2], ar8[2], ar[3], ar8[3], b10, b11, p);
+                            acc[ct][0] = fmaf(d_r, p[0], acc[ct][0]);
+                            acc[ct][1] = fmaf(d_r, p[1], acc[ct][1]);
+                            acc[ct][2] = fmaf(d_r8, p[2], acc[ct][2]);
+                            acc[ct][3] = fmaf(d_r8, p[3], acc[ct][3]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(&empty[s]);
+            }
+            if (head) {
+                // this CTA holds the tile's leading segments: fold them in order
+#pragma unroll
+                for (int ct = 0; ct < NT; ++ct)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) yrun[ct][e] = (seg == 0) ? acc[ct][e] : yrun[ct][e] + acc[ct][e];
             } else {
-                float *yp = reinterpret_cast<float *>(y) + (size_t)col * ldy + row;
-                *yp = accumulate ? (*yp + v) : v;
+                // a later CTA's segment: store its sum for the final fold
+                float *ps = wsp_seg + ((size_t)tile * ks + seg) * TILE_ELEMS;
+#pragma unroll
+                for (int ct = 0; ct < NT; ++ct) {
+                    const int c = ct * 8 + t;
+                    ps[c * BM + wrow + r] = acc[ct][0];
+                    ps[(c + 4) * BM + wrow + r] = acc[ct][1];
+                    ps[c * BM + wrow + r + 8] = acc[ct][2];
+                    ps[(c + 4) * BM + wrow + r + 8] = acc[ct][3];
+                }
             }
         }
+        // ---------------- finish this CTA's part of the tile ----------------
+        auto store_y = [&](int c, int row, float v) {
+            const int col = col0 + c, n = tile * BM + row;
+            if (col < n_cols && n < N) {
+                if (OUT_BF16) {
+                    reinterpret_cast<__nv_bfloat16 *>(y)[(size_t)col * ldy + n] = __float2bfloat16_rn(v);
+                } else {
+                    float *yp = reinterpret_cast<float *>(y) + (size_t)col * ldy + n;
+                    *yp = accumulate ? (*yp + v) : v;
+                }
+            }
+        };
+        if (whole) {
+#pragma unroll
+            for (int ct = 0; ct < NT; ++ct) {
+                store_y(ct * 8 + t, wrow + r, yrun[ct][0]);
+                store_y(ct * 8 + t + 4, wrow + r, yrun[ct][1]);
+                store_y(ct * 8 + t, wrow + r + 8, yrun[ct][2]);
+                store_y(ct * 8 + t + 4, wrow + r + 8, yrun[ct][3]);
+            }
+            continue;
+        }
+        if (head) {
+            float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS;
+#pragma unroll
+            for (int ct = 0; ct < NT; ++ct) {
+                const int c = ct * 8 + t;
+                pp[c * BM + wrow + r] = yrun[ct][0];
+                pp[(c + 4) * BM + wrow + r] = yrun[ct][1];
+                pp[c * BM + wrow + r + 8] = yrun[ct][2];
+                pp[(c + 4) * BM + wrow + r + 8] = yrun[ct][3];
+            }
+        }
+        __threadfence();
+        named_sync_consumers();
+        if (threadIdx.x == 0) {
+            const int touch = sch.cta_of(tile_u0 + ks - 1) - sch.cta_of(tile_u0) + 1;
+            const int prev = atomicAdd(&counters[tile], 1);
+            *flag = (prev == touch - 1) ? 1 : 0;
+        }
+        named_sync_consumers();
+        const int last = *flag;
+        named_sync_consumers();   // everyone has read the flag before it is reused
+        if (last) {
+            // last CTA of this tile: prefix of the head CTA, then the remaining segments in order
+            __threadfence();
+            const int head_cta = sch.cta_of(tile_u0);
+            const long long head_end = min(sch.begin(head_cta + 1), tile_u0 + ks);
+            const int seg_from = (int)(head_end - tile_u0);
+            const float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS;
+            for (int e = threadIdx.x; e < TILE_ELEMS; e += NCW * 32) {
+                float v = __ldcg(pp + e);
+                for (int sg = seg_from; sg < ks; ++sg) v += __ldcg(wsp_seg + ((size_t)tile * ks + sg) * TILE_ELEMS + e);
+                store_y(e / BM, e % BM, v);
+            }
+            if (threadIdx.x == 0) counters[tile] = 0;   // the workspace is left zeroed for the next call
+        }
     }
-    if (ksplit > 1) dev::cluster_sync();  // keep shared memory alive until every rank has read it
 }
 
 template <int NT, bool OUT_BF16>
-spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int N, int K, int n_cols,
-                      int ldx, void *y, int ldy, int accumulate, int ksplit, int32_t *dev_err, cudaStream_t stream) {
+spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N, int K,
+                      int n_cols, int col0, void *y, int ldy, int accumulate, int seg_st, void *workspace,
+                      int32_t *dev_err, cudaStream_t stream) {
     using C = Cfg<NT>;
-    CUtensorMap tx;
-    {
-        uint64_t dims[2] = {(uint64_t)K, (uint64_t)n_cols};
-        uint64_t strides[1] = {(uint64_t)ldx * 2};
-        uint32_t box[2] = {64, (uint32_t)(8 * NT)};
-        if (!spec::encode_tiled(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box,
-                                CU_TENSOR_MAP_SWIZZLE_128B))
-            return SPEC_ERR_CUDA;
-    }
     auto kern = qmm_kernel<NT, OUT_BF16>;
     static bool configured = false;
     if (!configured) {
@@ -259,25 +425,44 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
         if (e != cudaSuccess) return spec::cuda_status(e, "cudaFuncSetAttribute(qmm smem)");
         configured = true;
     }
+    const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
+    Sched sch;
+    sch.seg_st = seg_st;
+    sch.ks = n_segments(K, seg_st);
+    sch.tiles = (N + BM - 1) / BM;
+    sch.U = (long long)sch.tiles * sch.ks;
+    sch.G = (int)(sch.U < sms ? sch.U : sms);
+    const size_t tiles = (size_t)sch.tiles;
+    const size_t cnt_bytes = ((tiles * sizeof(int)) + 255) & ~size_t(255);
+    int *counters = reinterpret_cast<int *>(workspace);
+    float *prefix = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + cnt_bytes);
+    float *segs = prefix + tiles * BM * 8 * NT;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + BM - 1) / BM, ksplit, (n_cols + 8 * NT - 1) / (8 * NT));
+    cfg.gridDim = dim3(sch.G);
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = ksplit;
-    attr[0].val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tw, ts, tx, N, K, n_cols, y, ldy, accumulate, ksplit, dev_err);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, sch, prefix,
+                                       segs, counters, dev_err);
     return spec::cuda_status(e, "qmm launch");
 }
 
+int pass_nt(int n_cols) { return n_cols <= 8 ? 1 : (n_cols <= 16 ? 2 : MAX_NT); }
+
+size_t ws_bytes_for(int N, int K, int nt, int seg_st) {
+    const size_t tiles = (size_t)(N + BM - 1) / BM;
+    const size_t cnt = ((tiles * sizeof(int)) + 255) & ~size_t(255);
+    return cnt + tiles * (1 + (size_t)n_segments(K, seg_st)) * BM * 8 * nt * sizeof(float);
+}
+
 spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
-                    void *y, spec_dtype y_dt, int ldy, int accumulate, int ksplit, int nt_force, int32_t *dev_err,
-                    cudaStream_t stream) {
+                    void *y, spec_dtype y_dt, int ldy, int accumulate, int seg_st, int nt, void *workspace,
+                    int32_t *dev_err, cudaStream_t stream) {
     CUtensorMap tw, ts;
     {
         uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)N};
@@ -290,21 +475,28 @@ spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const u
     {
         uint64_t dims[2] = {(uint64_t)K / 32, (uint64_t)N};
         uint64_t strides[1] = {(uint64_t)K / 32 * 2};
-        uint32_t box[2] = {8, BM};
+        uint32_t box[2] = {16, BM};
         if (!spec::encode_tiled(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, ws, dims, strides, box,
                                 CU_TENSOR_MAP_SWIZZLE_NONE))
             return SPEC_ERR_CUDA;
     }
-    int nt = nt_force ? nt_force : (n_cols <= 8 ? 1 : (n_cols <= 16 ? 2 : 4));
     const bool bf = (y_dt == SPEC_BF16);
-    switch (nt) {
-    case 1: return bf ? launch_nt<1, true>(tw, ts, x, N, K, n_cols, ldx, y, ldy, 0, ksplit, dev_err, stream)
-                      : launch_nt<1, false>(tw, ts, x, N, K, n_cols, ldx, y, ldy, accumulate, ksplit, dev_err, stream);
-    case 2: return bf ? launch_nt<2, true>(tw, ts, x, N, K, n_cols, ldx, y, ldy, 0, ksplit, dev_err, stream)
-                      : launch_nt<2, false>(tw, ts, x, N, K, n_cols, ldx, y, ldy, accumulate, ksplit, dev_err, stream);
-    default: return bf ? launch_nt<4, true>(tw, ts, x, N, K, n_cols, ldx, y, ldy, 0, ksplit, dev_err, stream)
-                       : launch_nt<4, false>(tw, ts, x, N, K, n_cols, ldx, y, ldy, accumulate, ksplit, dev_err, stream);
+    // one pass per group of 8 nt columns; passes run back to back on the stream
+    for (int col0 = 0; col0 < n_cols; col0 += 8 * nt) {
+        spec_status st;
+#define SPEC_QMM_CASE(NTV)                                                                                         \
+    st = bf ? launch_nt<NTV, true>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg_st, workspace, dev_err, stream) \
+            : launch_nt<NTV, false>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg_st, workspace, dev_err, \
+                                    stream)
+        switch (nt) {
+        case 1: SPEC_QMM_CASE(1); break;
+        case 2: SPEC_QMM_CASE(2); break;
+        default: SPEC_QMM_CASE(MAX_NT);
+        }
+#undef SPEC_QMM_CASE
+        if (st != SPEC_OK) return st;
     }
+    return SPEC_OK;
 }
 
 spec_status check_args(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
@@ -321,46 +513,72 @@ spec_status check_args(const uint8_t *wq, const uint16_t *ws, int N, int K, cons
     return SPEC_OK;
 }
 
+spec_status check_ws(const void *workspace, size_t ws_bytes, size_t need) {
+    if (!workspace || ws_bytes < need || !spec::aligned16(workspace))
+        return spec::fail(SPEC_ERR_WORKSPACE, "qmatmul: workspace needs %zu bytes (16-byte aligned, zero-filled "
+                                              "before its first use), got %zu", need, ws_bytes);
+    return SPEC_OK;
+}
+
 }  // namespace
+
+extern "C" size_t spec_qmatmul_workspace(int N, int K, int n_cols) {
+    if (N <= 0 || K < 256 || n_cols <= 0) return 0;
+    // the largest layout either entry point may use for this shape (one-stage segments)
+    return ws_bytes_for(N, K, pass_nt(n_cols), 1);
+}
 
 extern "C" spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,
                                     int n_cols, int ldx, void *y, spec_dtype y_dt, int ldy, int accumulate,
-                                    int32_t *dev_err, spec_stream_t stream) {
+                                    void *workspace, size_t ws_bytes, int32_t *dev_err, spec_stream_t stream) {
     spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
     if (st != SPEC_OK) return st;
     SPEC_CHECK_ARG(y_dt == SPEC_F32 || y_dt == SPEC_BF16, "qmatmul: y_dt must be SPEC_F32 or SPEC_BF16");
     SPEC_CHECK_ARG(!(accumulate && y_dt != SPEC_F32), "qmatmul: accumulate needs SPEC_F32 output");
     if (n_cols == 0) return SPEC_OK;
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, ksplit_of(K), 0, dev_err,
+    const int nt = pass_nt(n_cols);
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, SEG_ST));
+    if (st != SPEC_OK) return st;
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, SEG_ST, nt, workspace, dev_err,
                    (cudaStream_t)stream);
 }
 
 extern "C" spec_status spec_qmatmul_noninvariant(const uint8_t *wq, const uint16_t *ws, int N, int K,
                                                  const uint16_t *x, int n_cols, int ldx, float *y, int ldy,
+                                                 int seg_stages, void *workspace, size_t ws_bytes,
                                                  spec_stream_t stream) {
     spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
     if (st != SPEC_OK) return st;
     if (n_cols == 0) return SPEC_OK;
-    // split of K chosen per call: enough CTAs for two per SM, whatever K is
-    const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
-    const int nt = n_cols <= 8 ? 1 : (n_cols <= 16 ? 2 : 4);
-    const long long tiles = (long long)((N + BM - 1) / BM) * ((n_cols + 8 * nt - 1) / (8 * nt));
-    int ks = (int)((2ll * sms + tiles - 1) / tiles);
-    const int nst = K / KST;
-    if (ks > 8) ks = 8;
-    if (ks > nst) ks = nst;
-    if (ks < 1) ks = 1;
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, ks, nt, nullptr, (cudaStream_t)stream);
+    const int nst = n_stages(K);
+    int seg = seg_stages;
+    if (seg <= 0) {
+        // per-call choice: the longest segment that still deals every SM about eight units
+        const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
+        const long long tiles = (N + BM - 1) / BM;
+        seg = nst;
+        while (seg > 1 && tiles * n_segments(K, seg) < 8ll * sms) seg = (seg + 1) / 2;
+    }
+    SPEC_CHECK_ARG(seg >= 1, "qmatmul_noninvariant: seg_stages must be >= 0");
+    if (seg > nst) seg = nst;
+    const int nt = pass_nt(n_cols);
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, seg));
+    if (st != SPEC_OK) return st;
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, seg, nt, workspace, nullptr,
+                   (cudaStream_t)stream);
 }
 
 // Test hook: run the invariant kernel with an explicit column-tile width so the
 // tests can show the per-column result does not depend on it.
 extern "C" spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,
-                                             int n_cols, int ldx, float *y, int ldy, int nt, spec_stream_t stream) {
+                                             int n_cols, int ldx, float *y, int ldy, int nt, void *workspace,
+                                             size_t ws_bytes, spec_stream_t stream) {
     spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
     if (st != SPEC_OK) return st;
-    SPEC_CHECK_ARG(nt == 1 || nt == 2 || nt == 4, "nt must be 1, 2 or 4");
+    SPEC_CHECK_ARG(nt == 1 || nt == 2 || nt == MAX_NT, "nt must be 1, 2 or 4");
     if (n_cols == 0) return SPEC_OK;
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, ksplit_of(K), nt, nullptr,
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, SEG_ST));
+    if (st != SPEC_OK) return st;
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, SEG_ST, nt, workspace, nullptr,
                    (cudaStream_t)stream);
 }

@@ -73,6 +73,9 @@ class Decoder:
         self.logits = torch.zeros((R, self.V), dtype=torch.float32, device=d)
         self.ws_bytes = L.spec_flash_decode_workspace(R, self.Hq, self.D, self.max_len)
         self.attn_ws = torch.empty(self.ws_bytes // 4 + 64, dtype=torch.float32, device=d)
+        shapes = [(self.nqkv, H), (H, self.Hq * self.D), (2 * F, H), (H, F), (self.V, H)]
+        self.qws_bytes = max(L.spec_qmatmul_workspace(N, K, R) for N, K in shapes)
+        self.qws = torch.zeros(self.qws_bytes // 4 + 64, dtype=torch.int32, device=d)   # zero once; calls keep it so
 
     # ------------------------------------------------------------------
     def embed(self, tokens, R):
@@ -83,7 +86,7 @@ class Decoder:
         max_kv_len = max_kv_len or self.max_len
         L.spec_add_rmsnorm(self.h, None, lay["norm1"], R, H, self.cfg.eps, self.a)
         L.spec_qmatmul(lay["qkv"][0], lay["qkv"][1], self.nqkv, H, self.a, R, H, self.qkv, L.SPEC_F32,
-                       self.nqkv, 0, self.dev_err)
+                       self.nqkv, 0, self.qws, self.qws_bytes, self.dev_err)
         L.spec_rope_append(self.qkv, R, self.Hq, self.Hkv, D, self.rope, self.max_len, cu_rows, ctx, S, self.q,
                            self.k_cache[li], self.v_cache[li], self.pages, self.block_table, self.max_blocks,
                            None, None, self.dev_err)
@@ -91,18 +94,18 @@ class Decoder:
                             self.v_cache[li], self.pages, self.block_table, self.max_blocks, ctx, cu_rows, S, R,
                             max_kv_len, self.attn, L.SPEC_BF16, self.attn_ws, self.ws_bytes, self.dev_err)
         L.spec_qmatmul(lay["o"][0], lay["o"][1], H, self.Hq * D, self.attn, R, self.Hq * D, self.h, L.SPEC_F32, H, 1,
-                       self.dev_err)
+                       self.qws, self.qws_bytes, self.dev_err)
         L.spec_add_rmsnorm(self.h, None, lay["norm2"], R, H, self.cfg.eps, self.a)
         L.spec_qmatmul(lay["gu"][0], lay["gu"][1], 2 * F, H, self.a, R, H, self.gu, L.SPEC_F32, 2 * F,
-                       0, self.dev_err)
+                       0, self.qws, self.qws_bytes, self.dev_err)
         L.spec_swiglu(self.gu, R, F, self.act)
         L.spec_qmatmul(lay["down"][0], lay["down"][1], H, F, self.act, R, F, self.h, L.SPEC_F32, H, 1,
-                       self.dev_err)
+                       self.qws, self.qws_bytes, self.dev_err)
 
     def head(self, R):
         L.spec_add_rmsnorm(self.h, None, self.final_norm, R, self.H, self.cfg.eps, self.a)
         L.spec_qmatmul(self.lm[0], self.lm[1], self.V, self.H, self.a, R, self.H, self.logits, L.SPEC_F32,
-                       self.V, 0, self.dev_err)
+                       self.V, 0, self.qws, self.qws_bytes, self.dev_err)
 
     def forward(self, tokens, cu_rows, ctx, S, R, max_kv_len=None):
         """Logits (fp32 [R][V], in self.logits) for a ragged verify batch whose rows

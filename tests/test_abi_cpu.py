@@ -49,7 +49,7 @@ def test_qmatmul_host_validation(kw, msg):
         a["ldx"] = max(a["K"], 8) if a["K"] % 8 == 0 else 512
     with pytest.raises(L.SpecError) as e:
         L.spec_qmatmul(a["wq"], a["ws"], a["N"], a["K"], a["x"], a["n_cols"], a["ldx"], a["y"], a["y_dt"], a["ldy"],
-                       stream=0)
+                       0, FAKE, 1 << 30, stream=0)
     assert msg in str(e.value) and e.value.status == 1
 
 
@@ -73,6 +73,15 @@ def test_flash_decode_host_validation_and_workspace():
     assert e.value.status == 3
 
 
+def test_qmatmul_workspace_is_checked_on_the_host():
+    import invariant_speculative_verification_gb300 as L
+    need = L.spec_qmatmul_workspace(64, 512, 8)
+    assert need > 0
+    with pytest.raises(L.SpecError) as e:
+        L.spec_qmatmul(FAKE, FAKE, 64, 512, FAKE, 8, 512, FAKE, 0, 64, 0, FAKE, 16, stream=0)
+    assert e.value.status == 3
+
+
 def test_verify_and_compact_host_validation():
     import invariant_speculative_verification_gb300 as L
     with pytest.raises(L.SpecError, match="multiple of 8"):
@@ -84,5 +93,5 @@ def test_verify_and_compact_host_validation():
 
 def test_zero_sized_calls_launch_nothing():
     import invariant_speculative_verification_gb300 as L
-    L.spec_qmatmul(FAKE, FAKE, 64, 512, FAKE, 0, 512, FAKE, 0, 64, stream=0)
+    L.spec_qmatmul(FAKE, FAKE, 64, 512, FAKE, 0, 512, FAKE, 0, 64, 0, None, 0, stream=0)
     L.spec_verify_greedy(FAKE, 0, 1000, FAKE, 0, 0, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, stream=0)

@@ -23,6 +23,17 @@ def _lib():
     return L
 
 
+_WS = {}
+
+
+def workspace(nbytes):
+    """A zero-filled workspace shared by the calls of this module (calls leave it zeroed)."""
+    key = "ws"
+    if key not in _WS or _WS[key].numel() * 4 < nbytes:
+        _WS[key] = torch.zeros(nbytes // 4 + 1024, dtype=torch.int32, device="cuda")
+    return _WS[key]
+
+
 def run(case_or_w, x_dev, n_cols, N, K, ldx=None, out_dt=0, y=None, accumulate=0, ldy=None):
     L = _lib()
     wq, ws = case_or_w
@@ -31,10 +42,17 @@ def run(case_or_w, x_dev, n_cols, N, K, ldx=None, out_dt=0, y=None, accumulate=0
     if y is None:
         y = torch.zeros((max(n_cols, 1), ldy), dtype=torch.float32 if out_dt == 0 else torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    L.spec_qmatmul(wq, ws, N, K, x_dev, n_cols, ldx, y, out_dt, ldy, accumulate, err)
+    need = L.spec_qmatmul_workspace(N, K, max(n_cols, 1))
+    wsp = workspace(need)
+    L.spec_qmatmul(wq, ws, N, K, x_dev, n_cols, ldx, y, out_dt, ldy, accumulate, wsp, wsp.numel() * 4, err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     return y
+
+
+def debug_nt_ws(N, K, nt):
+    tiles = (N + 127) // 128
+    return ((tiles * 4 + 255) // 256) * 256 + tiles * (1 + (K + 511) // 512) * 128 * 8 * nt * 4
 
 
 @pytest.fixture(scope="module")
@@ -84,7 +102,8 @@ def test_column_placement_and_tile_width_do_not_change_bits(tiny):
             assert bits_equal(y[pos], ref), (n_cols, pos)
             for nt in (1, 2, 4):
                 yy = torch.zeros((n_cols, 512), dtype=torch.float32, device="cuda")
-                L.spec_qmatmul_debug_nt(w[0], w[1], 512, 512, xs, n_cols, 512, yy, 512, nt)
+                wsp = workspace(debug_nt_ws(512, 512, nt))
+                L.spec_qmatmul_debug_nt(w[0], w[1], 512, 512, xs, n_cols, 512, yy, 512, nt, wsp, wsp.numel() * 4)
                 torch.cuda.synchronize()
                 assert bits_equal(yy, y), (n_cols, nt)
 
@@ -137,8 +156,32 @@ def test_dense_sweep_shapes_sampled_parity_and_invariance(N, K):
 def test_noninvariant_variant_matches_oracle(tiny):
     case, w, x = tiny
     L = _lib()
-    y = torch.zeros((8, 512), dtype=torch.float32, device="cuda")
-    L.spec_qmatmul_noninvariant(w[0], w[1], 512, 512, x, 8, 512, y, 512)
-    torch.cuda.synchronize()
     ref = oracle.qmatmul(case.wq, case.ws, case.x, 512, 512)
-    assert rel_err_rows(host(y), ref) <= TOL
+    for seg in (0, 1, 2):
+        y = torch.zeros((8, 512), dtype=torch.float32, device="cuda")
+        wsp = workspace(L.spec_qmatmul_workspace(512, 512, 8))
+        L.spec_qmatmul_noninvariant(w[0], w[1], 512, 512, x, 8, 512, y, 512, seg, wsp, wsp.numel() * 4)
+        torch.cuda.synchronize()
+        assert rel_err_rows(host(y), ref) <= TOL
+
+
+def test_workspace_is_left_zeroed_and_calls_repeat_bitwise():
+    L = _lib()
+    case = synth.qmatmul_case(55, 1000, 2048, 80)
+    w, x = (dev(case.wq), dev(case.ws)), dev(case.x)
+    need = L.spec_qmatmul_workspace(1000, 2048, 80)
+    wsp = torch.zeros(need // 4 + 16, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(3):
+        y = torch.zeros((80, 1000), dtype=torch.float32, device="cuda")
+        L.spec_qmatmul(w[0], w[1], 1000, 2048, x, 80, 2048, y, 0, 1000, 0, wsp, wsp.numel() * 4)
+        torch.cuda.synchronize()
+        outs.append(y)
+        counters = wsp[:(1000 + 127) // 128]
+        assert int(counters.abs().sum().item()) == 0
+    assert bits_equal(outs[0], outs[1]) and bits_equal(outs[1], outs[2])
+    ref = oracle.qmatmul(case.wq, case.ws, case.x, 1000, 2048)
+    assert rel_err_rows(host(outs[0]), ref) <= TOL
+    with pytest.raises(L.SpecError) as e:
+        L.spec_qmatmul(w[0], w[1], 1000, 2048, x, 80, 2048, outs[0], 0, 1000, 0, wsp, 64)
+    assert e.value.status == 3
