@@ -86,6 +86,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                     const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_start,
                     const int32_t *__restrict__ cu_rows, int R, int max_kv_len, int nc_max,
                     float2 *__restrict__ part_ml, float *__restrict__ part_o, int32_t *dev_err) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     using C = ACfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -351,6 +353,8 @@ __global__ void __launch_bounds__(128)
 attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__restrict__ cu_rows, int S, int R, int Hq,
                     int nc_max, const float2 *__restrict__ part_ml, const float *__restrict__ part_o, void *out,
                     int max_kv_len) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (wid >= R * Hq) return;
@@ -410,9 +414,10 @@ spec_status launch_partial(const CUtensorMap &tk, const CUtensorMap &tv, const v
         configured = true;
     }
     dim3 grid(nc_max, Hkv, S);
-    kern<<<grid, THREADS, C::SMEM, st>>>(tk, tv, reinterpret_cast<const uint16_t *>(q), Hq, Hkv, scale * LOG2E,
-                                         num_pages, bt, max_blocks, ctx, cu, R, max_kv_len, nc_max, ml, po, dev_err);
-    return spec::cuda_status(cudaGetLastError(), "attn partial launch");
+    cudaError_t le = spec::launch_pdl(kern, grid, dim3(THREADS), C::SMEM, st, tk, tv, reinterpret_cast<const uint16_t *>(q),
+                                      Hq, Hkv, scale * LOG2E, num_pages, bt, max_blocks, ctx, cu, R, max_kv_len, nc_max,
+                                      ml, po, dev_err);
+    return spec::cuda_status(le, "attn partial launch");
 }
 
 }  // namespace
@@ -460,22 +465,19 @@ spec_status attn_run(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, f
     const int warps = R * Hq;
     dim3 grid((warps + 3) / 4);
     const bool obf = (out_dt == SPEC_BF16);
+    cudaError_t le;
     if (D == 128) {
         if (obf)
-            attn_combine_kernel<128, true><<<grid, 128, 0, stream>>>(ctx_start, cu_rows, S, R, Hq, nc_max, ml, po, out,
-                                                                     max_kv_len);
+            le = launch_pdl(attn_combine_kernel<128, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len);
         else
-            attn_combine_kernel<128, false><<<grid, 128, 0, stream>>>(ctx_start, cu_rows, S, R, Hq, nc_max, ml, po,
-                                                                      out, max_kv_len);
+            le = launch_pdl(attn_combine_kernel<128, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len);
     } else {
         if (obf)
-            attn_combine_kernel<64, true><<<grid, 128, 0, stream>>>(ctx_start, cu_rows, S, R, Hq, nc_max, ml, po, out,
-                                                                    max_kv_len);
+            le = launch_pdl(attn_combine_kernel<64, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len);
         else
-            attn_combine_kernel<64, false><<<grid, 128, 0, stream>>>(ctx_start, cu_rows, S, R, Hq, nc_max, ml, po, out,
-                                                                     max_kv_len);
+            le = launch_pdl(attn_combine_kernel<64, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len);
     }
-    return cuda_status(cudaGetLastError(), "attn combine launch");
+    return cuda_status(le, "attn combine launch");
 }
 
 spec_status attn_check(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, const void *k_cache,

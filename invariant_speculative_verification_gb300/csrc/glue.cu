@@ -16,6 +16,8 @@ __device__ __forceinline__ int seq_of_row(const int32_t *cu_rows, int S, int r) 
 
 __global__ void embed_kernel(const uint16_t *__restrict__ emb, int V, int H, const int32_t *__restrict__ tokens,
                              float *__restrict__ h, int32_t *dev_err) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int r = blockIdx.x;
     int tok = tokens[r];
     const bool bad = tok < 0 || tok >= V;
@@ -30,6 +32,8 @@ constexpr int NT_NORM = 256;
 __global__ void __launch_bounds__(NT_NORM)
 add_rmsnorm_kernel(float *__restrict__ h, const float *__restrict__ delta, const float *__restrict__ w, int H,
                    float eps, uint16_t *__restrict__ out) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int r = blockIdx.x;
     float4 *hr = reinterpret_cast<float4 *>(h + (size_t)r * H);
     const float4 *dr = delta ? reinterpret_cast<const float4 *>(delta + (size_t)r * H) : nullptr;
@@ -71,6 +75,8 @@ add_rmsnorm_kernel(float *__restrict__ h, const float *__restrict__ delta, const
 }
 
 __global__ void rope_table_kernel(float *tab, int max_pos, int D, double theta) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int half = D / 2;
     const long long n = (long long)max_pos * half;
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
@@ -87,6 +93,8 @@ __global__ void rope_append_kernel(const float *__restrict__ qkv, int Hq, int Hk
                                    uint16_t *__restrict__ k_cache, uint16_t *__restrict__ v_cache, int num_pages,
                                    const int32_t *__restrict__ block_table, int max_blocks, uint16_t *__restrict__ k_stage,
                                    uint16_t *__restrict__ v_stage, int32_t *dev_err) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int r = blockIdx.x;
     const int s = seq_of_row(cu_rows, S, r);
     const int pos = ctx_start[s] + (r - cu_rows[s]);
@@ -151,6 +159,8 @@ __global__ void rope_append_kernel(const float *__restrict__ qkv, int Hq, int Hk
 }
 
 __global__ void swiglu_kernel(const float *__restrict__ gu, int F, uint16_t *__restrict__ out) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int r = blockIdx.x;
     const float *g = gu + (size_t)r * 2 * F;
     for (int i = threadIdx.x; i < F; i += blockDim.x) {
@@ -161,6 +171,8 @@ __global__ void swiglu_kernel(const float *__restrict__ gu, int F, uint16_t *__r
 }
 
 __global__ void cast_bf16_kernel(const float *__restrict__ in, size_t n, uint16_t *__restrict__ out) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
         out[i] = __bfloat16_as_ushort(__float2bfloat16_rn(in[i]));
 }
@@ -169,6 +181,8 @@ __global__ void cast_bf16_kernel(const float *__restrict__ in, size_t n, uint16_
 __global__ void ngram_draft_kernel(const int32_t *__restrict__ hist, int hist_cap, const int32_t *__restrict__ hist_len,
                                    int S, int W, const int32_t *__restrict__ pad, int32_t *__restrict__ drafts,
                                    int32_t *__restrict__ matched_n, int32_t *__restrict__ block_tokens) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int s = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (s >= S) return;
@@ -209,6 +223,8 @@ __global__ void commit_accepted_kernel(int32_t *__restrict__ hist, int hist_cap,
                                        const int32_t *__restrict__ drafts, int W, const int32_t *__restrict__ accepted,
                                        const int32_t *__restrict__ correction, const int32_t *__restrict__ ctx_new,
                                        int32_t *__restrict__ ctx, int S, int32_t *dev_err) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int s = blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= S) return;
     const int a = accepted[s];
@@ -231,7 +247,8 @@ extern "C" spec_status spec_embed(const uint16_t *emb, int V, int H, const int32
     SPEC_CHECK_ARG(V >= 1 && H >= 1 && R >= 0, "embed: bad sizes");
     SPEC_CHECK_ARG(emb && (tokens || R == 0) && (h || R == 0), "embed: NULL pointer");
     if (R == 0) return SPEC_OK;
-    embed_kernel<<<R, 256, 0, (cudaStream_t)stream>>>(emb, V, H, tokens, h, dev_err);
+    cudaError_t le = spec::launch_pdl(embed_kernel, dim3(R), dim3(256), 0, (cudaStream_t)stream, emb, V, H, tokens, h, dev_err);
+    if (le != cudaSuccess) return spec::cuda_status(le, "embed launch");
     return spec::cuda_status(cudaGetLastError(), "embed launch");
 }
 
@@ -242,7 +259,8 @@ extern "C" spec_status spec_add_rmsnorm(float *h, const float *delta, const floa
     SPEC_CHECK_ARG(spec::aligned16(h) && spec::aligned16(delta) && spec::aligned16(w) && spec::aligned16(out),
                    "add_rmsnorm: pointers must be 16-byte aligned");
     if (R == 0) return SPEC_OK;
-    add_rmsnorm_kernel<<<R, NT_NORM, 0, (cudaStream_t)stream>>>(h, delta, w, H, eps, out);
+    cudaError_t le = spec::launch_pdl(add_rmsnorm_kernel, dim3(R), dim3(NT_NORM), 0, (cudaStream_t)stream, h, delta, w, H, eps, out);
+    if (le != cudaSuccess) return spec::cuda_status(le, "add_rmsnorm launch");
     return spec::cuda_status(cudaGetLastError(), "add_rmsnorm launch");
 }
 
@@ -251,7 +269,8 @@ extern "C" spec_status spec_rope_table(float *tab, int max_pos, int D, float the
     const long long n = (long long)max_pos * (D / 2);
     int blocks = (int)((n + 255) / 256);
     if (blocks > 4096) blocks = 4096;
-    rope_table_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(tab, max_pos, D, (double)theta);
+    cudaError_t le = spec::launch_pdl(rope_table_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, tab, max_pos, D, (double)theta);
+    if (le != cudaSuccess) return spec::cuda_status(le, "rope_table launch");
     return spec::cuda_status(cudaGetLastError(), "rope_table launch");
 }
 
@@ -267,9 +286,10 @@ extern "C" spec_status spec_rope_append(const float *qkv, int R, int Hq, int Hkv
     SPEC_CHECK_ARG(k_stage || R == 0 || (k_cache && v_cache && block_table && num_pages >= 1 && max_blocks >= 1),
                    "rope_append: cache arguments needed when not staging");
     if (R == 0 || S == 0) return SPEC_OK;
-    rope_append_kernel<<<R, 256, 0, (cudaStream_t)stream>>>(qkv, Hq, Hkv, D, rope_tab, max_pos, cu_rows, ctx_start, S,
-                                                            q_out, k_cache, v_cache, num_pages, block_table,
-                                                            max_blocks, k_stage, v_stage, dev_err);
+    cudaError_t le = spec::launch_pdl(rope_append_kernel, dim3(R), dim3(256), 0, (cudaStream_t)stream, qkv, Hq, Hkv, D,
+                                      rope_tab, max_pos, cu_rows, ctx_start, S, q_out, k_cache, v_cache, num_pages,
+                                      block_table, max_blocks, k_stage, v_stage, dev_err);
+    if (le != cudaSuccess) return spec::cuda_status(le, "rope_append launch");
     return spec::cuda_status(cudaGetLastError(), "rope_append launch");
 }
 
@@ -277,7 +297,8 @@ extern "C" spec_status spec_swiglu(const float *gu, int R, int F, uint16_t *out,
     SPEC_CHECK_ARG(R >= 0 && F >= 1, "swiglu: bad sizes");
     SPEC_CHECK_ARG((gu && out) || R == 0, "swiglu: NULL pointer");
     if (R == 0) return SPEC_OK;
-    swiglu_kernel<<<R, 256, 0, (cudaStream_t)stream>>>(gu, F, out);
+    cudaError_t le = spec::launch_pdl(swiglu_kernel, dim3(R), dim3(256), 0, (cudaStream_t)stream, gu, F, out);
+    if (le != cudaSuccess) return spec::cuda_status(le, "swiglu launch");
     return spec::cuda_status(cudaGetLastError(), "swiglu launch");
 }
 
@@ -286,7 +307,8 @@ extern "C" spec_status spec_cast_bf16(const float *in, size_t n, uint16_t *out, 
     if (n == 0) return SPEC_OK;
     size_t blocks = (n + 255) / 256;
     if (blocks > 8192) blocks = 8192;
-    cast_bf16_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(in, n, out);
+    cudaError_t le = spec::launch_pdl(cast_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, (cudaStream_t)stream, in, n, out);
+    if (le != cudaSuccess) return spec::cuda_status(le, "cast_bf16 launch");
     return spec::cuda_status(cudaGetLastError(), "cast_bf16 launch");
 }
 
@@ -296,8 +318,9 @@ extern "C" spec_status spec_ngram_draft(const int32_t *hist, int hist_cap, const
     SPEC_CHECK_ARG(S >= 0 && W >= 0 && hist_cap >= 1, "ngram_draft: bad sizes");
     SPEC_CHECK_ARG(S == 0 || (hist && hist_len && (W == 0 || (pad && drafts))), "ngram_draft: NULL pointer");
     if (S == 0 || (W == 0 && !block_tokens && !matched_n)) return SPEC_OK;
-    ngram_draft_kernel<<<(S + 3) / 4, 128, 0, (cudaStream_t)stream>>>(hist, hist_cap, hist_len, S, W, pad, drafts,
-                                                                      matched_n, block_tokens);
+    cudaError_t le = spec::launch_pdl(ngram_draft_kernel, dim3((S + 3) / 4), dim3(128), 0, (cudaStream_t)stream, hist,
+                                      hist_cap, hist_len, S, W, pad, drafts, matched_n, block_tokens);
+    if (le != cudaSuccess) return spec::cuda_status(le, "ngram_draft launch");
     return spec::cuda_status(cudaGetLastError(), "ngram_draft launch");
 }
 
@@ -309,8 +332,9 @@ extern "C" spec_status spec_commit_accepted(int32_t *hist, int hist_cap, int32_t
     SPEC_CHECK_ARG(S == 0 || (hist && hist_len && accepted && correction && ctx_new && ctx && (W == 0 || drafts)),
                    "commit_accepted: NULL pointer");
     if (S == 0) return SPEC_OK;
-    commit_accepted_kernel<<<(S + 127) / 128, 128, 0, (cudaStream_t)stream>>>(hist, hist_cap, hist_len, drafts, W,
-                                                                              accepted, correction, ctx_new, ctx, S,
-                                                                              dev_err);
+    cudaError_t le = spec::launch_pdl(commit_accepted_kernel, dim3((S + 127) / 128), dim3(128), 0, (cudaStream_t)stream,
+                                      hist, hist_cap, hist_len, drafts, W, accepted, correction, ctx_new, ctx, S,
+                                      dev_err);
+    if (le != cudaSuccess) return spec::cuda_status(le, "commit_accepted launch");
     return spec::cuda_status(cudaGetLastError(), "commit_accepted launch");
 }

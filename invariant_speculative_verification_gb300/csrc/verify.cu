@@ -34,6 +34,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(VT)
 argmax_partial_kernel(const void *__restrict__ logits, int V, int split, int R, Best *__restrict__ part,
                       int32_t *dev_err) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int r = blockIdx.y, sp = blockIdx.x;
     if (r >= R) return;
     constexpr int VEC = BF16 ? 8 : 4;
@@ -83,6 +85,8 @@ verify_finalize_kernel(const Best *__restrict__ part, int split, const int32_t *
                        int V, const int32_t *__restrict__ drafts, const int32_t *__restrict__ ctx_start,
                        int32_t *__restrict__ argmax_out, int32_t *__restrict__ accepted,
                        int32_t *__restrict__ correction, int32_t *__restrict__ ctx_new, int32_t *dev_err) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int s = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (s >= S) return;
@@ -146,6 +150,8 @@ kv_compact_kernel(const uint16_t *__restrict__ k_stage, const uint16_t *__restri
                   const int32_t *__restrict__ accepted, const int32_t *__restrict__ cu_rows, int S, int R,
                   int32_t *__restrict__ cu_kept, int32_t *__restrict__ kept_src, int64_t *__restrict__ dst_slot,
                   int32_t *dev_err) {
+    dev::pdl_wait();
+    dev::pdl_launch_dependents();
     const int r = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __shared__ int sh_base;
@@ -244,15 +250,15 @@ extern "C" spec_status spec_verify_greedy(const void *logits, spec_dtype dt, int
     cudaStream_t st = (cudaStream_t)stream;
     Best *part = reinterpret_cast<Best *>(workspace);
     dim3 grid(split, R);
-    if (dt == SPEC_BF16)
-        argmax_partial_kernel<true><<<grid, VT, 0, st>>>(logits, V, split, R, part, dev_err);
-    else
-        argmax_partial_kernel<false><<<grid, VT, 0, st>>>(logits, V, split, R, part, dev_err);
-    spec_status s1 = spec::cuda_status(cudaGetLastError(), "argmax launch");
-    if (s1 != SPEC_OK) return s1;
-    verify_finalize_kernel<<<(S + 3) / 4, 128, 0, st>>>(part, split, cu_rows, S, R, V, drafts, ctx_start, argmax_out,
-                                                       accepted, correction, ctx_new, dev_err);
-    return spec::cuda_status(cudaGetLastError(), "verify finalize launch");
+    cudaError_t le = (dt == SPEC_BF16)
+                         ? spec::launch_pdl(argmax_partial_kernel<true>, grid, dim3(VT), 0, st, logits, V, split, R, part,
+                                            dev_err)
+                         : spec::launch_pdl(argmax_partial_kernel<false>, grid, dim3(VT), 0, st, logits, V, split, R, part,
+                                            dev_err);
+    if (le != cudaSuccess) return spec::cuda_status(le, "argmax launch");
+    le = spec::launch_pdl(verify_finalize_kernel, dim3((S + 3) / 4), dim3(128), 0, st, (const Best *)part, split, cu_rows,
+                          S, R, V, drafts, ctx_start, argmax_out, accepted, correction, ctx_new, dev_err);
+    return spec::cuda_status(le, "verify finalize launch");
 }
 
 extern "C" spec_status spec_kv_compact(const void *k_stage, const void *v_stage, void *k_cache, void *v_cache,
@@ -271,9 +277,10 @@ extern "C" spec_status spec_kv_compact(const void *k_stage, const void *v_stage,
                                 spec::aligned16(k_cache) && spec::aligned16(v_cache)),
                    "kv_compact: stage and cache pointers must be non-NULL and 16-byte aligned");
     if (S == 0) return SPEC_OK;
-    kv_compact_kernel<<<R, 256, 0, (cudaStream_t)stream>>>(
-        reinterpret_cast<const uint16_t *>(k_stage), reinterpret_cast<const uint16_t *>(v_stage),
-        reinterpret_cast<uint16_t *>(k_cache), reinterpret_cast<uint16_t *>(v_cache), Hkv, D, num_pages, block_table,
-        max_blocks, ctx_start, accepted, cu_rows, S, R, cu_kept, kept_src, dst_slot, dev_err);
-    return spec::cuda_status(cudaGetLastError(), "kv_compact launch");
+    cudaError_t le = spec::launch_pdl(
+        kv_compact_kernel, dim3(R), dim3(256), 0, (cudaStream_t)stream, reinterpret_cast<const uint16_t *>(k_stage),
+        reinterpret_cast<const uint16_t *>(v_stage), reinterpret_cast<uint16_t *>(k_cache),
+        reinterpret_cast<uint16_t *>(v_cache), Hkv, D, num_pages, block_table, max_blocks, ctx_start, accepted, cu_rows,
+        S, R, cu_kept, kept_src, dst_slot, dev_err);
+    return spec::cuda_status(le, "kv_compact launch");
 }
