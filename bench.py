@@ -133,7 +133,12 @@ def count_launches(fn):
         orig[name] = f
 
         def wrap(*a, _n=name, _f=f, **k):
-            counts[_n] = counts.get(_n, 0) + 1
+            if _n == "spec_qmatmul":   # one launch per pass of 8, 16 or 80 columns
+                nc = int(a[5])
+                per = 8 if nc <= 8 else (16 if nc <= 16 else 80)
+                counts[_n] = counts.get(_n, 0) + (nc + per - 1) // per
+            else:
+                counts[_n] = counts.get(_n, 0) + 1
             return _f(*a, **k)
         setattr(L, name, wrap)
     try:

@@ -113,7 +113,7 @@ spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
                          void *workspace, size_t ws_bytes,
                          int32_t *dev_err, spec_stream_t stream);
 
-/* The same product with a K-segment length of seg_stages x 256 chosen per
+/* The same product with a K-segment length of seg_stages x 512 chosen per
  * call (seg_stages = 0: picked from the problem size and the GPU for speed),
  * so its reduction order depends on the call: NOT batch invariant.  It exists
  * to measure what width-1 speed the invariant kernel gives up (the pages'
@@ -273,7 +273,7 @@ spec_status spec_commit_accepted(int32_t *hist, int hist_cap, int32_t *hist_len,
                                  int32_t *ctx, int S, int32_t *dev_err, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Test hook: spec_qmatmul with an explicit column-tile width nt in {1, 2, 4}
+ * Test hook: spec_qmatmul with an explicit column-tile width nt in {1, 2, 10}
  * (columns per pass = 8 nt; the workspace must hold T * (1 + ceil(K/512))
  * * 128 * 8 nt floats after 256-byte-rounded T int counters, T = ceil(N/128)).  The result of every column must not depend on
  * nt; the tests use this to show it.  y_dt is SPEC_F32.

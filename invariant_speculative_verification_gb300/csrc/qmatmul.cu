@@ -20,19 +20,23 @@
 // scheduling that may depend on the call; the arithmetic above never does.
 //
 // Execution: a persistent grid of one CTA per SM, each with eight consumer
-// warps (16 weight rows each, 128 rows per tile) and one producer warp.  The
-// (128-row tile x K-segment) units are dealt out in equal contiguous ranges
-// (stream-K), so every SM streams the same number of bytes.  The producer's
-// lane 0 issues TMA (cp.async.bulk.tensor) copies of each 512-k stage -- the
-// int4 codes (two 128-row x 128-byte boxes, 128B swizzle) and the fp16 scales
-// -- into a ring of mbarrier-guarded stages; the producer warp reads the
-// stage's activation columns from L2 with vector loads, writes them in the
-// MMA B-fragment order and writes the block sums, so consumers issue only
-// ldmatrix, 4 LOP3 per 8 weights, lds and mma.sync.  A tile covered by one CTA is folded in registers and written
-// directly.  A tile shared by several CTAs is finished through the workspace:
-// the CTA holding its first segment stores its fold so far, the others store
-// their segment sums, and the last CTA to finish (atomic counter) folds the
-// rest in segment order, writes y and resets the counter.
+// warps (16 weight rows each, 128 rows per tile), one TMA warp and two or three
+// activation warps.  The (128-row tile x K-segment) units are dealt out in
+// equal contiguous ranges (stream-K), so every SM streams the same number of
+// bytes.  The TMA warp's lane 0 issues cp.async.bulk.tensor copies of each
+// stage -- the int4 codes (128-row x 128-byte boxes, 128B swizzle) and the
+// fp16 scales -- into a ring of mbarrier-guarded stages.  A stage is 512 k
+// for passes of up to 16 columns and 256 k for the 80-column pass (a segment
+// is then two stages; only the delivery changes, not the arithmetic).  The
+// activation warps read the stage's activation columns from L2 with vector
+// loads, write them in the MMA B-fragment order together with the block sums
+// and hand the stage on, so consumers issue only ldmatrix, 4 LOP3 per 8
+// weights, lds and mma.sync.  A tile covered by one CTA is folded in
+// registers and written directly.  A tile shared by several CTAs is finished
+// through the workspace: the CTA holding its first segment stores its fold so
+// far, the others store their segment sums, and the last CTA to finish
+// (atomic counter) folds the rest in segment order, writes y and resets the
+// counter.
 //
 // The weight format (int4 block 32, fp16 scale, even k in the low nibble) is
 // the stand-in for the block-quantised formats named in ramgpt.org, "When
@@ -42,23 +46,28 @@
 
 namespace {
 
-constexpr int KST = 512;                     // k per stage (= one K-segment on the invariant path)
-constexpr int SEG_ST = 1;                    // stages per K-segment (invariant path)
+constexpr int SEG_K = 512;                   // k per K-segment (the invariant reduction unit)
 constexpr int BM = 128;                      // weight rows per tile
 constexpr int NCW = 8;                       // consumer warps (16 rows each)
-constexpr int NXW = 2;                       // activation warps (alternate stages)
-constexpr int THREADS = (NCW + 1 + NXW) * 32;  // + TMA warp
 constexpr int W_BOX = BM * 128;              // one 128-row x 128-byte code box (256 k)
-constexpr int W_BYTES = 2 * W_BOX;           // 32768
-constexpr int S_BYTES = BM * (KST / 32) * 2; // 4096
-constexpr int MAX_NT = 4;                    // column tiles per pass (32 columns)
+constexpr int MAX_NT = 10;                   // column tiles per pass (80 columns)
 constexpr int SMEM_BUDGET = 226 * 1024;
 
+// Narrow passes (<= 16 columns) stream 512-k stages; the 80-column pass uses
+// 256-k stages (its activations are 5x larger) and three activation warps.
+// The stage size only changes how a segment is delivered, never its arithmetic.
 template <int NT>
 struct Cfg {
-    static constexpr int X_BOX = 8 * NT * 128;            // 64 k of the stage's activation columns
-    static constexpr int X_BYTES = 8 * X_BOX;
-    static constexpr int CI_BYTES = 16 * 8 * NT * 4;       // [16 blocks][8 NT slots] fp32
+    static constexpr int KS = NT >= 10 ? 256 : 512;         // k per stage
+    static constexpr int NBLK = KS / 32;                    // 32-k blocks per stage
+    static constexpr int NWBOX = KS / 256;                  // code boxes per stage
+    static constexpr int NXW = NT >= 10 ? 3 : 2;            // activation warps (12 warps in all at most)
+    static constexpr int THREADS = (NCW + 1 + NXW) * 32;    // + TMA warp
+    static constexpr int W_BYTES = NWBOX * W_BOX;
+    static constexpr int S_BYTES = BM * NBLK * 2;
+    static constexpr int X_BOX = 8 * NT * 128;              // 64 k of the pass's activation columns
+    static constexpr int X_BYTES = (NBLK / 2) * X_BOX;
+    static constexpr int CI_BYTES = NBLK * 8 * NT * 4;      // [blocks][8 NT slots] fp32
     static constexpr int RAW = W_BYTES + X_BYTES + S_BYTES + CI_BYTES;
     static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
     static constexpr int NS = (SMEM_BUDGET / STAGE) > 6 ? 6 : (SMEM_BUDGET / STAGE);
@@ -67,14 +76,16 @@ struct Cfg {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// stages of 512 k (the last one may be half empty); segments of seg_st stages
-__host__ __device__ inline int n_stages(int K) { return (K + KST - 1) / KST; }
-__host__ __device__ inline int n_segments(int K, int seg_st) { return (n_stages(K) + seg_st - 1) / seg_st; }
+// 32-k blocks per stage of a pass with nt column tiles (the scale box width)
+inline int stage_blocks(int nt) { return nt >= MAX_NT ? Cfg<MAX_NT>::NBLK : nt == 2 ? Cfg<2>::NBLK : Cfg<1>::NBLK; }
+
+// number of K-segments of length seg_k (the last may be shorter)
+inline int n_segments(int K, int seg_k) { return (K + seg_k - 1) / seg_k; }
 
 struct Sched {
     int G;          // CTAs
     long long U;    // units = tiles * ks
-    int ks, tiles, seg_st;
+    int ks, tiles, seg_st;   // segments, tiles, stages per segment
     __device__ long long begin(int c) const { return (long long)c * U / G; }
     __device__ int cta_of(long long u) const { return (int)(((u + 1) * G - 1) / U); }
 };
@@ -92,7 +103,7 @@ __device__ __forceinline__ void named_sync_consumers() {
 }
 
 template <int NT, bool OUT_BF16>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ts,
            const uint16_t *__restrict__ x, int ldx, int N, int K, int n_cols, int col0, void *__restrict__ y, int ldy,
            int accumulate, Sched sch, float *__restrict__ wsp_prefix, float *__restrict__ wsp_seg,
@@ -106,10 +117,14 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     int *flag = reinterpret_cast<int *>(empty + C::NS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nst_total = n_stages(K);
-    const int seg_st = sch.seg_st, ks = sch.ks;
+    const int nst_total = (K + C::KS - 1) / C::KS;   // stages of this pass's size
+    const int seg_st = sch.seg_st, ks = sch.ks;       // stages per segment, segments
     const long long ua = sch.begin(blockIdx.x), ub = sch.begin(blockIdx.x + 1);
     constexpr int TILE_ELEMS = BM * 8 * NT;     // one tile's values for this pass
+    // Partial sums in the workspace keep the accumulator fragments as the
+    // consumer threads hold them: [column tile][warp][lane][4] floats, so every
+    // store and load is a coalesced 16-byte access by the thread that owns it.
+    const int frag = ((warp * 32 + (threadIdx.x & 31)) * 4);   // + ct * NCW * 128
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NS; ++s) {
@@ -146,12 +161,13 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                     break;
                 }
                 const int tile = (int)(iu / ks);
-                const int k0 = ((int)(iu % ks) * seg_st + ist) * KST;
+                const int k0 = ((int)(iu % ks) * seg_st + ist) * C::KS;
                 uint8_t *base = smem + s * C::STAGE;
-                dev::mbar_arrive_expect_tx(&full[s], W_BYTES + S_BYTES);
-                dev::tma_load_2d(base, &tw, k0 / 2, tile * BM, &full[s]);
-                dev::tma_load_2d(base + W_BOX, &tw, k0 / 2 + 128, tile * BM, &full[s]);
-                dev::tma_load_2d(base + W_BYTES + C::X_BYTES, &ts, k0 / 32, tile * BM, &full[s]);
+                dev::mbar_arrive_expect_tx(&full[s], C::W_BYTES + C::S_BYTES);
+#pragma unroll
+                for (int b = 0; b < C::NWBOX; ++b)
+                    dev::tma_load_2d(base + b * W_BOX, &tw, k0 / 2 + 128 * b, tile * BM, &full[s]);
+                dev::tma_load_2d(base + C::W_BYTES + C::X_BYTES, &ts, k0 / 32, tile * BM, &full[s]);
                 if (++ist == unit_stages(iu)) {
                     ist = 0;
                     ++iu;
@@ -162,7 +178,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     }
     if (warp > NCW) {
         // ======================== activation warps ========================
-        // warp NCW + 1 + h prepares stages i with i % NXW == h: it reads the
+        // warp NCW + 1 + h prepares stages i with i % C::NXW == h: it reads the
         // stage's activation columns from L2 (all loads of a group in flight),
         // writes them in B-fragment order with their block sums, waits for the
         // stage's TMA bytes, then hands the stage to the consumers.
@@ -172,19 +188,19 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
         long long pu = ua;
         int pst = 0;
         for (int i = 0; pu < ub; ++i) {
-            const int k0 = ((int)(pu % ks) * seg_st + pst) * KST;
+            const int k0 = ((int)(pu % ks) * seg_st + pst) * C::KS;
             if (++pst == unit_stages(pu)) {
                 pst = 0;
                 ++pu;
             }
-            if (i % NXW != h) continue;
+            if (i % C::NXW != h) continue;
             const int s = i % C::NS;
             bool slot_free = (i < C::NS);   // the slot's previous stage must be released before writing
-            uint8_t *xs = smem + s * C::STAGE + W_BYTES;
-            float *ci = reinterpret_cast<float *>(smem + s * C::STAGE + W_BYTES + C::X_BYTES + S_BYTES);
+            uint8_t *xs = smem + s * C::STAGE + C::W_BYTES;
+            float *ci = reinterpret_cast<float *>(smem + s * C::STAGE + C::W_BYTES + C::X_BYTES + C::S_BYTES);
             // (block, column) pairs p = lane + 32 j; each is four 16-byte chunks of k = 32 blk .. +31;
             // chunk sums in k order, block sum = chunk sums in order
-            constexpr int PAIRS = 16 * 8 * NT / 32;   // per lane
+            constexpr int PAIRS = C::NBLK * 8 * NT / 32;   // per lane
             constexpr int GROUP = 4;                  // pairs whose loads are in flight together
 #pragma unroll 1
             for (int j0 = 0; j0 < PAIRS; j0 += GROUP) {
@@ -263,6 +279,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     int i = 0;
     bool ok = true;
     long long u = ua;
+
     while (u < ub) {
         const int tile = (int)(u / ks);
         const long long tile_u0 = (long long)tile * ks;
@@ -284,12 +301,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                     ok = false;
                 }
                 const uint32_t wbase = dev::smem_u32(smem + s * C::STAGE);
-                const uint32_t xbase = wbase + W_BYTES;
+                const uint32_t xbase = wbase + C::W_BYTES;
                 const uint32_t sbase = xbase + C::X_BYTES;
-                const uint32_t cbase = sbase + S_BYTES;
-                constexpr int BP_UNROLL = NT > 4 ? 1 : 8;
+                const uint32_t cbase = sbase + C::S_BYTES;
+                constexpr int BP_UNROLL = NT > 4 ? 1 : C::NBLK / 2;
 #pragma unroll BP_UNROLL
-                for (int bp = 0; bp < 8; ++bp) {
+                for (int bp = 0; bp < C::NBLK / 2; ++bp) {
                     uint32_t wv[4];
                     {
                         // blocks 2bp, 2bp+1: box bp/4 (256 k each), 16-byte chunk (2bp + m/2) % 8
@@ -300,8 +317,10 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                                          wbase + (blk >> 3) * W_BOX + row * 128 + (((blk & 7) ^ (row & 7)) << 4));
                     }
                     uint32_t s2, s28;   // the two fp16 scales of blocks 2bp, 2bp+1 for rows r and r+8
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2) : "r"(sbase + (wrow + r) * 32 + bp * 4));
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s28) : "r"(sbase + (wrow + r + 8) * 32 + bp * 4));
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2) : "r"(sbase + (wrow + r) * (2 * C::NBLK) + bp * 4));
+                    asm volatile("ld.shared.u32 %0, [%1];"
+                                 : "=r"(s28)
+                                 : "r"(sbase + (wrow + r + 8) * (2 * C::NBLK) + bp * 4));
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int blk = 2 * bp + h;
@@ -342,15 +361,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                     for (int e = 0; e < 4; ++e) yrun[ct][e] = (seg == 0) ? acc[ct][e] : yrun[ct][e] + acc[ct][e];
             } else {
                 // a later CTA's segment: store its sum for the final fold
-                float *ps = wsp_seg + ((size_t)tile * ks + seg) * TILE_ELEMS;
+                float *ps = wsp_seg + ((size_t)tile * ks + seg) * TILE_ELEMS + frag;
 #pragma unroll
-                for (int ct = 0; ct < NT; ++ct) {
-                    const int c = ct * 8 + t;
-                    ps[c * BM + wrow + r] = acc[ct][0];
-                    ps[(c + 4) * BM + wrow + r] = acc[ct][1];
-                    ps[c * BM + wrow + r + 8] = acc[ct][2];
-                    ps[(c + 4) * BM + wrow + r + 8] = acc[ct][3];
-                }
+                for (int ct = 0; ct < NT; ++ct)
+                    if (col0 + ct * 8 < n_cols)
+                        __stcg(reinterpret_cast<float4 *>(ps + ct * NCW * 128),
+                               make_float4(acc[ct][0], acc[ct][1], acc[ct][2], acc[ct][3]));
             }
         }
         // ---------------- finish this CTA's part of the tile ----------------
@@ -376,46 +392,88 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             continue;
         }
         if (head) {
-            float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS;
+            float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS + frag;
 #pragma unroll
-            for (int ct = 0; ct < NT; ++ct) {
-                const int c = ct * 8 + t;
-                pp[c * BM + wrow + r] = yrun[ct][0];
-                pp[(c + 4) * BM + wrow + r] = yrun[ct][1];
-                pp[c * BM + wrow + r + 8] = yrun[ct][2];
-                pp[(c + 4) * BM + wrow + r + 8] = yrun[ct][3];
-            }
+            for (int ct = 0; ct < NT; ++ct)
+                if (col0 + ct * 8 < n_cols)
+                    __stcg(reinterpret_cast<float4 *>(pp + ct * NCW * 128),
+                           make_float4(yrun[ct][0], yrun[ct][1], yrun[ct][2], yrun[ct][3]));
         }
-        __threadfence();
-        named_sync_consumers();
+        // shared tile: count this CTA's arrival; the last CTA folds the segments in order
+        named_sync_consumers();                 // all partial stores of this CTA are issued
         if (threadIdx.x == 0) {
+            __threadfence();                    // ... and visible device-wide before the counter moves
             const int touch = sch.cta_of(tile_u0 + ks - 1) - sch.cta_of(tile_u0) + 1;
             const int prev = atomicAdd(&counters[tile], 1);
             *flag = (prev == touch - 1) ? 1 : 0;
         }
         named_sync_consumers();
         const int last = *flag;
-        named_sync_consumers();   // everyone has read the flag before it is reused
         if (last) {
-            // last CTA of this tile: prefix of the head CTA, then the remaining segments in order
             __threadfence();
             const int head_cta = sch.cta_of(tile_u0);
             const long long head_end = min(sch.begin(head_cta + 1), tile_u0 + ks);
             const int seg_from = (int)(head_end - tile_u0);
-            const float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS;
-            for (int e = threadIdx.x; e < TILE_ELEMS; e += NCW * 32) {
-                float v = __ldcg(pp + e);
-                for (int sg = seg_from; sg < ks; ++sg) v += __ldcg(wsp_seg + ((size_t)tile * ks + sg) * TILE_ELEMS + e);
-                store_y(e / BM, e % BM, v);
+            const float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS + frag;
+            const float *p0 = wsp_seg + (size_t)tile * ks * TILE_ELEMS + frag;
+            // each thread folds its own fragments: prefix, then segment sums in
+            // ascending segment order; loads of several segments are in flight together
+            constexpr int SG = NT >= 8 ? 2 : (NT >= 2 ? 4 : 8);
+#pragma unroll
+            for (int ct = 0; ct < NT; ++ct) {
+                if (col0 + ct * 8 < n_cols) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp + ct * NCW * 128));
+                    yrun[ct][0] = v.x, yrun[ct][1] = v.y, yrun[ct][2] = v.z, yrun[ct][3] = v.w;
+                }
+            }
+            int sg = seg_from;
+            for (; sg + SG <= ks; sg += SG) {
+                float4 l[SG][NT];
+#pragma unroll
+                for (int q = 0; q < SG; ++q)
+#pragma unroll
+                    for (int ct = 0; ct < NT; ++ct)
+                        l[q][ct] = (col0 + ct * 8 < n_cols)
+                                       ? __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)(sg + q) * TILE_ELEMS +
+                                                                                 ct * NCW * 128))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < SG; ++q)
+#pragma unroll
+                    for (int ct = 0; ct < NT; ++ct) {
+                        yrun[ct][0] += l[q][ct].x;
+                        yrun[ct][1] += l[q][ct].y;
+                        yrun[ct][2] += l[q][ct].z;
+                        yrun[ct][3] += l[q][ct].w;
+                    }
+            }
+            for (; sg < ks; ++sg) {
+#pragma unroll
+                for (int ct = 0; ct < NT; ++ct) {
+                    if (col0 + ct * 8 < n_cols) {
+                        const float4 l = __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)sg * TILE_ELEMS +
+                                                                                 ct * NCW * 128));
+                        yrun[ct][0] += l.x, yrun[ct][1] += l.y, yrun[ct][2] += l.z, yrun[ct][3] += l.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int ct = 0; ct < NT; ++ct) {
+                store_y(ct * 8 + t, wrow + r, yrun[ct][0]);
+                store_y(ct * 8 + t + 4, wrow + r, yrun[ct][1]);
+                store_y(ct * 8 + t, wrow + r + 8, yrun[ct][2]);
+                store_y(ct * 8 + t + 4, wrow + r + 8, yrun[ct][3]);
             }
             if (threadIdx.x == 0) counters[tile] = 0;   // the workspace is left zeroed for the next call
         }
+        named_sync_consumers();   // the flag is read by everyone before it is reused
     }
 }
 
+// seg512: segment length in units of 512 k (1 for the invariant entry points)
 template <int NT, bool OUT_BF16>
 spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N, int K,
-                      int n_cols, int col0, void *y, int ldy, int accumulate, int seg_st, void *workspace,
+                      int n_cols, int col0, void *y, int ldy, int accumulate, int seg512, void *workspace,
                       int32_t *dev_err, cudaStream_t stream) {
     using C = Cfg<NT>;
     auto kern = qmm_kernel<NT, OUT_BF16>;
@@ -427,8 +485,8 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     }
     const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
     Sched sch;
-    sch.seg_st = seg_st;
-    sch.ks = n_segments(K, seg_st);
+    sch.seg_st = seg512 * (SEG_K / C::KS);
+    sch.ks = n_segments(K, seg512 * SEG_K);
     sch.tiles = (N + BM - 1) / BM;
     sch.U = (long long)sch.tiles * sch.ks;
     sch.G = (int)(sch.U < sms ? sch.U : sms);
@@ -439,7 +497,7 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     float *segs = prefix + tiles * BM * 8 * NT;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sch.G);
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -454,14 +512,14 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
 
 int pass_nt(int n_cols) { return n_cols <= 8 ? 1 : (n_cols <= 16 ? 2 : MAX_NT); }
 
-size_t ws_bytes_for(int N, int K, int nt, int seg_st) {
+size_t ws_bytes_for(int N, int K, int nt, int seg512) {
     const size_t tiles = (size_t)(N + BM - 1) / BM;
     const size_t cnt = ((tiles * sizeof(int)) + 255) & ~size_t(255);
-    return cnt + tiles * (1 + (size_t)n_segments(K, seg_st)) * BM * 8 * nt * sizeof(float);
+    return cnt + tiles * (1 + (size_t)n_segments(K, seg512 * SEG_K)) * BM * 8 * nt * sizeof(float);
 }
 
 spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
-                    void *y, spec_dtype y_dt, int ldy, int accumulate, int seg_st, int nt, void *workspace,
+                    void *y, spec_dtype y_dt, int ldy, int accumulate, int seg512, int nt, void *workspace,
                     int32_t *dev_err, cudaStream_t stream) {
     CUtensorMap tw, ts;
     {
@@ -475,7 +533,7 @@ spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const u
     {
         uint64_t dims[2] = {(uint64_t)K / 32, (uint64_t)N};
         uint64_t strides[1] = {(uint64_t)K / 32 * 2};
-        uint32_t box[2] = {16, BM};
+        uint32_t box[2] = {(uint32_t)stage_blocks(nt), BM};
         if (!spec::encode_tiled(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, ws, dims, strides, box,
                                 CU_TENSOR_MAP_SWIZZLE_NONE))
             return SPEC_ERR_CUDA;
@@ -485,8 +543,8 @@ spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const u
     for (int col0 = 0; col0 < n_cols; col0 += 8 * nt) {
         spec_status st;
 #define SPEC_QMM_CASE(NTV)                                                                                         \
-    st = bf ? launch_nt<NTV, true>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg_st, workspace, dev_err, stream) \
-            : launch_nt<NTV, false>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg_st, workspace, dev_err, \
+    st = bf ? launch_nt<NTV, true>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err, stream) \
+            : launch_nt<NTV, false>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace, dev_err, \
                                     stream)
         switch (nt) {
         case 1: SPEC_QMM_CASE(1); break;
@@ -537,9 +595,9 @@ extern "C" spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N
     SPEC_CHECK_ARG(!(accumulate && y_dt != SPEC_F32), "qmatmul: accumulate needs SPEC_F32 output");
     if (n_cols == 0) return SPEC_OK;
     const int nt = pass_nt(n_cols);
-    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, SEG_ST));
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
     if (st != SPEC_OK) return st;
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, SEG_ST, nt, workspace, dev_err,
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, nt, workspace, dev_err,
                    (cudaStream_t)stream);
 }
 
@@ -550,14 +608,14 @@ extern "C" spec_status spec_qmatmul_noninvariant(const uint8_t *wq, const uint16
     spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
     if (st != SPEC_OK) return st;
     if (n_cols == 0) return SPEC_OK;
-    const int nst = n_stages(K);
+    const int nst = n_segments(K, SEG_K);   // 512-k units
     int seg = seg_stages;
     if (seg <= 0) {
         // per-call choice: the longest segment that still deals every SM about eight units
         const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
         const long long tiles = (N + BM - 1) / BM;
         seg = nst;
-        while (seg > 1 && tiles * n_segments(K, seg) < 8ll * sms) seg = (seg + 1) / 2;
+        while (seg > 1 && tiles * n_segments(K, seg * SEG_K) < 8ll * sms) seg = (seg + 1) / 2;
     }
     SPEC_CHECK_ARG(seg >= 1, "qmatmul_noninvariant: seg_stages must be >= 0");
     if (seg > nst) seg = nst;
@@ -575,10 +633,10 @@ extern "C" spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *
                                              size_t ws_bytes, spec_stream_t stream) {
     spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
     if (st != SPEC_OK) return st;
-    SPEC_CHECK_ARG(nt == 1 || nt == 2 || nt == MAX_NT, "nt must be 1, 2 or 4");
+    SPEC_CHECK_ARG(nt == 1 || nt == 2 || nt == MAX_NT, "nt must be 1, 2 or 10");
     if (n_cols == 0) return SPEC_OK;
-    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, SEG_ST));
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
     if (st != SPEC_OK) return st;
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, SEG_ST, nt, workspace, nullptr,
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, 1, nt, workspace, nullptr,
                    (cudaStream_t)stream);
 }
