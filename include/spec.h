@@ -125,6 +125,34 @@ spec_status spec_qmatmul_noninvariant(const uint8_t *wq, const uint16_t *ws, int
                                       float *y, int ldy, int seg_stages,
                                       void *workspace, size_t ws_bytes, spec_stream_t stream);
 
+/* spec_qmatmul without a workspace argument; the source pages describe no
+ * such call, it is a convenience of this library.  Its scratch is a fixed
+ * 8 MiB array in the library's own device memory (one per device), so the
+ * call allocates nothing.  It is meant for callers that cannot hand over a
+ * buffer: a plain C host loop that owns no device allocator, a caller whose
+ * device memory is all reserved by another framework's caching allocator, or
+ * one that must not call cudaMalloc / cudaFree because those calls may
+ * synchronise the device and stall the streams it is feeding.
+ *
+ * Arguments, arithmetic and results are those of spec_qmatmul with the same
+ * inputs (bit for bit).  Shapes whose scratch would exceed 8 MiB, i.e.
+ * ceil(N/128) * (1 + ceil(K/512)) * 4096 * nt bytes plus 256-byte-rounded
+ * ceil(N/128) ints, with nt = 1 for n_cols <= 8, 2 for <= 16 and 10 above,
+ * are rejected with SPEC_ERR_WORKSPACE and a message (for example N = 17408,
+ * K = 5120 fits at up to 8 columns).  The scratch's leading counters must be
+ * zero when the kernel starts: the call clears them on `stream` itself before
+ * each launch, so nothing has to be zeroed by the caller.
+ * There is one scratch per device: two calls whose work can overlap on the
+ * GPU (different streams without an ordering between them) race on it and
+ * give wrong results.  Order such calls, for example by issuing them on one
+ * stream.  The first call on a device, made with that device current, looks
+ * up the scratch address (cudaGetSymbolAddress); make that first call before
+ * any stream capture begins. */
+spec_status spec_qmatmul_static_scratch(const uint8_t *wq, const uint16_t *ws, int N, int K,
+                                        const uint16_t *x, int n_cols, int ldx,
+                                        void *y, spec_dtype y_dt, int ldy, int accumulate,
+                                        int32_t *dev_err, spec_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * K2 + K3  split-KV causal attention for verify blocks (paged KV cache)
  *

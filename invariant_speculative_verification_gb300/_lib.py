@@ -35,6 +35,7 @@ _SIGS = {
     "spec_qmatmul": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "spec_qmatmul_noninvariant": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _sz, _vp]),
     "spec_qmatmul_debug_nt": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _sz, _vp]),
+    "spec_qmatmul_static_scratch": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _vp]),
     "spec_flash_decode_workspace": (_sz, [_i32, _i32, _i32, _i32]),
     "spec_flash_decode": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32, _i32,
                                  _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
@@ -130,6 +131,12 @@ def spec_qmatmul_noninvariant(wq, ws, N, K, x, n_cols, ldx, y, ldy, seg_stages, 
     _check("spec_qmatmul_noninvariant", load().spec_qmatmul_noninvariant(
         _ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx, _ptr(y), ldy, int(seg_stages), _ptr(workspace),
         int(ws_bytes), _stream(stream)))
+
+
+def spec_qmatmul_static_scratch(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, dev_err=None, stream=None):
+    _check("spec_qmatmul_static_scratch",
+           load().spec_qmatmul_static_scratch(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx, _ptr(y), y_dt, ldy,
+                                              int(accumulate), _ptr(dev_err), _stream(stream)))
 
 
 def spec_qmatmul_debug_nt(wq, ws, N, K, x, n_cols, ldx, y, ldy, nt, workspace, ws_bytes, stream=None):

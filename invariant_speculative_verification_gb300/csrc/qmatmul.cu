@@ -42,6 +42,8 @@
 // the stand-in for the block-quantised formats named in ramgpt.org, "When
 // Lossless Speculation Stops Being Lossless on Blackwell", section
 // "Quantized Matrix Multiplication Shows the Same Class of Failure".
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -638,5 +640,69 @@ extern "C" spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *
     st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
     if (st != SPEC_OK) return st;
     return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, 1, nt, workspace, nullptr,
+                   (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------
+// spec_qmatmul_static_scratch: the invariant product with its scratch in a
+// fixed, statically sized device array instead of a caller-supplied buffer.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
+constexpr int kMaxDevices = 64;
+
+// One scratch area per device (module-scope __device__ storage is per device).
+// Its front holds the per-tile arrival counters, which must be zero when a
+// launch starts; the rest holds partial sums that each call writes before it
+// reads them.
+static __device__ __align__(256) unsigned char g_qmm_static_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of this device's scratch; looked up on the first call made
+// with that device current.
+spec_status static_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return spec::cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return spec::fail(SPEC_ERR_INVALID_ARG, "qmatmul_static_scratch: device %d", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_qmm_static_scratch);
+        if (e != cudaSuccess) return spec::cuda_status(e, "cudaGetSymbolAddress(qmatmul scratch)");
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" spec_status spec_qmatmul_static_scratch(const uint8_t *wq, const uint16_t *ws, int N, int K,
+                                                   const uint16_t *x, int n_cols, int ldx, void *y, spec_dtype y_dt,
+                                                   int ldy, int accumulate, int32_t *dev_err, spec_stream_t stream) {
+    spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
+    if (st != SPEC_OK) return st;
+    SPEC_CHECK_ARG(y_dt == SPEC_F32 || y_dt == SPEC_BF16, "qmatmul: y_dt must be SPEC_F32 or SPEC_BF16");
+    SPEC_CHECK_ARG(!(accumulate && y_dt != SPEC_F32), "qmatmul: accumulate needs SPEC_F32 output");
+    if (n_cols == 0) return SPEC_OK;
+    const int nt = pass_nt(n_cols);
+    const size_t need = ws_bytes_for(N, K, nt, 1);
+    if (need > kStaticScratchBytes)
+        return spec::fail(SPEC_ERR_WORKSPACE,
+                          "qmatmul_static_scratch: N=%d K=%d n_cols=%d needs %zu bytes of scratch, more than the "
+                          "fixed %zu; use spec_qmatmul with a workspace",
+                          N, K, n_cols, need, kStaticScratchBytes);
+    void *scratch = nullptr;
+    st = static_scratch(&scratch);
+    if (st != SPEC_OK) return st;
+    // the arrival counters must start at zero: clear them on the stream first
+    const size_t tiles = (size_t)(N + BM - 1) / BM;
+    cudaError_t e = cudaMemsetAsync(scratch, 0, tiles * sizeof(int), (cudaStream_t)stream);
+    if (e != cudaSuccess) return spec::cuda_status(e, "cudaMemsetAsync(qmatmul scratch counters)");
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, nt, scratch, dev_err,
                    (cudaStream_t)stream);
 }
