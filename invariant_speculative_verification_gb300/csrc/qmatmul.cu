@@ -281,6 +281,69 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     int i = 0;
     bool ok = true;
     long long u = ua;
+    int nh_tile = -1, nh_prev = 0, nh_touch = 0;   // thread 0: this CTA's later-segment part, if any
+
+    // y for this thread's fragments of `tile` from yrun
+    auto store_tile = [&](int tile) {
+        auto store_y = [&](int c, int row, float v) {
+            const int col = col0 + c, n = tile * BM + row;
+            if (col < n_cols && n < N) {
+                if (OUT_BF16) {
+                    reinterpret_cast<__nv_bfloat16 *>(y)[(size_t)col * ldy + n] = __float2bfloat16_rn(v);
+                } else {
+                    float *yp = reinterpret_cast<float *>(y) + (size_t)col * ldy + n;
+                    *yp = accumulate ? (*yp + v) : v;
+                }
+            }
+        };
+#pragma unroll
+        for (int ct = 0; ct < NT; ++ct) {
+            store_y(ct * 8 + t, wrow + r, yrun[ct][0]);
+            store_y(ct * 8 + t + 4, wrow + r, yrun[ct][1]);
+            store_y(ct * 8 + t, wrow + r + 8, yrun[ct][2]);
+            store_y(ct * 8 + t + 4, wrow + r + 8, yrun[ct][3]);
+        }
+    };
+    // yrun holds the fold of segments 0 .. seg_from-1 of `tile`: add the stored
+    // sums of segments seg_from .. ks-1 in ascending order, write y and reset the
+    // tile's counter (the workspace is left zeroed for the next call)
+    auto fold_tile = [&](int tile, int seg_from) {
+        const float *p0 = wsp_seg + (size_t)tile * ks * TILE_ELEMS + frag;
+        constexpr int SG = NT >= 8 ? 2 : (NT >= 2 ? 4 : 8);   // segments whose loads are in flight together
+        int sg = seg_from;
+        for (; sg + SG <= ks; sg += SG) {
+            float4 l[SG][NT];
+#pragma unroll
+            for (int q = 0; q < SG; ++q)
+#pragma unroll
+                for (int ct = 0; ct < NT; ++ct)
+                    l[q][ct] = (col0 + ct * 8 < n_cols)
+                                   ? __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)(sg + q) * TILE_ELEMS +
+                                                                             ct * NCW * 128))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < SG; ++q)
+#pragma unroll
+                for (int ct = 0; ct < NT; ++ct) {
+                    yrun[ct][0] += l[q][ct].x;
+                    yrun[ct][1] += l[q][ct].y;
+                    yrun[ct][2] += l[q][ct].z;
+                    yrun[ct][3] += l[q][ct].w;
+                }
+        }
+        for (; sg < ks; ++sg) {
+#pragma unroll
+            for (int ct = 0; ct < NT; ++ct) {
+                if (col0 + ct * 8 < n_cols) {
+                    const float4 l = __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)sg * TILE_ELEMS +
+                                                                             ct * NCW * 128));
+                    yrun[ct][0] += l.x, yrun[ct][1] += l.y, yrun[ct][2] += l.z, yrun[ct][3] += l.w;
+                }
+            }
+        }
+        store_tile(tile);
+        if (threadIdx.x == 0) counters[tile] = 0;
+    };
 
     while (u < ub) {
         const int tile = (int)(u / ks);
@@ -372,103 +435,79 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             }
         }
         // ---------------- finish this CTA's part of the tile ----------------
-        auto store_y = [&](int c, int row, float v) {
-            const int col = col0 + c, n = tile * BM + row;
-            if (col < n_cols && n < N) {
-                if (OUT_BF16) {
-                    reinterpret_cast<__nv_bfloat16 *>(y)[(size_t)col * ldy + n] = __float2bfloat16_rn(v);
-                } else {
-                    float *yp = reinterpret_cast<float *>(y) + (size_t)col * ldy + n;
-                    *yp = accumulate ? (*yp + v) : v;
-                }
-            }
-        };
         if (whole) {
-#pragma unroll
-            for (int ct = 0; ct < NT; ++ct) {
-                store_y(ct * 8 + t, wrow + r, yrun[ct][0]);
-                store_y(ct * 8 + t + 4, wrow + r, yrun[ct][1]);
-                store_y(ct * 8 + t, wrow + r + 8, yrun[ct][2]);
-                store_y(ct * 8 + t + 4, wrow + r + 8, yrun[ct][3]);
+            store_tile(tile);
+            continue;
+        }
+        const int touch = sch.cta_of(tile_u0 + ks - 1) - sch.cta_of(tile_u0) + 1;   // CTAs sharing the tile
+        if (!head) {
+            // Later segments of a shared tile: publish their sums and move on.  Whether
+            // this CTA was the last to arrive is looked at only after all its units.
+            named_sync_consumers();             // all partial stores of this CTA are issued
+            if (threadIdx.x == 0) {
+                __threadfence();                // ... and visible device-wide before the counter moves
+                nh_prev = atomicAdd(&counters[tile], 1);
+                nh_tile = tile;
+                nh_touch = touch;
             }
             continue;
         }
-        if (head) {
+        // Leading segments of a shared tile (the end of this CTA's range).  Usually
+        // every other CTA has arrived long ago: then fold at once from registers.
+        if (threadIdx.x == 0) {
+            int seen;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(counters + tile) : "memory");
+            flag[0] = (seen == touch - 1) ? 1 : 0;
+        }
+        named_sync_consumers();
+        int fold_now = flag[0];
+        if (!fold_now) {
+            // not yet: leave the prefix for whichever CTA arrives last
             float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS + frag;
 #pragma unroll
             for (int ct = 0; ct < NT; ++ct)
                 if (col0 + ct * 8 < n_cols)
                     __stcg(reinterpret_cast<float4 *>(pp + ct * NCW * 128),
                            make_float4(yrun[ct][0], yrun[ct][1], yrun[ct][2], yrun[ct][3]));
+            named_sync_consumers();             // prefix stores issued; flag[0] read by all
+            if (threadIdx.x == 0) {
+                __threadfence();
+                const int prev = atomicAdd(&counters[tile], 1);
+                if (prev == touch - 1) __threadfence();
+                flag[0] = (prev == touch - 1) ? 1 : 0;
+            }
+            named_sync_consumers();
+            fold_now = flag[0];
         }
-        // shared tile: count this CTA's arrival; the last CTA folds the segments in order
-        named_sync_consumers();                 // all partial stores of this CTA are issued
-        if (threadIdx.x == 0) {
-            __threadfence();                    // ... and visible device-wide before the counter moves
-            const int touch = sch.cta_of(tile_u0 + ks - 1) - sch.cta_of(tile_u0) + 1;
-            const int prev = atomicAdd(&counters[tile], 1);
-            *flag = (prev == touch - 1) ? 1 : 0;
+        if (fold_now) {
+            const long long head_end = min(sch.begin(blockIdx.x + 1), tile_u0 + ks);
+            fold_tile(tile, (int)(head_end - tile_u0));
         }
-        named_sync_consumers();
-        const int last = *flag;
-        if (last) {
-            __threadfence();
-            const int head_cta = sch.cta_of(tile_u0);
-            const long long head_end = min(sch.begin(head_cta + 1), tile_u0 + ks);
-            const int seg_from = (int)(head_end - tile_u0);
-            const float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS + frag;
-            const float *p0 = wsp_seg + (size_t)tile * ks * TILE_ELEMS + frag;
-            // each thread folds its own fragments: prefix, then segment sums in
-            // ascending segment order; loads of several segments are in flight together
-            constexpr int SG = NT >= 8 ? 2 : (NT >= 2 ? 4 : 8);
+        named_sync_consumers();   // flag[0] is read by everyone before it is reused
+    }
+
+    // A later-segment part that turned out to arrive last folds its tile now,
+    // the prefix and every segment sum coming from the workspace.
+    if (threadIdx.x == 0) {
+        flag[0] = (nh_tile >= 0 && nh_prev == nh_touch - 1) ? 1 : 0;
+        flag[1] = nh_tile;
+        if (flag[0]) __threadfence();
+    }
+    named_sync_consumers();
+    if (flag[0]) {
+        const int tile = flag[1];
+        const long long tile_u0 = (long long)tile * ks;
+        const int head_cta = sch.cta_of(tile_u0);
+        const long long head_end = min(sch.begin(head_cta + 1), tile_u0 + ks);
+        const float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS + frag;
 #pragma unroll
-            for (int ct = 0; ct < NT; ++ct) {
-                if (col0 + ct * 8 < n_cols) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp + ct * NCW * 128));
-                    yrun[ct][0] = v.x, yrun[ct][1] = v.y, yrun[ct][2] = v.z, yrun[ct][3] = v.w;
-                }
+        for (int ct = 0; ct < NT; ++ct) {
+            if (col0 + ct * 8 < n_cols) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp + ct * NCW * 128));
+                yrun[ct][0] = v.x, yrun[ct][1] = v.y, yrun[ct][2] = v.z, yrun[ct][3] = v.w;
             }
-            int sg = seg_from;
-            for (; sg + SG <= ks; sg += SG) {
-                float4 l[SG][NT];
-#pragma unroll
-                for (int q = 0; q < SG; ++q)
-#pragma unroll
-                    for (int ct = 0; ct < NT; ++ct)
-                        l[q][ct] = (col0 + ct * 8 < n_cols)
-                                       ? __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)(sg + q) * TILE_ELEMS +
-                                                                                 ct * NCW * 128))
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int q = 0; q < SG; ++q)
-#pragma unroll
-                    for (int ct = 0; ct < NT; ++ct) {
-                        yrun[ct][0] += l[q][ct].x;
-                        yrun[ct][1] += l[q][ct].y;
-                        yrun[ct][2] += l[q][ct].z;
-                        yrun[ct][3] += l[q][ct].w;
-                    }
-            }
-            for (; sg < ks; ++sg) {
-#pragma unroll
-                for (int ct = 0; ct < NT; ++ct) {
-                    if (col0 + ct * 8 < n_cols) {
-                        const float4 l = __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)sg * TILE_ELEMS +
-                                                                                 ct * NCW * 128));
-                        yrun[ct][0] += l.x, yrun[ct][1] += l.y, yrun[ct][2] += l.z, yrun[ct][3] += l.w;
-                    }
-                }
-            }
-#pragma unroll
-            for (int ct = 0; ct < NT; ++ct) {
-                store_y(ct * 8 + t, wrow + r, yrun[ct][0]);
-                store_y(ct * 8 + t + 4, wrow + r, yrun[ct][1]);
-                store_y(ct * 8 + t, wrow + r + 8, yrun[ct][2]);
-                store_y(ct * 8 + t + 4, wrow + r + 8, yrun[ct][3]);
-            }
-            if (threadIdx.x == 0) counters[tile] = 0;   // the workspace is left zeroed for the next call
         }
-        named_sync_consumers();   // the flag is read by everyone before it is reused
+        fold_tile(tile, (int)(head_end - tile_u0));
     }
 }
 
