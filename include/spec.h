@@ -18,9 +18,12 @@
  * Conventions for every entry point:
  *  - Pointers are DEVICE pointers owned by the caller unless stated.  The
  *    library allocates no device memory and keeps no per-call state; scratch
- *    is caller-supplied workspace sized by the matching *_workspace() call.
+ *    is caller-supplied workspace sized by the matching *_workspace() call
+ *    (spec_qmatmul_static_scratch, below, is the one exception: its scratch
+ *    is a fixed array inside the library).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
- *    default stream) and may be captured in a CUDA graph.
+ *    default stream).  All calls except spec_qmatmul_static_scratch may be
+ *    captured in a CUDA graph.
  *  - The returned status reports errors the host can see: bad shapes, NULL or
  *    misaligned pointers, short workspace, launch failure.  On any status
  *    other than SPEC_OK nothing was launched, and spec_last_error() gives a
@@ -303,7 +306,8 @@ spec_status spec_commit_accepted(int32_t *hist, int hist_cap, int32_t *hist_len,
 /* ------------------------------------------------------------------------
  * Test hook: spec_qmatmul with an explicit column-tile width nt in {1, 2, 10}
  * (columns per pass = 8 nt; the workspace must hold T * (1 + ceil(K/512))
- * * 128 * 8 nt floats after 256-byte-rounded T int counters, T = ceil(N/128)).  The result of every column must not depend on
+ * * 128 * 8 nt floats after 256-byte-rounded T int counters, T = ceil(N/128),
+ * and for nt = 10 another K/256 * 43520 bytes of packed activations).  The result of every column must not depend on
  * nt; the tests use this to show it.  y_dt is SPEC_F32.
  * ---------------------------------------------------------------------- */
 spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,

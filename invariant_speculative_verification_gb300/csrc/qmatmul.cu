@@ -55,26 +55,34 @@ constexpr int W_BOX = BM * 128;              // one 128-row x 128-byte code box 
 constexpr int MAX_NT = 10;                   // column tiles per pass (80 columns)
 constexpr int SMEM_BUDGET = 226 * 1024;
 
-// Narrow passes (<= 16 columns) stream 512-k stages; the 80-column pass uses
-// 256-k stages (its activations are 5x larger) and three activation warps.
+// Narrow passes (<= 16 columns) stream 512-k stages and prepare each stage's
+// activations in the CTA (two activation warps).  The 80-column pass uses
+// 256-k stages (its activations are 5x larger); its activations are prepared
+// once per call by a small kernel (xpack_kernel) into the workspace, in the
+// very byte layout of a stage, and each stage's part is copied in by TMA.
 // The stage size only changes how a segment is delivered, never its arithmetic.
 template <int NT>
 struct Cfg {
     static constexpr int KS = NT >= 10 ? 256 : 512;         // k per stage
     static constexpr int NBLK = KS / 32;                    // 32-k blocks per stage
     static constexpr int NWBOX = KS / 256;                  // code boxes per stage
-    static constexpr int NXW = NT >= 10 ? 3 : 2;            // activation warps (12 warps in all at most)
+    static constexpr bool XPACK = NT >= 10;                 // activations pre-packed per call
+    static constexpr int NXW = XPACK ? 0 : 2;               // activation warps
     static constexpr int THREADS = (NCW + 1 + NXW) * 32;    // + TMA warp
     static constexpr int W_BYTES = NWBOX * W_BOX;
     static constexpr int S_BYTES = BM * NBLK * 2;
     static constexpr int X_BOX = 8 * NT * 128;              // 64 k of the pass's activation columns
     static constexpr int X_BYTES = (NBLK / 2) * X_BOX;
     static constexpr int CI_BYTES = NBLK * 8 * NT * 4;      // [blocks][8 NT slots] fp32
+    // stage layout: codes | scales | activations (B-fragment order) | -136 x block sums
+    static constexpr int S_OFF = W_BYTES, X_OFF = W_BYTES + S_BYTES, CI_OFF = X_OFF + X_BYTES;
+    static constexpr int XC_BYTES = X_BYTES + CI_BYTES;     // one stage of packed activations
     static constexpr int RAW = W_BYTES + X_BYTES + S_BYTES + CI_BYTES;
     static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
     static constexpr int NS = (SMEM_BUDGET / STAGE) > 6 ? 6 : (SMEM_BUDGET / STAGE);
     static constexpr int SMEM = 1024 + NS * STAGE + 3 * NS * 8 + 64;
     static_assert(NS >= 2, "at least two stages");
+    static_assert(X_OFF % 128 == 0 && XC_BYTES % 16 == 0, "activation area alignment");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -100,6 +108,67 @@ __device__ __forceinline__ void codes_to_bf16(uint32_t w, uint32_t (&o)[4]) {
     o[3] = dev::lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);
 }
 
+// The activations of one (32-k block, column) pair of a stage: four 16-byte
+// chunks of k = kb .. kb + 31 of column col (zero past K or n_cols).
+__device__ __forceinline__ void load_pair(uint4 (&v)[4], const uint16_t *__restrict__ x, int ldx, int K, int n_cols,
+                                          int col, int kb) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[q] = make_uint4(0, 0, 0, 0);
+        if (col < n_cols && kb + 8 * q < K) v[q] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)col * ldx + kb + 8 * q));
+    }
+}
+
+// Writes pair (blk, c) of a stage: the bf16 values in MMA B-fragment order into
+// the stage's activation area xs, and -136 x the block sum into ci (the block
+// sum is the four 8-k chunk sums, each summed in k order, added in chunk order).
+template <int NT>
+__device__ __forceinline__ void put_pair(const uint4 (&v)[4], int blk, int c, uint8_t *xs, float *ci) {
+    uint8_t *row = xs + (blk >> 1) * Cfg<NT>::X_BOX + c * 128;
+    float sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+        float cs = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            cs += __uint_as_float(w4[e] << 16);
+            cs += __uint_as_float(w4[e] & 0xFFFF0000u);
+        }
+        sum = (q == 0) ? cs : sum + cs;
+        uint4 o;
+        o.x = dev::prmt(w4[0], w4[2], 0x5410);   // (x0, x4)
+        o.y = dev::prmt(w4[0], w4[2], 0x7632);   // (x1, x5)
+        o.z = dev::prmt(w4[1], w4[3], 0x5410);   // (x2, x6)
+        o.w = dev::prmt(w4[1], w4[3], 0x7632);   // (x3, x7)
+        const int chunk = (((blk & 1) * 4 + q) ^ (c & 7)) << 4;
+        *reinterpret_cast<uint4 *>(row + chunk) = o;
+    }
+    // MMA column slot g carries activation column pi(g) = (g & 1) * 4 + g / 2
+    const int cc = c & 7, slot = (cc & 3) * 2 + (cc >> 2);
+    ci[blk * 8 * NT + (c & ~7) + slot] = -136.0f * sum;
+}
+
+// Packs the activations of one pass (columns col0 .. col0 + 8 NT - 1) for every
+// stage of K into out: stage st occupies out[st * XC_BYTES ...] in the byte
+// layout of a stage's activation and block-sum areas.
+template <int NT>
+__global__ void __launch_bounds__(256) xpack_kernel(const uint16_t *__restrict__ x, int ldx, int K, int n_cols, int col0,
+                                                    uint8_t *__restrict__ out) {
+    using C = Cfg<NT>;
+    dev::pdl_wait();   // x is the preceding kernel's output; out may still be read by it
+    dev::pdl_launch_dependents();
+    constexpr int PAIRS = C::NBLK * 8 * NT;   // per stage
+    const long long p = blockIdx.x * 256ll + threadIdx.x;
+    const int st = (int)(p / PAIRS), pr = (int)(p % PAIRS);
+    if (st * C::KS >= K) return;
+    const int blk = pr / (8 * NT), c = pr % (8 * NT);
+    uint4 v[4];
+    load_pair(v, x, ldx, K, n_cols, col0 + c, st * C::KS + 32 * blk);
+    uint8_t *base = out + (size_t)st * C::XC_BYTES;
+    put_pair<NT>(v, blk, c, base, reinterpret_cast<float *>(base + C::X_BYTES));
+}
+
 __device__ __forceinline__ void named_sync_consumers() {
     asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
 }
@@ -109,7 +178,7 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ts,
            const uint16_t *__restrict__ x, int ldx, int N, int K, int n_cols, int col0, void *__restrict__ y, int ldy,
            int accumulate, Sched sch, float *__restrict__ wsp_prefix, float *__restrict__ wsp_seg,
-           int *__restrict__ counters, int32_t *dev_err) {
+           int *__restrict__ counters, const uint8_t *__restrict__ xpk, int32_t *dev_err) {
     using C = Cfg<NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -156,8 +225,20 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             dev::prefetch_tmap(&ts);
             long long iu = ua;
             int ist = 0;
-            for (int issued = 0; iu < ub; ++issued) {
+            int k0s[C::NS];   // packed-activation pass: stages whose activations are still to be copied
+            bool x_sent = false;
+            int issued = 0;
+            for (; iu < ub; ++issued) {
                 const int s = issued % C::NS;
+                if (issued == C::NS && C::XPACK) {
+                    x_sent = true;
+                    // the first NS stages' weights are on their way; the packed activations
+                    // are written by the preceding kernel, so wait for it before copying them
+                    dev::pdl_wait();
+                    for (int j = 0; j < C::NS; ++j)
+                        dev::bulk_load(smem + j * C::STAGE + C::X_OFF, xpk + (size_t)(k0s[j] / C::KS) * C::XC_BYTES,
+                                       C::XC_BYTES, &full[j]);
+                }
                 if (issued >= C::NS && !dev::mbar_wait(&empty[s], ((issued / C::NS) - 1) & 1)) {
                     dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     break;
@@ -165,19 +246,33 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                 const int tile = (int)(iu / ks);
                 const int k0 = ((int)(iu % ks) * seg_st + ist) * C::KS;
                 uint8_t *base = smem + s * C::STAGE;
-                dev::mbar_arrive_expect_tx(&full[s], C::W_BYTES + C::S_BYTES);
+                dev::mbar_arrive_expect_tx(&full[s], C::W_BYTES + C::S_BYTES + (C::XPACK ? C::XC_BYTES : 0));
 #pragma unroll
                 for (int b = 0; b < C::NWBOX; ++b)
                     dev::tma_load_2d(base + b * W_BOX, &tw, k0 / 2 + 128 * b, tile * BM, &full[s]);
-                dev::tma_load_2d(base + C::W_BYTES + C::X_BYTES, &ts, k0 / 32, tile * BM, &full[s]);
+                dev::tma_load_2d(base + C::S_OFF, &ts, k0 / 32, tile * BM, &full[s]);
+                if (C::XPACK) {
+                    if (issued < C::NS)
+                        k0s[issued] = k0;
+                    else
+                        dev::bulk_load(base + C::X_OFF, xpk + (size_t)(k0 / C::KS) * C::XC_BYTES, C::XC_BYTES, &full[s]);
+                }
                 if (++ist == unit_stages(iu)) {
                     ist = 0;
                     ++iu;
                 }
             }
+            if (C::XPACK && !x_sent) {
+                // no more stages than slots: copy the activations of all of them now
+                dev::pdl_wait();
+                for (int j = 0; j < issued; ++j)
+                    dev::bulk_load(smem + j * C::STAGE + C::X_OFF, xpk + (size_t)(k0s[j] / C::KS) * C::XC_BYTES,
+                                   C::XC_BYTES, &full[j]);
+            }
         }
         return;
     }
+    if constexpr (!C::XPACK) {
     if (warp > NCW) {
         // ======================== activation warps ========================
         // warp NCW + 1 + h prepares stages i with i % C::NXW == h: it reads the
@@ -198,10 +293,9 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             if (i % C::NXW != h) continue;
             const int s = i % C::NS;
             bool slot_free = (i < C::NS);   // the slot's previous stage must be released before writing
-            uint8_t *xs = smem + s * C::STAGE + C::W_BYTES;
-            float *ci = reinterpret_cast<float *>(smem + s * C::STAGE + C::W_BYTES + C::X_BYTES + C::S_BYTES);
-            // (block, column) pairs p = lane + 32 j; each is four 16-byte chunks of k = 32 blk .. +31;
-            // chunk sums in k order, block sum = chunk sums in order
+            uint8_t *xs = smem + s * C::STAGE + C::X_OFF;
+            float *ci = reinterpret_cast<float *>(smem + s * C::STAGE + C::CI_OFF);
+            // (block, column) pairs p = lane + 32 j
             constexpr int PAIRS = C::NBLK * 8 * NT / 32;   // per lane
             constexpr int GROUP = 4;                  // pairs whose loads are in flight together
 #pragma unroll 1
@@ -211,13 +305,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                 for (int jj = 0; jj < GROUP; ++jj) {
                     const int p = lane + 32 * (j0 + jj);
                     const int blk = p / (8 * NT), c = p % (8 * NT);
-                    const int col = col0 + c, kb = k0 + 32 * blk;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        v[jj][q] = make_uint4(0, 0, 0, 0);
-                        if (col < n_cols && kb + 8 * q < K)
-                            v[jj][q] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)col * ldx + kb + 8 * q));
-                    }
+                    load_pair(v[jj], x, ldx, K, n_cols, col0 + c, k0 + 32 * blk);
                 }
                 if (!slot_free) {   // loads are in flight; now wait for the consumers' release
                     int got = 1;
@@ -232,30 +320,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
 #pragma unroll
                 for (int jj = 0; jj < GROUP; ++jj) {
                     const int p = lane + 32 * (j0 + jj);
-                    const int blk = p / (8 * NT), c = p % (8 * NT);
-                    uint8_t *row = xs + (blk >> 1) * C::X_BOX + c * 128;
-                    float sum = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t w4[4] = {v[jj][q].x, v[jj][q].y, v[jj][q].z, v[jj][q].w};
-                        float cs = 0.f;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            cs += __uint_as_float(w4[e] << 16);
-                            cs += __uint_as_float(w4[e] & 0xFFFF0000u);
-                        }
-                        sum = (q == 0) ? cs : sum + cs;
-                        uint4 o;
-                        o.x = dev::prmt(w4[0], w4[2], 0x5410);   // (x0, x4)
-                        o.y = dev::prmt(w4[0], w4[2], 0x7632);   // (x1, x5)
-                        o.z = dev::prmt(w4[1], w4[3], 0x5410);   // (x2, x6)
-                        o.w = dev::prmt(w4[1], w4[3], 0x7632);   // (x3, x7)
-                        const int chunk = (((blk & 1) * 4 + q) ^ (c & 7)) << 4;
-                        *reinterpret_cast<uint4 *>(row + chunk) = o;
-                    }
-                    // MMA column slot g carries activation column pi(g) = (g & 1) * 4 + g / 2
-                    const int cc = c & 7, slot = (cc & 3) * 2 + (cc >> 2);
-                    ci[blk * 8 * NT + (c & ~7) + slot] = -136.0f * sum;
+                    put_pair<NT>(v[jj], p / (8 * NT), p % (8 * NT), xs, ci);
                 }
             }
             int got = 1;
@@ -269,6 +334,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             if (lane == 0) dev::mbar_arrive(&ready[s]);
         }
         return;
+    }
     }
 
     // ============================ consumers ============================
@@ -361,14 +427,14 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             for (int ct = 0; ct < NT; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
             for (int st = 0; st < nstg; ++st, ++i) {
                 const int s = i % C::NS;
-                if (ok && !dev::mbar_wait(&ready[s], (i / C::NS) & 1)) {
+                if (ok && !dev::mbar_wait(C::XPACK ? &full[s] : &ready[s], (i / C::NS) & 1)) {
                     dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     ok = false;
                 }
                 const uint32_t wbase = dev::smem_u32(smem + s * C::STAGE);
-                const uint32_t xbase = wbase + C::W_BYTES;
-                const uint32_t sbase = xbase + C::X_BYTES;
-                const uint32_t cbase = sbase + C::S_BYTES;
+                const uint32_t xbase = wbase + C::X_OFF;
+                const uint32_t sbase = wbase + C::S_OFF;
+                const uint32_t cbase = wbase + C::CI_OFF;
                 constexpr int BP_UNROLL = NT > 4 ? 1 : C::NBLK / 2;
 #pragma unroll BP_UNROLL
                 for (int bp = 0; bp < C::NBLK / 2; ++bp) {
@@ -536,6 +602,14 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     int *counters = reinterpret_cast<int *>(workspace);
     float *prefix = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + cnt_bytes);
     float *segs = prefix + tiles * BM * 8 * NT;
+    const uint8_t *xpk = reinterpret_cast<const uint8_t *>(segs + tiles * sch.ks * BM * 8 * NT);
+    if constexpr (C::XPACK) {
+        // this pass's activations, packed once for every CTA (into the workspace after the partial sums)
+        const long long pairs = (long long)(K / C::KS) * C::NBLK * 8 * NT;
+        cudaError_t e = spec::launch_pdl(xpack_kernel<NT>, dim3((unsigned)((pairs + 255) / 256)), dim3(256), 0, stream,
+                                         x, ldx, K, n_cols, col0, const_cast<uint8_t *>(xpk));
+        if (e != cudaSuccess) return spec::cuda_status(e, "qmm activation pack launch");
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sch.G);
     cfg.blockDim = dim3(C::THREADS);
@@ -547,7 +621,7 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, sch, prefix,
-                                       segs, counters, dev_err);
+                                       segs, counters, xpk, dev_err);
     return spec::cuda_status(e, "qmm launch");
 }
 
@@ -556,7 +630,9 @@ int pass_nt(int n_cols) { return n_cols <= 8 ? 1 : (n_cols <= 16 ? 2 : MAX_NT); 
 size_t ws_bytes_for(int N, int K, int nt, int seg512) {
     const size_t tiles = (size_t)(N + BM - 1) / BM;
     const size_t cnt = ((tiles * sizeof(int)) + 255) & ~size_t(255);
-    return cnt + tiles * (1 + (size_t)n_segments(K, seg512 * SEG_K)) * BM * 8 * nt * sizeof(float);
+    // the 80-column pass also keeps its packed activations: K / 256 stages of XC_BYTES
+    const size_t packed = nt >= MAX_NT ? (size_t)(K / Cfg<MAX_NT>::KS) * Cfg<MAX_NT>::XC_BYTES : 0;
+    return cnt + tiles * (1 + (size_t)n_segments(K, seg512 * SEG_K)) * BM * 8 * nt * sizeof(float) + packed;
 }
 
 spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,

@@ -52,7 +52,8 @@ def run(case_or_w, x_dev, n_cols, N, K, ldx=None, out_dt=0, y=None, accumulate=0
 
 def debug_nt_ws(N, K, nt):
     tiles = (N + 127) // 128
-    return ((tiles * 4 + 255) // 256) * 256 + tiles * (1 + (K + 511) // 512) * 128 * 8 * nt * 4
+    packed = (K // 256) * 43520 if nt == 10 else 0   # the 80-column pass's packed activations
+    return ((tiles * 4 + 255) // 256) * 256 + tiles * (1 + (K + 511) // 512) * 128 * 8 * nt * 4 + packed
 
 
 @pytest.fixture(scope="module")
