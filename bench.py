@@ -267,6 +267,146 @@ def attention_invariance(torch, L):
     return cases, passed
 
 
+def graph_time(torch, body, n_calls, reps=5):
+    """Best per-call device time of `body` (n_calls launches) captured in a CUDA graph."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        body()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        body()
+    g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / n_calls
+        best = t if best is None else min(best, t)
+    return best
+
+
+def kernel_rooflines(torch, L, hbm_peak):
+    """Per-call time and HBM roofline fraction of attention (K2+K3), greedy verify (K4) and KV
+    compaction (K5) on the attention and ragged-verify workloads; inputs rotated over >= 4x L2
+    where they are larger than a few MB."""
+    dev = torch.device("cuda")
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20)
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    out = {}
+    # K2 + K3: one sequence, 40/8 heads of 128, bf16 K/V, scale folded into Q
+    att = {}
+    Hq, Hkv, D = 40, 8, 128
+    for Lk in (1024, 4096, 16384):
+        for n in (1, 4, 8):
+            c = synth.attention_case(1003 + Lk + 10 * n, rows=[n], ctx=[Lk - n], Hq=Hq, Hkv=Hkv, D=D,
+                                     dt=synth.DT_BF16, q_std=1 / math.sqrt(D), scale=1.0)
+            q, bt = up(c.q), up(c.block_table)
+            kv_bytes = 4 * Hkv * D * Lk
+            copies = max(2, math.ceil(4 * l2 / kv_bytes))
+            k0, v0 = up(c.k_cache), up(c.v_cache)
+            ks = [k0] + [k0.clone() for _ in range(copies - 1)]
+            vs = [v0] + [v0.clone() for _ in range(copies - 1)]
+            pages = c.k_cache.shape[0]
+            wsb = L.spec_flash_decode_workspace(n, Hq, D, Lk)
+            wsp = torch.empty(wsb // 4 + 64, dtype=torch.float32, device=dev)
+            o = torch.zeros((n, Hq, D), dtype=torch.float32, device=dev)
+            ctx_t = torch.tensor([Lk - n], dtype=torch.int32, device=dev)
+            cu_t = torch.tensor([0, n], dtype=torch.int32, device=dev)
+
+            def body():
+                for i in range(copies):
+                    L.spec_flash_decode(q, L.SPEC_BF16, Hq, Hkv, D, 1.0, ks[i], vs[i], pages, bt,
+                                        c.block_table.shape[1], ctx_t, cu_t, 1, n, Lk, o, L.SPEC_F32, wsp, wsb, None)
+
+            t = graph_time(torch, body, copies)
+            algo = kv_bytes + n * Hq * D * (2 + 4)
+            att[f"L{Lk}_w{n}"] = {"us": round(t * 1e6, 2), "GBps": round(algo / t / 1e9, 1),
+                                  "frac": round(algo / t / 1e9 / hbm_peak, 3)}
+            del ks, vs, k0, v0
+            torch.cuda.empty_cache()
+    out["attention"] = {"workload": "1 seq, 40/8 heads x 128, bf16 K/V, widths 1/4/8",
+                        "algorithmic_bytes": "4*Hkv*D*L (K+V) + Q/out", "per_case": att}
+
+    # K4: 64 sequences, drafts U{1..7}, bf16 logits over 152064, sigma 2, 1% planted near-ties
+    g = np.random.default_rng(1004)
+    dl = g.integers(1, 8, size=64)
+    vc = synth.verify_case(1004, dl, 152064, synth.DT_BF16, sigma=2.0, tie_frac=0.01)
+    lg0 = up(vc.logits)
+    lbytes = lg0.numel() * 2
+    copies = max(2, math.ceil(4 * l2 / lbytes))
+    lgs = [lg0] + [lg0.clone() for _ in range(copies - 1)]
+    cu, dr, cs = up(vc.cu_rows), up(vc.drafts), up(vc.ctx_start)
+    am = torch.zeros(vc.R, dtype=torch.int32, device=dev)
+    acc, cor, cn = (torch.zeros(vc.S, dtype=torch.int32, device=dev) for _ in range(3))
+    vwb = L.spec_verify_greedy_workspace(vc.R, vc.V)
+    vws = torch.empty(vwb // 8 + 2, dtype=torch.int64, device=dev)
+
+    def vbody():
+        for i in range(copies):
+            L.spec_verify_greedy(lgs[i], L.SPEC_BF16, vc.V, cu, vc.S, vc.R, dr, cs, am, acc, cor, cn, vws, vwb, None)
+
+    t = graph_time(torch, vbody, copies)
+    out["verify"] = {"workload": f"64 seqs, R={vc.R} rows x V=152064 bf16", "us": round(t * 1e6, 2),
+                     "GBps": round(lbytes / t / 1e9, 1), "frac": round(lbytes / t / 1e9 / hbm_peak, 3),
+                     "algorithmic_bytes": "R*V*2"}
+    torch.cuda.synchronize()
+    accepted = acc.clone()
+    del lgs, lg0
+    torch.cuda.empty_cache()
+
+    # K5: the same 64 sequences, 32 KV heads x 128 bf16, contexts U[256, 8192], pages shuffled
+    Hkv5, D5 = 32, 128
+    ctx = vc.ctx_start.astype(np.int64)
+    lens = ctx + dl + 1
+    nblk = (lens + 15) // 16
+    max_blocks = int(nblk.max())
+    total = int(nblk.sum())
+    perm = g.permutation(total).astype(np.int32)
+    bt = np.full((64, max_blocks), -1, dtype=np.int32)
+    o_ = 0
+    for s_ in range(64):
+        bt[s_, :nblk[s_]] = perm[o_:o_ + nblk[s_]]
+        o_ += nblk[s_]
+    kc = torch.empty((total, Hkv5, 16, D5), dtype=torch.int16, device=dev)
+    vcache = torch.empty_like(kc)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1005)
+    kst = torch.randint(-20000, 20000, (vc.R, Hkv5, D5), generator=gen, device=dev, dtype=torch.int32).to(torch.int16)
+    vst = torch.randint(-20000, 20000, (vc.R, Hkv5, D5), generator=gen, device=dev, dtype=torch.int32).to(torch.int16)
+    btd = up(bt)
+    cuk = torch.zeros(65, dtype=torch.int32, device=dev)
+    src = torch.zeros(vc.R, dtype=torch.int32, device=dev)
+    dst = torch.zeros(vc.R, dtype=torch.int64, device=dev)
+    reps = 20
+
+    def cbody():
+        for _ in range(reps):
+            L.spec_kv_compact(kst, vst, kc, vcache, Hkv5, D5, total, btd, max_blocks, cs, accepted, cu, 64, vc.R,
+                              cuk, src, dst, None)
+
+    t = graph_time(torch, cbody, reps)
+    kept = int(accepted.sum().item()) + 64
+    cbytes = 2 * 2 * kept * Hkv5 * D5 * 2
+    out["kv_compact"] = {"workload": f"64 seqs, {kept} kept rows x 32 heads x 128 bf16 (K and V)",
+                         "us": round(t * 1e6, 2), "GBps": round(cbytes / t / 1e9, 1),
+                         "frac": round(cbytes / t / 1e9 / hbm_peak, 3),
+                         "algorithmic_bytes": "2 (read+write) * 2 (K,V) * kept * Hkv * D * 2",
+                         "note": "6 MB per call stays in L2: launch- and latency-bound"}
+    del kc, vcache
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -398,6 +538,7 @@ def run_ours(args):
 
     # ---- GEMV sweep + invariance ----
     sweep, qc, qp = qgemv_sweep(torch, L, hbm_peak)
+    kernels = kernel_rooflines(torch, L, hbm_peak)
     ac, ap = attention_invariance(torch, L)
     inv_cases = qc + ac + N_SEQ
     inv_pass = qp + ap + equal_seqs
@@ -418,6 +559,7 @@ def run_ours(args):
                        "equivalence": equal_seqs / N_SEQ, "dev_err": [err4, err0, err_steps]},
         "invariance": {"cases": inv_cases, "passed": inv_pass, "pct": round(100.0 * inv_pass / inv_cases, 2)},
         "qgemv": sweep,
+        "kernels": kernels,
         "roofline": roof,
         "e2e": {"value": round(e2e_tokens / te, 1), "unit": "tok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -6,19 +6,23 @@
 // Here every row's reduction structure is fixed by its own position p:
 //  * keys are cut into chunks of CHUNK = 256 (a constant), chunk c covers keys
 //    [256c, 256c + 255]; row p has partials for chunks 0 .. p / 256;
-//  * inside a chunk, keys are visited in sub-tiles of 64 in ascending order
-//    with an online softmax (running max m, sum l, weighted values o);
+//  * a chunk is cut into sub-tiles of 64 keys; for each sub-tile w whose first
+//    key is <= p the row gets (m_w, l_w, o_w): the max of its visible scores,
+//    the sum of 2^(s - m_w) and the 2^(s - m_w)-weighted values;
+//  * the chunk partial merges those sub-tiles in ascending w:
+//    m = max_w m_w, l = sum_w l_w 2^(m_w - m), o = sum_w o_w 2^(m_w - m);
 //  * K3 combines a row's chunk partials in ascending chunk order.
-// The other rows of the call only decide which warp or CTA runs a row and how
-// many fully masked sub-tiles it also visits; a fully masked sub-tile leaves
-// (m, l, o) bit-unchanged (rescale factor exactly 1, probabilities exactly 0).
+// The other rows of the call only decide which warp, round or CTA handles a
+// row; sub-tiles past p are left out of the row's merge altogether.
 //
 // K2 (attn_partial_kernel): one CTA per (chunk, kv head, sequence).  A
-// producer thread streams the chunk's K and V pages with 4-D TMA boxes
-// (128B swizzle) into a ring of 64-key slots; four consumer warps each own a
-// 16-row M-tile of (query row, grouped head) pairs and run S = Q K^T and
-// O += P V on mma.sync m16n8k16 with fp32 accumulation.  P enters the PV
-// product as a hi + lo pair of 16-bit values so its rounding error is ~2^-17.
+// producer thread copies the chunk's K and V pages (4-D TMA boxes, 128B
+// swizzle) into four resident 64-key slots; consumer warp w owns sub-tile w
+// and, for each 16-row M-tile of (query row, grouped head) pairs, runs
+// S = Q K^T and O = P V on mma.sync m16n8k16 with fp32 accumulation (P enters
+// the PV product as a hi + lo pair of 16-bit values, rounding error ~2^-17),
+// leaving its (m_w, l_w, o_w) in shared memory; the four warps then merge
+// them and write the chunk partials.
 // K3 (attn_combine_kernel): one warp per (row, head).
 #include "common.cuh"
 
@@ -27,17 +31,22 @@ namespace {
 constexpr int CHUNK = 256;
 constexpr int SUB = 64;
 constexpr int PAGE = 16;
-constexpr int NCONS = 4;
+constexpr int NCONS = CHUNK / SUB;   // one consumer warp per sub-tile
 constexpr int THREADS = (NCONS + 1) * 32;
 constexpr float LOG2E = 1.4426950408889634f;
 
 template <int D>
 struct ACfg {
     static constexpr int HALVES = D / 64;                 // 64-wide d boxes per key row
-    static constexpr int KV_BYTES = HALVES * SUB * 128;   // one of K or V for a slot
+    static constexpr int KV_BYTES = HALVES * SUB * 128;   // one of K or V for a sub-tile
     static constexpr int SLOT = 2 * KV_BYTES;
-    static constexpr int NSLOT = (D == 128) ? 3 : 5;
-    static constexpr int SMEM = 1024 + NSLOT * SLOT + 2 * NSLOT * 8;
+    static constexpr int MR = D == 128 ? 2 : 4;           // M-tiles per round
+    static constexpr int OSTR = D + 4;                    // padded row stride of a sub-tile's o (floats)
+    static constexpr int PART = 16 * OSTR * 4 + 16 * 8;   // o and (m, l) of one (M-tile, sub-tile)
+    static constexpr int PART_OFF = NCONS * SLOT;
+    static constexpr int BAR_OFF = PART_OFF + MR * NCONS * PART;
+    static constexpr int SMEM = 1024 + BAR_OFF + NCONS * 8;
+    static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 template <bool BF16>
@@ -91,8 +100,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     using C = ACfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NSLOT * C::SLOT);
-    uint64_t *empty = full + C::NSLOT;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
 
     const int c = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -116,234 +124,252 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     const int G = Hq / Hkv;
     const int i0 = max(0, kbeg - ctx);  // first row whose position reaches this chunk
     const int mrows = (rows - i0) * G;
-    const int rounds = (mrows + 16 * NCONS - 1) / (16 * NCONS);
+    const int mtiles = (mrows + 15) / 16;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < C::NSLOT; ++b) {
-            dev::mbar_init(&full[b], 1);
-            dev::mbar_init(&empty[b], NCONS);
-        }
+        for (int b = 0; b < NCONS; ++b) dev::mbar_init(&full[b], 1);
         dev::fence_barrier_init();
     }
     __syncthreads();
-    const int total = rounds * nsub;
 
     if (warp == NCONS) {
-        // ---------------- producer ----------------
+        // ---------------- producer: the chunk's sub-tiles into their slots ----------------
+        // The chunk's (at most 16) block-table entries are read by 16 lanes at once;
+        // lane 0 then issues every copy.
+        const int32_t *bt = block_table + (size_t)s * max_blocks;
+        const int pg_first = kbeg / PAGE, pg_end = (kend + PAGE - 1) / PAGE;
+        int my_phys = 0;
+        if (lane < pg_end - pg_first) {
+            my_phys = bt[pg_first + lane];
+            if (my_phys < 0 || my_phys >= num_pages) {
+                dev::report(dev_err, SPEC_DEVERR_BLOCK_TABLE);
+                my_phys = 0;
+            }
+        }
         if (lane == 0) {
             dev::prefetch_tmap(&tk);
             dev::prefetch_tmap(&tv);
-            const int32_t *bt = block_table + (size_t)s * max_blocks;
-            int issued = 0;
-            for (int it = 0; it < total; ++it) {
-                const int b = it % C::NSLOT;
-                if (it >= C::NSLOT && !dev::mbar_wait(&empty[b], ((it / C::NSLOT) - 1) & 1)) {
-                    dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
-                    break;
-                }
-                const int sub = it % nsub;
-                const int key0 = kbeg + sub * SUB;
-                const int pg0 = key0 / PAGE;
-                const int pg1 = min(pg0 + SUB / PAGE, (len + PAGE - 1) / PAGE);
-                uint8_t *kdst = smem + b * C::SLOT;
-                uint8_t *vdst = kdst + C::KV_BYTES;
-                dev::mbar_arrive_expect_tx(&full[b], (uint32_t)((pg1 - pg0) * C::HALVES * 2 * 2048));
-                for (int pg = pg0; pg < pg1; ++pg) {
-                    int phys = bt[pg];
-                    if (phys < 0 || phys >= num_pages) {
-                        dev::report(dev_err, SPEC_DEVERR_BLOCK_TABLE);
-                        phys = 0;
-                    }
+        }
+        for (int w = 0; w < nsub; ++w) {
+            const int key0 = kbeg + w * SUB;
+            const int pg0 = key0 / PAGE;
+            const int pg1 = min(pg0 + SUB / PAGE, pg_end);
+            uint8_t *kdst = smem + w * C::SLOT;
+            uint8_t *vdst = kdst + C::KV_BYTES;
+            if (lane == 0)
+                dev::mbar_arrive_expect_tx(&full[w], (uint32_t)((pg1 - pg0) * C::HALVES * 2 * 2048));
+            for (int pg = pg0; pg < pg1; ++pg) {
+                const int phys = __shfl_sync(0xffffffffu, my_phys, pg - pg_first);
+                if (lane == 0) {
                     const int off = (pg - pg0) * 2048;
 #pragma unroll
                     for (int hh = 0; hh < C::HALVES; ++hh) {
-                        dev::tma_load_4d(kdst + hh * SUB * 128 + off, &tk, hh * 64, 0, kvh, phys, &full[b]);
-                        dev::tma_load_4d(vdst + hh * SUB * 128 + off, &tv, hh * 64, 0, kvh, phys, &full[b]);
+                        dev::tma_load_4d(kdst + hh * SUB * 128 + off, &tk, hh * 64, 0, kvh, phys, &full[w]);
+                        dev::tma_load_4d(vdst + hh * SUB * 128 + off, &tv, hh * 64, 0, kvh, phys, &full[w]);
                     }
                 }
-                issued = it + 1;
             }
-            for (int it = (issued > C::NSLOT ? issued - C::NSLOT : 0); it < issued; ++it)
-                if (!dev::mbar_wait(&full[it % C::NSLOT], (it / C::NSLOT) & 1))
-                    dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
         }
+        // the CTA must not exit with copies in flight
+        if (lane == 0)
+            for (int w = 0; w < nsub; ++w)
+                if (!dev::mbar_wait(&full[w], 0)) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
         return;
     }
 
-    // ---------------- consumers ----------------
+    // ---------------- consumers: warp w owns sub-tile w ----------------
+    const int w = warp;
     const int g = lane >> 2, t = lane & 3;
-    int it = 0;
+    const int key0 = kbeg + w * SUB;
+    const bool has_sub = w < nsub;
     bool ok = true;
-    for (int ro = 0; ro < rounds; ++ro) {
-        const int mt = ro * NCONS + warp;
-        const bool active = (mt * 16 < mrows);
-        // rows of this lane: m0 = 16 mt + g, m1 = m0 + 8
-        int pos[2];
-        bool valid[2];
-        size_t qoff[2];
-        int orow[2], ohead[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int m = mt * 16 + g + 8 * h;
-            valid[h] = active && m < mrows;
-            const int i = i0 + (valid[h] ? m / G : 0);
-            const int gg = valid[h] ? m % G : 0;
-            pos[h] = ctx + i;
-            orow[h] = r0 + i;
-            ohead[h] = kvh * G + gg;
-            qoff[h] = ((size_t)orow[h] * Hq + ohead[h]) * D;
-        }
-        // Q fragments for all k-steps (A operand): row m0 / m1, d = 16 kk + 2t (+8)
-        uint32_t qa[D / 16][4];
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const int d0 = 16 * kk + 2 * t;
-            qa[kk][0] = valid[0] ? *reinterpret_cast<const uint32_t *>(q + qoff[0] + d0) : 0u;
-            qa[kk][1] = valid[1] ? *reinterpret_cast<const uint32_t *>(q + qoff[1] + d0) : 0u;
-            qa[kk][2] = valid[0] ? *reinterpret_cast<const uint32_t *>(q + qoff[0] + d0 + 8) : 0u;
-            qa[kk][3] = valid[1] ? *reinterpret_cast<const uint32_t *>(q + qoff[1] + d0 + 8) : 0u;
-        }
-        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-        float o[D / 8][4];
-#pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    uint8_t *kslot = smem + w * C::SLOT;
+    uint8_t *vslot = kslot + C::KV_BYTES;
+    bool waited = false;   // the slot is waited for after the first Q loads are in flight
+    const uint32_t kb = dev::smem_u32(kslot), vb = dev::smem_u32(vslot);
 
-        for (int sub = 0; sub < nsub; ++sub, ++it) {
-            const int b = it % C::NSLOT;
-            if (ok && !dev::mbar_wait(&full[b], (it / C::NSLOT) & 1)) {
-                dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
-                ok = false;  // keep walking the loop so named barriers stay matched
-            }
-            const int key0 = kbeg + sub * SUB;
-            uint8_t *kslot = smem + b * C::SLOT;
-            uint8_t *vslot = kslot + C::KV_BYTES;
-            const int nvalid = len - key0;  // keys of this slot inside the sequence
-            if (nvalid < SUB) {
-                // V rows past the sequence end hold stale or unloaded data: zero them so
-                // that 0-probability keys contribute exactly 0 to P V
-                const int tid = threadIdx.x;
-                for (int idx = tid; idx < C::HALVES * (SUB - nvalid) * 8; idx += NCONS * 32) {
-                    const int hh = idx / ((SUB - nvalid) * 8);
-                    const int rem = idx % ((SUB - nvalid) * 8);
-                    const int key = nvalid + rem / 8, ch = rem % 8;
-                    *reinterpret_cast<uint4 *>(vslot + hh * SUB * 128 + key * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-                }
-                dev::fence_proxy_async();
-                asm volatile("bar.sync 1, %0;" ::"n"(NCONS * 32) : "memory");
-            }
-            if (active && ok) {
-                const uint32_t kb = dev::smem_u32(kslot), vb = dev::smem_u32(vslot);
-                // ---- S = Q K^T (16 rows x 64 keys) ----
-                float sc[8][4];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int hh = (16 * kk) / 64;
-                    const int cbase = ((16 * kk) % 64) / 8;
-#pragma unroll
-                    for (int jp = 0; jp < 4; ++jp) {
-                        const int mi = lane >> 3;
-                        const int key = 8 * (2 * jp + (mi >> 1)) + (lane & 7);
-                        const int ch = cbase + (mi & 1);
-                        uint32_t b0, b1, b2, b3;
-                        dev::ldmatrix_x4(b0, b1, b2, b3, kb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
-                        mma16<BF16>(sc[2 * jp], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1, sc[2 * jp]);
-                        mma16<BF16>(sc[2 * jp + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3,
-                                    sc[2 * jp + 1]);
-                    }
-                }
-                // ---- mask, scale to log2 units, online softmax ----
-                float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int h = e >> 1;
-                        const int key = key0 + 8 * j + 2 * t + (e & 1);
-                        const bool vis = valid[h] && key <= pos[h];
-                        const float v = vis ? sc[j][e] * scale_log2 : -INFINITY;
-                        sc[j][e] = v;
-                        mx[h] = fmaxf(mx[h], v);
-                    }
-                }
-                float alpha[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                    const float mnew = fmaxf(m_run[h], mx[h]);
-                    alpha[h] = (mnew == m_run[h]) ? 1.0f : exp2f(m_run[h] - mnew);
-                    m_run[h] = mnew;
-                }
-                float rs[2] = {0.f, 0.f};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int h = e >> 1;
-                        const float p = (m_run[h] == -INFINITY) ? 0.f : exp2f(sc[j][e] - m_run[h]);
-                        sc[j][e] = p;
-                        rs[h] += p;
-                    }
-                }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 1);
-                    rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 2);
-                    l_run[h] = l_run[h] * alpha[h] + rs[h];
-                }
-#pragma unroll
-                for (int nd = 0; nd < D / 8; ++nd) {
-                    o[nd][0] *= alpha[0];
-                    o[nd][1] *= alpha[0];
-                    o[nd][2] *= alpha[1];
-                    o[nd][3] *= alpha[1];
-                }
-                // ---- O += P V with P = hi + lo ----
-#pragma unroll
-                for (int kk = 0; kk < SUB / 16; ++kk) {
-                    uint32_t ph[4], pl[4];
-                    float r00, r01, r10, r11, r20, r21, r30, r31;
-                    ph[0] = pack_hi<BF16>(sc[2 * kk][0], sc[2 * kk][1], r00, r01);
-                    ph[1] = pack_hi<BF16>(sc[2 * kk][2], sc[2 * kk][3], r10, r11);
-                    ph[2] = pack_hi<BF16>(sc[2 * kk + 1][0], sc[2 * kk + 1][1], r20, r21);
-                    ph[3] = pack_hi<BF16>(sc[2 * kk + 1][2], sc[2 * kk + 1][3], r30, r31);
-                    pl[0] = pack2<BF16>(r00, r01);
-                    pl[1] = pack2<BF16>(r10, r11);
-                    pl[2] = pack2<BF16>(r20, r21);
-                    pl[3] = pack2<BF16>(r30, r31);
-#pragma unroll
-                    for (int ndp = 0; ndp < D / 16; ++ndp) {
-                        const int mi = lane >> 3;
-                        const int key = 16 * kk + 8 * (mi & 1) + (lane & 7);
-                        const int dch = 2 * ndp + (mi >> 1);     // 8-wide d chunk
-                        const int hh = dch / 8, ch = dch % 8;
-                        uint32_t b0, b1, b2, b3;
-                        dev::ldmatrix_x4_trans(b0, b1, b2, b3, vb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
-                        mma16<BF16>(o[2 * ndp], ph[0], ph[1], ph[2], ph[3], b0, b1, o[2 * ndp]);
-                        mma16<BF16>(o[2 * ndp], pl[0], pl[1], pl[2], pl[3], b0, b1, o[2 * ndp]);
-                        mma16<BF16>(o[2 * ndp + 1], ph[0], ph[1], ph[2], ph[3], b2, b3, o[2 * ndp + 1]);
-                        mma16<BF16>(o[2 * ndp + 1], pl[0], pl[1], pl[2], pl[3], b2, b3, o[2 * ndp + 1]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) dev::mbar_arrive(&empty[b]);
-        }
-        // ---- write this chunk's partial for the lane's rows ----
-        if (active && ok) {
+    for (int mt0 = 0; mt0 < mtiles; mt0 += C::MR) {
+        // ---- each warp: (m_w, l_w, o_w) of its sub-tile for up to MR M-tiles ----
+        for (int j = 0; j < C::MR && mt0 + j < mtiles && has_sub && ok; ++j) {
+            const int mt = mt0 + j;
+            int pos[2];
+            bool valid[2];
+            size_t qoff[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                if (!valid[h]) continue;
-                const size_t pidx = ((size_t)orow[h] * Hq + ohead[h]) * nc_max + c;
-                if (t == 0) part_ml[pidx] = make_float2(m_run[h], l_run[h]);
-                float *op = part_o + pidx * D;
+                const int m = mt * 16 + g + 8 * h;
+                valid[h] = m < mrows;
+                const int i = i0 + (valid[h] ? m / G : 0);
+                const int gg = valid[h] ? m % G : 0;
+                pos[h] = ctx + i;
+                qoff[h] = ((size_t)(r0 + i) * Hq + kvh * G + gg) * D;
+            }
+            // Q fragments for all k-steps (A operand): row m0 / m1, d = 16 kk + 2t (+8), all loads in flight together
+            uint32_t qa[D / 16][4];
 #pragma unroll
-                for (int nd = 0; nd < D / 8; ++nd)
-                    *reinterpret_cast<float2 *>(op + 8 * nd + 2 * t) = make_float2(o[nd][2 * h], o[nd][2 * h + 1]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int d0 = 16 * kk + 2 * t;
+                qa[kk][0] = valid[0] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[0] + d0)) : 0u;
+                qa[kk][1] = valid[1] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[1] + d0)) : 0u;
+                qa[kk][2] = valid[0] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[0] + d0 + 8)) : 0u;
+                qa[kk][3] = valid[1] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[1] + d0 + 8)) : 0u;
+            }
+            if (!waited) {
+                waited = true;
+                if (!dev::mbar_wait(&full[w], 0)) {
+                    if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                const int nvalid = len - key0;  // keys of this slot inside the sequence
+                if (nvalid < SUB) {
+                    // V rows past the sequence end hold stale or unloaded data: zero them so
+                    // that 0-probability keys contribute exactly 0 to P V
+                    for (int idx = lane; idx < C::HALVES * (SUB - nvalid) * 8; idx += 32) {
+                        const int hh = idx / ((SUB - nvalid) * 8);
+                        const int rem = idx % ((SUB - nvalid) * 8);
+                        const int key = nvalid + rem / 8, ch = rem % 8;
+                        *reinterpret_cast<uint4 *>(vslot + hh * SUB * 128 + key * 128 + ch * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+                __syncwarp();
+            }
+            // ---- S = Q K^T (16 rows x 64 keys) ----
+            float sc[8][4];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) sc[jj][0] = sc[jj][1] = sc[jj][2] = sc[jj][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t qa0 = qa[kk][0], qa1 = qa[kk][1], qa2 = qa[kk][2], qa3 = qa[kk][3];
+                const int hh = (16 * kk) / 64;
+                const int cbase = ((16 * kk) % 64) / 8;
+#pragma unroll
+                for (int jp = 0; jp < 4; ++jp) {
+                    const int mi = lane >> 3;
+                    const int key = 8 * (2 * jp + (mi >> 1)) + (lane & 7);
+                    const int ch = cbase + (mi & 1);
+                    uint32_t b0, b1, b2, b3;
+                    dev::ldmatrix_x4(b0, b1, b2, b3, kb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
+                    mma16<BF16>(sc[2 * jp], qa0, qa1, qa2, qa3, b0, b1, sc[2 * jp]);
+                    mma16<BF16>(sc[2 * jp + 1], qa0, qa1, qa2, qa3, b2, b3, sc[2 * jp + 1]);
+                }
+            }
+            // ---- mask, scale to log2 units, softmax within the sub-tile ----
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = e >> 1;
+                    const int key = key0 + 8 * jj + 2 * t + (e & 1);
+                    const bool vis = valid[h] && key <= pos[h];
+                    const float v = vis ? sc[jj][e] * scale_log2 : -INFINITY;
+                    sc[jj][e] = v;
+                    mx[h] = fmaxf(mx[h], v);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+            }
+            float rs[2] = {0.f, 0.f};
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = e >> 1;
+                    const float p = (mx[h] == -INFINITY) ? 0.f : exp2f(sc[jj][e] - mx[h]);
+                    sc[jj][e] = p;
+                    rs[h] += p;
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 1);
+                rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 2);
+            }
+            // ---- O = P V with P = hi + lo ----
+            float o[D / 8][4];
+#pragma unroll
+            for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < SUB / 16; ++kk) {
+                uint32_t ph[4], pl[4];
+                float r00, r01, r10, r11, r20, r21, r30, r31;
+                ph[0] = pack_hi<BF16>(sc[2 * kk][0], sc[2 * kk][1], r00, r01);
+                ph[1] = pack_hi<BF16>(sc[2 * kk][2], sc[2 * kk][3], r10, r11);
+                ph[2] = pack_hi<BF16>(sc[2 * kk + 1][0], sc[2 * kk + 1][1], r20, r21);
+                ph[3] = pack_hi<BF16>(sc[2 * kk + 1][2], sc[2 * kk + 1][3], r30, r31);
+                pl[0] = pack2<BF16>(r00, r01);
+                pl[1] = pack2<BF16>(r10, r11);
+                pl[2] = pack2<BF16>(r20, r21);
+                pl[3] = pack2<BF16>(r30, r31);
+#pragma unroll
+                for (int ndp = 0; ndp < D / 16; ++ndp) {
+                    const int mi = lane >> 3;
+                    const int key = 16 * kk + 8 * (mi & 1) + (lane & 7);
+                    const int dch = 2 * ndp + (mi >> 1);     // 8-wide d chunk
+                    const int hh = dch / 8, ch = dch % 8;
+                    uint32_t b0, b1, b2, b3;
+                    dev::ldmatrix_x4_trans(b0, b1, b2, b3, vb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
+                    mma16<BF16>(o[2 * ndp], ph[0], ph[1], ph[2], ph[3], b0, b1, o[2 * ndp]);
+                    mma16<BF16>(o[2 * ndp], pl[0], pl[1], pl[2], pl[3], b0, b1, o[2 * ndp]);
+                    mma16<BF16>(o[2 * ndp + 1], ph[0], ph[1], ph[2], ph[3], b2, b3, o[2 * ndp + 1]);
+                    mma16<BF16>(o[2 * ndp + 1], pl[0], pl[1], pl[2], pl[3], b2, b3, o[2 * ndp + 1]);
+                }
+            }
+            // ---- leave (m_w, l_w, o_w) of rows g, g + 8 in shared memory ----
+            uint8_t *pb = smem + C::PART_OFF + (j * NCONS + w) * C::PART;
+            float *po_s = reinterpret_cast<float *>(pb);
+            float2 *pml = reinterpret_cast<float2 *>(pb + 16 * C::OSTR * 4);
+#pragma unroll
+            for (int nd = 0; nd < D / 8; ++nd) {
+                *reinterpret_cast<float2 *>(po_s + g * C::OSTR + 8 * nd + 2 * t) = make_float2(o[nd][0], o[nd][1]);
+                *reinterpret_cast<float2 *>(po_s + (g + 8) * C::OSTR + 8 * nd + 2 * t) = make_float2(o[nd][2], o[nd][3]);
+            }
+            if (t == 0) {
+                pml[g] = make_float2(mx[0], rs[0]);
+                pml[g + 8] = make_float2(mx[1], rs[1]);
             }
         }
+        asm volatile("bar.sync 1, %0;" ::"n"(NCONS * 32) : "memory");
+        // ---- merge the sub-tiles of each row in ascending order, write the chunk partial ----
+        if (ok) {
+            constexpr int D4 = D / 4;
+            for (int e = threadIdx.x; e < C::MR * 16 * D4; e += NCONS * 32) {
+                const int j = e / (16 * D4), row = (e / D4) % 16, d4 = e % D4;
+                const int mt = mt0 + j;
+                const int m = mt * 16 + row;
+                if (mt >= mtiles || m >= mrows) continue;
+                const int i = i0 + m / G, gg = m % G;
+                const int p = ctx + i;
+                const int nw = min(nsub, (p - kbeg) / SUB + 1);   // sub-tiles whose first key is visible
+                const uint8_t *pb0 = smem + C::PART_OFF + (j * NCONS) * C::PART;
+                float mmax = -INFINITY;
+                for (int ww = 0; ww < nw; ++ww)
+                    mmax = fmaxf(mmax, reinterpret_cast<const float2 *>(pb0 + ww * C::PART + 16 * C::OSTR * 4)[row].x);
+                float l = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int ww = 0; ww < nw; ++ww) {
+                    const uint8_t *pb = pb0 + ww * C::PART;
+                    const float2 ml = reinterpret_cast<const float2 *>(pb + 16 * C::OSTR * 4)[row];
+                    const float sc = exp2f(ml.x - mmax);
+                    l = fmaf(ml.y, sc, l);
+                    const float4 ov = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(pb) +
+                                                                        row * C::OSTR + 4 * d4);
+                    acc.x = fmaf(ov.x, sc, acc.x);
+                    acc.y = fmaf(ov.y, sc, acc.y);
+                    acc.z = fmaf(ov.z, sc, acc.z);
+                    acc.w = fmaf(ov.w, sc, acc.w);
+                }
+                const size_t pidx = ((size_t)(r0 + i) * Hq + kvh * G + gg) * nc_max + c;
+                *reinterpret_cast<float4 *>(part_o + pidx * D + 4 * d4) = acc;
+                if (d4 == 0) part_ml[pidx] = make_float2(mmax, l);
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(NCONS * 32) : "memory");
     }
 }
 
@@ -366,6 +392,7 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
     }
     const int p = ctx_start[lo] + (r - cu_rows[lo]);
     constexpr int PER = D / 32;
+    static_assert(PER == 2 || PER == 4, "head dimension 64 or 128");
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
@@ -374,15 +401,49 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
     } else {
         const int nc = p / CHUNK + 1;
         const float2 *ml = part_ml + ((size_t)r * Hq + h) * nc_max;
+        const float *ob = part_o + ((size_t)r * Hq + h) * nc_max * D + lane * PER;
+        // m: max over the chunks (exact, any order); lane j holds chunks j, j + 32, ...
         float m = -INFINITY;
-        for (int c = 0; c < nc; ++c) m = fmaxf(m, ml[c].x);
-        float l = 0.f;
-        for (int c = 0; c < nc; ++c) {
-            const float w = exp2f(ml[c].x - m);
-            l += ml[c].y * w;
-            const float *op = part_o + (((size_t)r * Hq + h) * nc_max + c) * D + lane * PER;
+        for (int c = lane; c < nc; c += 32) m = fmaxf(m, ml[c].x);
 #pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] += op[e] * w;
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        // l and the weighted values in ascending chunk order; the partials of
+        // eight chunks are loaded together
+        float l = 0.f;
+        for (int c0 = 0; c0 < nc; c0 += 32) {
+            const int cl = c0 + lane;
+            const float2 mlv = cl < nc ? ml[cl] : make_float2(-INFINITY, 0.f);
+            const float wl = cl < nc ? exp2f(mlv.x - m) : 0.f;
+            const int cn = min(32, nc - c0);
+            for (int j0 = 0; j0 < cn; j0 += 8) {
+                float ov[8][PER];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    if (j0 + jj < cn) {
+                        const float *src = ob + (size_t)(c0 + j0 + jj) * D;
+                        if constexpr (PER == 4) {
+                            const float4 v = *reinterpret_cast<const float4 *>(src);
+                            ov[jj][0] = v.x, ov[jj][1] = v.y, ov[jj][2] = v.z, ov[jj][3] = v.w;
+                        } else {
+                            const float2 v = *reinterpret_cast<const float2 *>(src);
+                            ov[jj][0] = v.x, ov[jj][1] = v.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < PER; ++e) ov[jj][e] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const float w = __shfl_sync(0xffffffffu, wl, j0 + jj);
+                    const float lc = __shfl_sync(0xffffffffu, mlv.y, j0 + jj);
+                    if (j0 + jj < cn) {
+                        l = fmaf(lc, w, l);
+#pragma unroll
+                        for (int e = 0; e < PER; ++e) acc[e] = fmaf(ov[jj][e], w, acc[e]);
+                    }
+                }
+            }
         }
         const float inv = 1.0f / l;
 #pragma unroll

@@ -45,8 +45,7 @@ argmax_partial_kernel(const void *__restrict__ logits, int V, int split, int R, 
                                                       (size_t)r * V * (BF16 ? 2 : 4));
     Best b{-INFINITY, INT_MAX};
     bool nan = false;
-    for (int v = v0 + threadIdx.x; v < v1; v += VT) {
-        const uint4 w = __ldg(row + v);
+    auto scan = [&](const uint4 &w, int v) {
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
@@ -62,7 +61,19 @@ argmax_partial_kernel(const void *__restrict__ logits, int V, int split, int R, 
                 b.i = idx;
             }
         }
+    };
+    // four 16-byte loads in flight per thread; every comparison is exact, so the
+    // order in which a thread visits its elements does not change the result
+    constexpr int U = 4;
+    int v = v0 + threadIdx.x;
+    for (; v + (U - 1) * VT < v1; v += U * VT) {
+        uint4 w[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) w[j] = __ldcs(row + v + j * VT);
+#pragma unroll
+        for (int j = 0; j < U; ++j) scan(w[j], v + j * VT);
     }
+    for (; v < v1; v += VT) scan(__ldcs(row + v), v);
     if (nan) dev::report(dev_err, SPEC_DEVERR_NAN);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -133,7 +144,7 @@ verify_finalize_kernel(const Best *__restrict__ part, int split, const int32_t *
 
 int argmax_split(int R, int V) {
     const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
-    int sp = (4 * sms + R - 1) / R;          // about four CTAs per SM
+    int sp = (8 * sms + R - 1) / R;          // about eight CTAs per SM
     const int max_sp = V / 4096 > 0 ? V / 4096 : 1;  // at least 4096 logits per CTA
     if (sp > max_sp) sp = max_sp;
     if (sp < 1) sp = 1;
