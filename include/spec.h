@@ -163,9 +163,11 @@ spec_status spec_qmatmul_static_scratch(const uint8_t *wq, const uint16_t *ws, i
  * the tile geometry chosen by query width changed the KV traversal and the
  * combine order.  Here the KV sequence is cut into chunks of a constant 256
  * keys; row r (position p) gets one partial (max, sum, weighted values) per
- * chunk c <= p / 256 computed over keys [256c, min(256c + 255, p)] in
- * ascending order, and the partials are combined in ascending c.  Nothing
- * depends on the other rows of the call.
+ * chunk c <= p / 256 over keys [256c, min(256c + 255, p)]: each 64-key
+ * sub-tile of the chunk whose first key is <= p yields its own (max, sum,
+ * values) and the sub-tiles are merged in ascending order; the chunk
+ * partials are then combined in ascending c.  Nothing depends on the other
+ * rows of the call.
  *
  *   q        [R][Hq][D] of qkv_dt (SPEC_F16 or SPEC_BF16), 16-byte aligned
  *   k_cache, v_cache  [num_pages][Hkv][16][D] of qkv_dt, 16-byte aligned
