@@ -133,10 +133,10 @@ def count_launches(fn):
         orig[name] = f
 
         def wrap(*a, _n=name, _f=f, **k):
-            if _n == "spec_qmatmul":   # one launch per pass of 8, 16 or 80 columns
+            if _n == "spec_qmatmul":   # one launch per pass of 8 or 16 columns, two (pack + matmul) per 80
                 nc = int(a[5])
                 per = 8 if nc <= 8 else (16 if nc <= 16 else 80)
-                counts[_n] = counts.get(_n, 0) + (nc + per - 1) // per
+                counts[_n] = counts.get(_n, 0) + (nc + per - 1) // per * (2 if nc > 16 else 1)
             else:
                 counts[_n] = counts.get(_n, 0) + 1
             return _f(*a, **k)

@@ -158,15 +158,29 @@ __global__ void rope_append_kernel(const float *__restrict__ qkv, int Hq, int Hk
     }
 }
 
-__global__ void swiglu_kernel(const float *__restrict__ gu, int F, uint16_t *__restrict__ out) {
+__device__ __forceinline__ uint16_t swiglu1(float x, float u) {
+    const float silu = x / (1.0f + expf(-x));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(silu * u));
+}
+
+// grid (ceil(F / 1024), R): each thread one group of four consecutive features
+// (16-byte loads when F % 4 == 0 and the buffers are aligned, one element at a time otherwise)
+__global__ void swiglu_kernel(const float *__restrict__ gu, int F, uint16_t *__restrict__ out, int vec) {
     dev::pdl_wait();
     dev::pdl_launch_dependents();
-    const int r = blockIdx.x;
+    const int r = blockIdx.y;
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= F) return;
     const float *g = gu + (size_t)r * 2 * F;
-    for (int i = threadIdx.x; i < F; i += blockDim.x) {
-        const float x = g[i];
-        const float silu = x / (1.0f + expf(-x));
-        out[(size_t)r * F + i] = __bfloat16_as_ushort(__float2bfloat16_rn(silu * g[F + i]));
+    uint16_t *o = out + (size_t)r * F;
+    if (vec) {
+        const float4 x = *reinterpret_cast<const float4 *>(g + i);
+        const float4 u = *reinterpret_cast<const float4 *>(g + F + i);
+        const uint2 v = make_uint2((uint32_t)swiglu1(x.x, u.x) | ((uint32_t)swiglu1(x.y, u.y) << 16),
+                                   (uint32_t)swiglu1(x.z, u.z) | ((uint32_t)swiglu1(x.w, u.w) << 16));
+        *reinterpret_cast<uint2 *>(o + i) = v;
+    } else {
+        for (int e = i; e < i + 4 && e < F; ++e) o[e] = swiglu1(g[e], g[F + e]);
     }
 }
 
@@ -297,7 +311,10 @@ extern "C" spec_status spec_swiglu(const float *gu, int R, int F, uint16_t *out,
     SPEC_CHECK_ARG(R >= 0 && F >= 1, "swiglu: bad sizes");
     SPEC_CHECK_ARG((gu && out) || R == 0, "swiglu: NULL pointer");
     if (R == 0) return SPEC_OK;
-    cudaError_t le = spec::launch_pdl(swiglu_kernel, dim3(R), dim3(256), 0, (cudaStream_t)stream, gu, F, out);
+    SPEC_CHECK_ARG(R <= 65535, "swiglu: at most 65535 rows per call");
+    const int vec = (F % 4 == 0) && spec::aligned16(gu) && (reinterpret_cast<uintptr_t>(out) % 8 == 0);
+    cudaError_t le = spec::launch_pdl(swiglu_kernel, dim3((F + 1023) / 1024, R), dim3(256), 0, (cudaStream_t)stream,
+                                      gu, F, out, vec);
     if (le != cudaSuccess) return spec::cuda_status(le, "swiglu launch");
     return spec::cuda_status(cudaGetLastError(), "swiglu launch");
 }

@@ -83,6 +83,20 @@ def test_swiglu_embed_and_cast():
     got = synth.bf16_bits_to_f32(host(out, np.uint16))
     ref = np.array([[oracle.silu_mul(gu[r, i], gu[r, F + i]) for i in range(F)] for r in range(R)])
     assert rel_err_rows(got, ref) <= 2 ** -7
+    # the 16-byte path (aligned, F % 4 == 0) and the element path give the same bits
+    buf = torch.zeros(R * 2 * F + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = dev(gu).reshape(-1)
+    out2 = torch.zeros((R, F), dtype=torch.int16, device="cuda")
+    L.spec_swiglu(buf[1:], R, F, out2)   # misaligned by 4 bytes: element path
+    torch.cuda.synchronize()
+    assert torch.equal(out2, out)
+    F3 = 643
+    gu3 = g.normal(0, 2, (3, 2 * F3)).astype(np.float32)
+    out3 = torch.zeros((3, F3), dtype=torch.int16, device="cuda")
+    L.spec_swiglu(dev(gu3), 3, F3, out3)
+    torch.cuda.synchronize()
+    ref3 = np.array([[oracle.silu_mul(gu3[r, i], gu3[r, F3 + i]) for i in range(F3)] for r in range(3)])
+    assert rel_err_rows(synth.bf16_bits_to_f32(host(out3, np.uint16)), ref3) <= 2 ** -7
     x = g.normal(0, 3, 1000).astype(np.float32)
     o = torch.zeros(1000, dtype=torch.int16, device="cuda")
     L.spec_cast_bf16(dev(x), 1000, o)
