@@ -623,7 +623,8 @@ def qmatmul_step_roofline(torch, L, w, hbm_peak, peak_kind):
     return {"kernel": "qmm_kernel (spec_qmatmul), the 33 int4 matmuls of one 80-row verify step",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 3), "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-            "traffic": traffic, "algorithmic_bytes_per_step": int(algo), "launches": len(mats),
+            "traffic": traffic, "algorithmic_bytes_per_launch": int(algo / len(mats)),
+            "algorithmic_bytes_per_step": int(algo), "launches": len(mats),
             "avg_launch_us": round(per_launch * 1e6, 2)}
 
 
@@ -637,7 +638,7 @@ def recorded_traffic(kernel: str):
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     txt = open(p).read()
     m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
-    m_b = re.search(r"traffic_bytes_per_step:\s*([0-9.e+]+)", txt)
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)", txt)
     if not m_sha or not m_b or m_sha.group(1) != sha:
         return None
     return float(m_b.group(1))
