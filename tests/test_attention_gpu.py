@@ -172,3 +172,30 @@ def test_bad_block_table_is_reported_not_faulted():
     with pytest.raises(L.SpecError):
         L.spec_flash_decode(d.q, case.dt, 4, 2, 64, case.scale, d.k, d.v, d.pages, d.bt, bt.shape[1],
                             dev(case.ctx_start), dev(case.cu_rows), 1, 2, 42, out, 0, ws, 16, err)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_rows_across_subtile_and_chunk_edges(D):
+    """Verify blocks whose rows cross the 64-key sub-tile and 256-key chunk edges:
+    every row equals its width-1 evaluation and the oracle."""
+    for ctx, n in ((60, 8), (125, 6), (190, 5), (250, 8), (511, 3), (0, 1), (63, 1), (64, 1)):
+        case = synth.attention_case(5100 + ctx + D, rows=[n], ctx=[ctx], Hq=8, Hkv=2, D=D, dt=DT_BF16,
+                                    scale=1 / math.sqrt(D))
+        d = Dev(case)
+        out = d.call()
+        assert rel_err_rows(host(out), oracle.attention(case)) <= TOL, (ctx, n)
+        for i in range(n):
+            assert bits_equal(d.single_row(0, i), out[i]), (ctx, n, i)
+
+
+def test_empty_sequences_in_a_batch():
+    """Sequences with no rows contribute nothing and change no other row."""
+    rows = [3, 0, 2, 0]
+    ctx = [100, 40, 300, 7]
+    case = synth.attention_case(6100, rows=rows, ctx=ctx, Hq=8, Hkv=2, D=128, dt=DT_BF16, scale=1 / math.sqrt(128))
+    d = Dev(case)
+    out = d.call()
+    assert rel_err_rows(host(out), oracle.attention(case)) <= TOL
+    for s, n in enumerate(rows):
+        for i in range(n):
+            assert bits_equal(d.single_row(s, i), out[int(case.cu_rows[s]) + i]), (s, i)

@@ -186,3 +186,15 @@ def test_workspace_is_left_zeroed_and_calls_repeat_bitwise():
     with pytest.raises(L.SpecError) as e:
         L.spec_qmatmul(w[0], w[1], 1000, 2048, x, 80, 2048, outs[0], 0, 1000, 0, wsp, 64)
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("N,K,n", [(1, 256, 3), (129, 256, 17), (300, 1280, 81), (140, 512, 161)])
+def test_edge_shapes_and_pass_boundaries(N, K, n):
+    """One output row, a single 256-k segment, 17 columns (first wide pass), and
+    81 / 161 columns (two and three 80-column passes): parity and width-1 bits."""
+    case = synth.qmatmul_case(8800 + N + n, N, K, n)
+    w, x = (dev(case.wq), dev(case.ws)), dev(case.x)
+    y = run(w, x, n, N, K)
+    assert rel_err_rows(host(y), oracle.qmatmul(case.wq, case.ws, case.x, N, K)) <= TOL
+    for j in sorted({0, n // 2, n - 1}):
+        assert bits_equal(run(w, x[j:j + 1], 1, N, K)[0], y[j]), j
