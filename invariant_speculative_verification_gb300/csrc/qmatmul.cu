@@ -20,23 +20,25 @@
 // scheduling that may depend on the call; the arithmetic above never does.
 //
 // Execution: a persistent grid of one CTA per SM, each with eight consumer
-// warps (16 weight rows each, 128 rows per tile), one TMA warp and two or three
-// activation warps.  The (128-row tile x K-segment) units are dealt out in
-// equal contiguous ranges (stream-K), so every SM streams the same number of
-// bytes.  The TMA warp's lane 0 issues cp.async.bulk.tensor copies of each
-// stage -- the int4 codes (128-row x 128-byte boxes, 128B swizzle) and the
-// fp16 scales -- into a ring of mbarrier-guarded stages.  A stage is 512 k
-// for passes of up to 16 columns and 256 k for the 80-column pass (a segment
-// is then two stages; only the delivery changes, not the arithmetic).  The
-// activation warps read the stage's activation columns from L2 with vector
-// loads, write them in the MMA B-fragment order together with the block sums
-// and hand the stage on, so consumers issue only ldmatrix, 4 LOP3 per 8
-// weights, lds and mma.sync.  A tile covered by one CTA is folded in
-// registers and written directly.  A tile shared by several CTAs is finished
-// through the workspace: the CTA holding its first segment stores its fold so
-// far, the others store their segment sums, and the last CTA to finish
-// (atomic counter) folds the rest in segment order, writes y and resets the
-// counter.
+// warps (16 weight rows each, 128 rows per tile) and one TMA warp.  The
+// (128-row tile x K-segment) units are dealt out in equal contiguous ranges
+// (stream-K), so every SM streams the same number of bytes.  The TMA warp's
+// lane 0 issues cp.async.bulk.tensor copies of each stage -- the int4 codes
+// (128-row x 128-byte boxes, 128B swizzle) and the fp16 scales -- into a ring
+// of mbarrier-guarded stages.  Passes of up to 16 columns use 512-k stages and
+// two activation warps, which read the stage's activation columns from L2,
+// write them in MMA B-fragment order together with the block sums and hand the
+// stage on.  The 80-column pass uses 256-k stages (a segment is two stages;
+// only the delivery changes, not the arithmetic); its activations are packed
+// into that same layout once per call by xpack_kernel and copied in with the
+// stage by one cp.async.bulk.  Consumers issue only ldmatrix, 4 LOP3 + 3
+// shifts per 8 weights, lds and mma.sync.  A tile covered by one CTA is folded
+// in registers and written directly.  A tile shared by several CTAs: the CTAs
+// holding its later segments store their segment sums and count themselves
+// in, without waiting; the CTA holding the leading segments folds them in
+// segment order once all have arrived (the usual case when it gets there),
+// else leaves its prefix for whichever CTA arrives last.  No CTA waits for
+// another; the counters end at zero.
 //
 // The weight format (int4 block 32, fp16 scale, even k in the low nibble) is
 // the stand-in for the block-quantised formats named in ramgpt.org, "When
