@@ -54,6 +54,10 @@ def lib():
             c.oracle_attention.argtypes = [vp, i32, i32, i32, i32, dbl, vp, vp, vp, i32, vp, vp, i32, vp, vp]
             c.oracle_verify_greedy.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp]
             c.oracle_verify_greedy.restype = i32
+            u32, f32 = ctypes.c_uint32, ctypes.c_float
+            c.oracle_philox4x32_10.argtypes = [vp, vp, vp]
+            c.oracle_verify_sample.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, f32, u32, u32, vp, vp, vp, vp, vp]
+            c.oracle_verify_sample.restype = i32
             c.oracle_kv_compact.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, vp, vp, vp, i32, vp, vp, vp]
             c.oracle_rmsnorm.argtypes = [vp, i32, vp, dbl, vp]
             c.oracle_rope.argtypes = [vp, i32, i32, dbl]
@@ -151,6 +155,39 @@ def verify_greedy(logits, dt: int, V: int, cu_rows, drafts, ctx_start):
         dr = np.zeros(1, np.int32)
     nans = lib().oracle_verify_greedy(_p(lg), dt, V, _p(cu), S, _p(dr), _p(ctx), _p(am), _p(acc), _p(cor), _p(cn))
     return dict(argmax=am, accepted=acc, correction=cor, ctx_new=cn, nans=int(nans))
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 of four 32-bit counter words and two key words -> four words."""
+    ctr = np.asarray(counter, np.uint32).copy()
+    k = np.asarray(key, np.uint32).copy()
+    out = np.zeros(4, np.uint32)
+    lib().oracle_philox4x32_10(_p(ctr), _p(k), _p(out))
+    return out
+
+
+def verify_sample(logits, dt: int, V: int, cu_rows, drafts, ctx_start, inv_temp: float, seed: int, seq_id=None):
+    """Temperature-sampling verification (Gumbel-max with Philox draws keyed by
+    sequence and position).  Returns dict(token, accepted, correction, ctx_new,
+    top2_gap, nans); top2_gap is each row's winning margin in fp32 scores."""
+    lg = _c(logits, np.float32 if dt == DT_F32 else np.uint16)
+    cu = _c(cu_rows, np.int32)
+    dr = _c(drafts, np.int32)
+    ctx = _c(ctx_start, np.int32)
+    S = len(ctx)
+    R = int(cu[-1])
+    tok = np.zeros(R, np.int32)
+    acc = np.zeros(S, np.int32)
+    cor = np.zeros(S, np.int32)
+    cn = np.zeros(S, np.int32)
+    gap = np.zeros(R, np.float32)
+    if dr.size == 0:
+        dr = np.zeros(1, np.int32)
+    sid = None if seq_id is None else _c(seq_id, np.int32)
+    nans = lib().oracle_verify_sample(_p(lg), dt, V, _p(cu), S, _p(dr), _p(ctx), _p(sid), float(inv_temp),
+                                      seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF,
+                                      _p(tok), _p(acc), _p(cor), _p(cn), _p(gap))
+    return dict(token=tok, accepted=acc, correction=cor, ctx_new=cn, top2_gap=gap, nans=int(nans))
 
 
 def kv_compact(k_stage, v_stage, k_cache, v_cache, Hkv, D, block_table, ctx_start, accepted, cu_rows):
@@ -259,8 +296,9 @@ class Decoder:
         return self.lm_head(h)
 
 
-def generate(weights, prompts_arr, n_new: int, draft_width: int, pads):
-    """Greedy generation with the oracle decoder.
+def generate(weights, prompts_arr, n_new: int, draft_width: int, pads, inv_temp: float = 0.0, seed: int = 0):
+    """Greedy generation with the oracle decoder (inv_temp > 0: temperature
+    sampling through verify_sample, draws keyed by sequence and position).
 
     draft_width == 0: ordinary decoding, one row per sequence per step.
     draft_width  > 0: speculative decoding; each step verifies the last token
@@ -293,7 +331,11 @@ def generate(weights, prompts_arr, n_new: int, draft_width: int, pads):
         cu = np.zeros(len(live) + 1, np.int32)
         cu[1:] = np.cumsum(rows)
         lg = dec.forward(np.array(toks, np.int32), ctx[live], cu, seqs=live)
-        res = verify_greedy(lg, DT_F32, V, cu, np.array(drafts, np.int32), ctx[live])
+        if inv_temp > 0:
+            res = verify_sample(lg, DT_F32, V, cu, np.array(drafts, np.int32), ctx[live], inv_temp, seed,
+                                seq_id=np.array(live, np.int32))
+        else:
+            res = verify_greedy(lg, DT_F32, V, cu, np.array(drafts, np.int32), ctx[live])
         for k, s in enumerate(live):
             a = int(res["accepted"][k])
             acc_total += a

@@ -246,6 +246,106 @@ int oracle_verify_greedy(const void *logits, int dt, int V, const int32_t *cu_ro
 }
 
 /* ---------------------------------------------------------------------------
+ * 3b. Speculative verification with temperature sampling
+ *
+ * ramgpt.org, "When Lossless Speculation Stops Being Lossless on Blackwell",
+ * section "A Better Backend Test Matrix": the byte-identity requirement is
+ * stated for greedy decoding; the method's extension to sampling (keep the
+ * random draws tied to the sequence and the position, not to the batch) is
+ * our reading.  Each verify row r of sequence s at absolute position p draws
+ * its token as
+ *     t_r = argmax_v  fma(logit[r][v], inv_temp, g(id_s, p, v))    (ties: lower v)
+ * where id_s is the sequence's identity (seq_id[s], or s when seq_id is NULL)
+ * with a Gumbel variate g = -log(-log(u)), u = (b >> 9) * 2^-23 + 2^-24 and
+ * b = word (v mod 4) of Philox4x32-10(counter = (v / 4, p, s, 0x53504543),
+ * key = (seed_lo, seed_hi)).  Gumbel-max makes t_r an exact sample of
+ * softmax(logit / T).  Drafts are accepted while draft_i == t_{r0+i}; the
+ * correction is t at the first mismatch (or of the last row).  A width-1
+ * decode with the same seed draws the same tokens at the same positions, so
+ * speculative sampling reproduces it byte for byte.  Scores are computed in
+ * fp32 with a fused multiply-add, as a kernel computes them.
+ *
+ * Philox4x32-10 is the counter-based generator of Salmon, Moraes, Dror and
+ * Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11): ten rounds of
+ * two 32x32->64-bit products with multipliers 0xD2511F53 and 0xCD9E8D57 and
+ * a key advanced by the Weyl constants 0x9E3779B9 and 0xBB67AE85 between
+ * rounds.
+ * ------------------------------------------------------------------------- */
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+        c0 = n0, c1 = n1, c2 = n2, c3 = n3;
+    }
+    out[0] = c0, out[1] = c1, out[2] = c2, out[3] = c3;
+}
+
+static float or_sample_score(float x, float inv_temp, uint32_t seed_lo, uint32_t seed_hi, int s, int p, int v)
+{
+    const uint32_t ctr[4] = {(uint32_t)v / 4u, (uint32_t)p, (uint32_t)s, 0x53504543u};
+    const uint32_t key[2] = {seed_lo, seed_hi};
+    uint32_t w[4];
+    oracle_philox4x32_10(ctr, key, w);
+    const float u = (float)(w[v % 4] >> 9) * (1.0f / 8388608.0f) + (1.0f / 16777216.0f);
+    const float g = -logf(-logf(u));
+    return fmaf(x, inv_temp, g);
+}
+
+int oracle_verify_sample(const void *logits, int dt, int V, const int32_t *cu_rows, int S,
+                         const int32_t *drafts, const int32_t *ctx_start, const int32_t *seq_id, float inv_temp,
+                         uint32_t seed_lo, uint32_t seed_hi,
+                         int32_t *token, int32_t *accepted, int32_t *correction, int32_t *ctx_new,
+                         float *top2_gap)
+{
+    int nans = 0;
+    for (int s = 0; s < S; ++s) {
+        for (int r = cu_rows[s]; r < cu_rows[s + 1]; ++r) {
+            const int p = ctx_start[s] + (r - cu_rows[s]);
+            int best = -1;
+            float bv = 0.f, second = -INFINITY;
+            for (int v = 0; v < V; ++v) {
+                const float x = (float)or_elem(logits, dt, (size_t)r * V + v);
+                if (isnan(x)) {
+                    ++nans;
+                    continue;
+                }
+                const float sc = or_sample_score(x, inv_temp, seed_lo, seed_hi, seq_id ? seq_id[s] : s, p, v);
+                if (best < 0 || sc > bv) {
+                    if (best >= 0) second = bv;
+                    bv = sc;
+                    best = v;
+                } else if (sc > second) {
+                    second = sc;
+                }
+            }
+            token[r] = best < 0 ? 0 : best;
+            if (top2_gap) top2_gap[r] = bv - second;
+        }
+    }
+    for (int s = 0; s < S; ++s) {
+        int r0 = cu_rows[s];
+        int L = cu_rows[s + 1] - r0 - 1;
+        int a = 0;
+        while (a < L && drafts[r0 - s + a] == token[r0 + a])
+            ++a;
+        accepted[s] = a;
+        correction[s] = token[r0 + a];
+        ctx_new[s] = ctx_start[s] + a + 1;
+    }
+    return nans;
+}
+
+/* ---------------------------------------------------------------------------
  * 4. KV-cache realignment after ragged acceptance
  *
  * [P] "Batching breaks the implementation": sequences in a batch accept
