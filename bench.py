@@ -359,6 +359,17 @@ def kernel_rooflines(torch, L, hbm_peak):
     out["verify"] = {"workload": f"64 seqs, R={vc.R} rows x V=152064 bf16", "us": round(t * 1e6, 2),
                      "GBps": round(lbytes / t / 1e9, 1), "frac": round(lbytes / t / 1e9 / hbm_peak, 3),
                      "algorithmic_bytes": "R*V*2"}
+
+    # the same verification with temperature sampling (a Philox draw and a Gumbel variate per logit)
+    def sbody():
+        for i in range(copies):
+            L.spec_verify_sample(lgs[i], L.SPEC_BF16, vc.V, cu, vc.S, vc.R, dr, cs, None, 1.25, 1234, am, acc, cor,
+                                 cn, vws, vwb, None)
+
+    t = graph_time(torch, sbody, copies)
+    out["verify_sample"] = {"workload": f"64 seqs, R={vc.R} rows x V=152064 bf16, T = 0.8", "us": round(t * 1e6, 2),
+                            "GBps": round(lbytes / t / 1e9, 1), "frac": round(lbytes / t / 1e9 / hbm_peak, 3),
+                            "algorithmic_bytes": "R*V*2"}
     torch.cuda.synchronize()
     accepted = acc.clone()
     del lgs, lg0

@@ -216,6 +216,31 @@ spec_status spec_verify_greedy(const void *logits, spec_dtype dt, int V,
                                int32_t *ctx_new, void *workspace, size_t ws_bytes,
                                int32_t *dev_err, spec_stream_t stream);
 
+/* K4 with temperature sampling.  The pages state the byte-identity contract
+ * for greedy decoding; extending it to sampling by tying every random draw to
+ * the sequence and the position (never to the batch) is this library's
+ * reading of ramgpt.org, section "A Better Backend Test Matrix".
+ * Row r of sequence s at position p = ctx_start[s] + (r - cu_rows[s]) draws
+ *     token[r] = argmax_v fma(logit[r][v], inv_temperature, -log(-log(u)))
+ * (ties: lowest v; a Gumbel-max draw, i.e. an exact sample of
+ * softmax(logit / T)), where u = (w >> 9) * 2^-23 + 2^-24 and w is word v % 4 of
+ * Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3")
+ * with counter (v / 4, p, id_s, 0x53504543) and key (seed low, seed high 32
+ * bits); id_s = seq_id[s], or s when seq_id is NULL.  Acceptance, correction
+ * and ctx_new are then those of spec_verify_greedy with token[] in place of
+ * argmax[]: a width-1 decode that samples with the same seed and sequence ids
+ * produces the same tokens, so speculative sampling reproduces it byte for
+ * byte.  inv_temperature = 1 / T > 0 and finite.  Other arguments, the
+ * workspace (spec_verify_greedy_workspace) and errors as in
+ * spec_verify_greedy. */
+spec_status spec_verify_sample(const void *logits, spec_dtype dt, int V,
+                               const int32_t *cu_rows, int S, int R,
+                               const int32_t *drafts, const int32_t *ctx_start,
+                               const int32_t *seq_id, float inv_temperature, uint64_t seed,
+                               int32_t *token_out, int32_t *accepted, int32_t *correction,
+                               int32_t *ctx_new, void *workspace, size_t ws_bytes,
+                               int32_t *dev_err, spec_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * K5  KV-cache realignment after ragged acceptance
  *

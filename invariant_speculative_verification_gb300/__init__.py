@@ -10,6 +10,6 @@ from ._lib import (DEVERR, SPEC_BF16, SPEC_F16, SPEC_F32, SpecError, library_pat
                    spec_flash_decode_workspace, spec_kv_compact, spec_ngram_draft, spec_qmatmul,
                    spec_qmatmul_debug_nt, spec_qmatmul_noninvariant, spec_qmatmul_static_scratch, spec_qmatmul_workspace,
                    spec_rope_append, spec_rope_table,
-                   spec_swiglu, spec_verify_greedy, spec_verify_greedy_workspace)
+                   spec_swiglu, spec_verify_greedy, spec_verify_greedy_workspace, spec_verify_sample)
 
 load()

@@ -41,6 +41,8 @@ _SIGS = {
                                  _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
     "spec_verify_greedy_workspace": (_sz, [_i32, _i32]),
     "spec_verify_greedy": (_i32, [_vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "spec_verify_sample": (_i32, [_vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _f32, ctypes.c_uint64, _vp, _vp,
+                                  _vp, _vp, _vp, _sz, _vp, _vp]),
     "spec_kv_compact": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp,
                                _vp, _vp, _vp]),
     "spec_embed": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp]),
@@ -166,6 +168,14 @@ def spec_verify_greedy(logits, dt, V, cu_rows, S, R, drafts, ctx_start, argmax_o
     _check("spec_verify_greedy", load().spec_verify_greedy(
         _ptr(logits), dt, V, _ptr(cu_rows), S, R, _ptr(drafts), _ptr(ctx_start), _ptr(argmax_out), _ptr(accepted),
         _ptr(correction), _ptr(ctx_new), _ptr(workspace), int(ws_bytes), _ptr(dev_err), _stream(stream)))
+
+
+def spec_verify_sample(logits, dt, V, cu_rows, S, R, drafts, ctx_start, seq_id, inv_temperature, seed, token_out,
+                       accepted, correction, ctx_new, workspace, ws_bytes, dev_err=None, stream=None):
+    _check("spec_verify_sample", load().spec_verify_sample(
+        _ptr(logits), dt, V, _ptr(cu_rows), S, R, _ptr(drafts), _ptr(ctx_start), _ptr(seq_id), float(inv_temperature),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(token_out), _ptr(accepted), _ptr(correction), _ptr(ctx_new),
+        _ptr(workspace), int(ws_bytes), _ptr(dev_err), _stream(stream)))
 
 
 def spec_kv_compact(k_stage, v_stage, k_cache, v_cache, Hkv, D, num_pages, block_table, max_blocks, ctx_start,

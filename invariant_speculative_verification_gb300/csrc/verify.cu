@@ -30,10 +30,43 @@ __device__ __forceinline__ Best better(Best a, Best b) {
     return a;
 }
 
-template <bool BF16>
+// Temperature sampling (spec_verify_sample): the row's token is the argmax of
+// fma(logit, inv_temp, g) with g = -log(-log(u)) a Gumbel variate; u comes from
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+// as 1, 2, 3", SC'11) with counter (v / 4, position, sequence id, 0x53504543)
+// and key (seed_lo, seed_hi), word v % 4: u = (w >> 9) 2^-23 + 2^-24.
+struct SampleArgs {
+    float inv_temp;
+    uint32_t seed_lo, seed_hi;
+    const int32_t *cu_rows, *ctx_start, *seq_id;
+    int S;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                               uint32_t k1) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0, c1 = lo1, c2 = n2, c3 = lo0;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
+__device__ __forceinline__ float gumbel(uint32_t w) {
+    const float u = __uint2float_rn(w >> 9) * (1.0f / 8388608.0f) + (1.0f / 16777216.0f);
+    return -logf(-logf(u));
+}
+
+template <bool BF16, bool SAMPLE>
 __global__ void __launch_bounds__(VT)
 argmax_partial_kernel(const void *__restrict__ logits, int V, int split, int R, Best *__restrict__ part,
-                      int32_t *dev_err) {
+                      int32_t *dev_err, SampleArgs sa) {
     dev::pdl_wait();
     dev::pdl_launch_dependents();
     const int r = blockIdx.y, sp = blockIdx.x;
@@ -45,8 +78,29 @@ argmax_partial_kernel(const void *__restrict__ logits, int V, int split, int R, 
                                                       (size_t)r * V * (BF16 ? 2 : 4));
     Best b{-INFINITY, INT_MAX};
     bool nan = false;
+    // sampling: this row's sequence (the last s with cu_rows[s] <= r), position and identity
+    uint32_t pos = 0, sid = 0;
+    if (SAMPLE) {
+        int lo = 0, hi = sa.S;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (sa.cu_rows[mid] <= r) lo = mid; else hi = mid;
+        }
+        pos = (uint32_t)(sa.ctx_start[lo] + (r - sa.cu_rows[lo]));
+        sid = (uint32_t)(sa.seq_id ? sa.seq_id[lo] : lo);
+    }
     auto scan = [&](const uint4 &w, int v) {
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        uint32_t rnd[8];
+        if (SAMPLE) {
+            // the 16-byte vector holds elements v*VEC .. v*VEC+VEC-1: counters (v*VEC)/4 ..
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q) {
+                const uint4 ph = philox4x32_10((uint32_t)((v * VEC) / 4 + q), pos, sid, 0x53504543u, sa.seed_lo,
+                                               sa.seed_hi);
+                rnd[4 * q] = ph.x, rnd[4 * q + 1] = ph.y, rnd[4 * q + 2] = ph.z, rnd[4 * q + 3] = ph.w;
+            }
+        }
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
             float x;
@@ -55,6 +109,7 @@ argmax_partial_kernel(const void *__restrict__ logits, int V, int split, int R, 
             else
                 x = __uint_as_float(u[e]);
             nan |= (x != x);
+            if (SAMPLE) x = fmaf(x, sa.inv_temp, gumbel(rnd[e]));
             const int idx = v * VEC + e;
             if (x > b.v || (x == b.v && idx < b.i)) {
                 b.v = x;
@@ -261,14 +316,50 @@ extern "C" spec_status spec_verify_greedy(const void *logits, spec_dtype dt, int
     cudaStream_t st = (cudaStream_t)stream;
     Best *part = reinterpret_cast<Best *>(workspace);
     dim3 grid(split, R);
+    const SampleArgs none{};
     cudaError_t le = (dt == SPEC_BF16)
-                         ? spec::launch_pdl(argmax_partial_kernel<true>, grid, dim3(VT), 0, st, logits, V, split, R, part,
-                                            dev_err)
-                         : spec::launch_pdl(argmax_partial_kernel<false>, grid, dim3(VT), 0, st, logits, V, split, R, part,
-                                            dev_err);
+                         ? spec::launch_pdl(argmax_partial_kernel<true, false>, grid, dim3(VT), 0, st, logits, V, split,
+                                            R, part, dev_err, none)
+                         : spec::launch_pdl(argmax_partial_kernel<false, false>, grid, dim3(VT), 0, st, logits, V,
+                                            split, R, part, dev_err, none);
     if (le != cudaSuccess) return spec::cuda_status(le, "argmax launch");
     le = spec::launch_pdl(verify_finalize_kernel, dim3((S + 3) / 4), dim3(128), 0, st, (const Best *)part, split, cu_rows,
                           S, R, V, drafts, ctx_start, argmax_out, accepted, correction, ctx_new, dev_err);
+    return spec::cuda_status(le, "verify finalize launch");
+}
+
+extern "C" spec_status spec_verify_sample(const void *logits, spec_dtype dt, int V, const int32_t *cu_rows, int S,
+                                          int R, const int32_t *drafts, const int32_t *ctx_start,
+                                          const int32_t *seq_id, float inv_temperature, uint64_t seed,
+                                          int32_t *token_out, int32_t *accepted, int32_t *correction,
+                                          int32_t *ctx_new, void *workspace, size_t ws_bytes, int32_t *dev_err,
+                                          spec_stream_t stream) {
+    SPEC_CHECK_ARG(dt == SPEC_F32 || dt == SPEC_BF16, "verify_sample: dt must be SPEC_F32 or SPEC_BF16");
+    SPEC_CHECK_ARG(V >= 8 && V % 8 == 0, "verify_sample: V must be a positive multiple of 8 (V=%d)", V);
+    SPEC_CHECK_ARG(S >= 0 && R >= S && R <= 65535, "verify_sample: need S <= R <= 65535 (S=%d R=%d)", S, R);
+    SPEC_CHECK_ARG(inv_temperature > 0.f && inv_temperature < INFINITY,
+                   "verify_sample: inv_temperature must be positive and finite");
+    SPEC_CHECK_ARG(cu_rows && ctx_start && token_out && accepted && correction && ctx_new &&
+                       (logits || R == 0) && (drafts || R == S),
+                   "verify_sample: NULL pointer");
+    SPEC_CHECK_ARG(spec::aligned16(logits), "verify_sample: logits must be 16-byte aligned");
+    if (S == 0) return SPEC_OK;
+    const int split = argmax_split(R, V);
+    const size_t need = (size_t)R * split * sizeof(Best);
+    if (!workspace || ws_bytes < need || !spec::aligned16(workspace))
+        return spec::fail(SPEC_ERR_WORKSPACE, "verify_sample: workspace needs %zu bytes, got %zu", need, ws_bytes);
+    cudaStream_t st = (cudaStream_t)stream;
+    Best *part = reinterpret_cast<Best *>(workspace);
+    const SampleArgs sa{inv_temperature, (uint32_t)seed, (uint32_t)(seed >> 32), cu_rows, ctx_start, seq_id, S};
+    dim3 grid(split, R);
+    cudaError_t le = (dt == SPEC_BF16)
+                         ? spec::launch_pdl(argmax_partial_kernel<true, true>, grid, dim3(VT), 0, st, logits, V, split,
+                                            R, part, dev_err, sa)
+                         : spec::launch_pdl(argmax_partial_kernel<false, true>, grid, dim3(VT), 0, st, logits, V,
+                                            split, R, part, dev_err, sa);
+    if (le != cudaSuccess) return spec::cuda_status(le, "sample launch");
+    le = spec::launch_pdl(verify_finalize_kernel, dim3((S + 3) / 4), dim3(128), 0, st, (const Best *)part, split, cu_rows,
+                          S, R, V, drafts, ctx_start, token_out, accepted, correction, ctx_new, dev_err);
     return spec::cuda_status(le, "verify finalize launch");
 }
 

@@ -125,10 +125,14 @@ def max_len_for(P: int, n_new: int, W: int) -> int:
 
 class Generator:
     """Greedy generation for S sequences, W drafts per step (W = 0: ordinary
-    width-1 decoding).  All per-step state lives on the device."""
+    width-1 decoding).  All per-step state lives on the device.  With
+    inv_temp > 0 tokens are sampled at temperature 1 / inv_temp instead
+    (spec_verify_sample; draws keyed by seed, sequence index and position)."""
 
-    def __init__(self, dec: Decoder, prompts: np.ndarray, W: int, pads: np.ndarray, n_new: int):
+    def __init__(self, dec: Decoder, prompts: np.ndarray, W: int, pads: np.ndarray, n_new: int,
+                 inv_temp: float = 0.0, seed: int = 0):
         self.dec, self.W = dec, W
+        self.inv_temp, self.seed = float(inv_temp), int(seed)
         S, P = prompts.shape
         assert S == dec.S
         d = dec.device
@@ -168,9 +172,14 @@ class Generator:
         dec, W, S, R = self.dec, self.W, self.S, self.R
         L.spec_ngram_draft(self.hist, self.cap, self.hist_len, S, W, self.pad_step, self.drafts, None, self.block)
         logits = dec.forward(self.block, self.cu, self.ctx, S, R)
-        L.spec_verify_greedy(logits, L.SPEC_F32, dec.V, self.cu, S, R, self.drafts if W else None, self.ctx,
-                             self.argmax, self.accepted, self.correction, self.ctx_new, self.vws, self.vws_bytes,
-                             dec.dev_err)
+        if self.inv_temp > 0:
+            L.spec_verify_sample(logits, L.SPEC_F32, dec.V, self.cu, S, R, self.drafts if W else None, self.ctx,
+                                 None, self.inv_temp, self.seed, self.argmax, self.accepted, self.correction,
+                                 self.ctx_new, self.vws, self.vws_bytes, dec.dev_err)
+        else:
+            L.spec_verify_greedy(logits, L.SPEC_F32, dec.V, self.cu, S, R, self.drafts if W else None, self.ctx,
+                                 self.argmax, self.accepted, self.correction, self.ctx_new, self.vws, self.vws_bytes,
+                                 dec.dev_err)
         # the block's K/V were written into the cache in place: realignment is index-only
         L.spec_kv_compact(None, None, None, None, dec.Hkv, dec.D, dec.pages, dec.block_table, dec.max_blocks,
                           self.ctx, self.accepted, self.cu, S, R, self.cu_kept, self.kept_src, self.dst_slot,
