@@ -68,7 +68,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        out_dir = os.environ.get("SPEC_BENCH_LOG_DIR") or os.path.join(ROOT, "gpurun_out")
+        self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:

@@ -55,7 +55,7 @@ typedef struct CUstream_st *spec_stream_t; /* a cudaStream_t */
 typedef enum {
     SPEC_OK = 0,
     SPEC_ERR_INVALID_ARG = 1, /* bad shape, NULL or misaligned pointer */
-    SPEC_ERR_UNSUPPORTED = 2, /* valid request this build does not support */
+    SPEC_ERR_UNSUPPORTED = 2, /* valid request the library does not support */
     SPEC_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than *_workspace() */
     SPEC_ERR_CUDA = 4         /* a CUDA runtime call failed */
 } spec_status;
