@@ -57,6 +57,22 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), n, int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def over_ranks(t_dev, tokens, device):
+    """Whole-job figures of a timed region: the slowest rank's time and the tokens of all ranks.
+
+    Every rank runs its own replica of the workload (no data-path collective); this is the only
+    exchange, made once after the timed region. With one process it returns its inputs."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(t_dev), float(tokens)
+    t = torch.tensor([float(t_dev)], dtype=torch.float64, device=device)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -496,14 +512,7 @@ def run_ours(args):
         dist.barrier()
     t_dev = e0.elapsed_time(e1) / 1e3
     tokens = int(gen.hist_len.sum().item()) - acc_before
-    if world > 1:
-        tt = torch.tensor([t_dev, float(tokens)], dtype=torch.float64, device=dev)
-        tmax = tt.clone()
-        dist.all_reduce(tmax[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(tt[1:], op=dist.ReduceOp.SUM)
-        t_all, tokens_all = float(tmax[0]), float(tt[1])
-    else:
-        t_all, tokens_all = t_dev, float(tokens)
+    t_all, tokens_all = over_ranks(t_dev, tokens, dev)
     value = tokens_all / t_all
     rows_per_s = N_SEQ * (WIDTH + 1) * args.steps * world / t_all
     acceptance = tokens / (args.steps * N_SEQ) - 1.0   # accepted drafts per sequence-step
