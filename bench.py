@@ -150,13 +150,10 @@ def count_launches(fn):
         orig[name] = f
 
         def wrap(*a, _n=name, _f=f, **k):
-            if _n == "spec_qmatmul":   # one launch per pass: 80 columns, the last <= 16 columns in a 16-wide one
+            if _n == "spec_qmatmul":   # one launch per pass of 8 or 16 columns, two (pack + matmul) per 80
                 nc = int(a[5])
-                passes = 0
-                while nc > 0:
-                    nc -= 16 if nc <= 16 else 80
-                    passes += 1
-                counts[_n] = counts.get(_n, 0) + passes
+                per = 8 if nc <= 8 else (16 if nc <= 16 else 80)
+                counts[_n] = counts.get(_n, 0) + (nc + per - 1) // per * (2 if nc > 16 else 1)
             else:
                 counts[_n] = counts.get(_n, 0) + 1
             return _f(*a, **k)

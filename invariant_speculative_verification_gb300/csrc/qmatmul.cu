@@ -1,5 +1,4 @@
-// K1: batch-invariant int4 block-32 dequantising matmul on the 5th-generation
-// tensor cores (sm_103a: tcgen05.mma, tensor memory, TMA).
+// K1: batch-invariant int4 block-32 dequantising matmul (sm_103a).
 //
 //   y[j][n] = sum_k x[j][k] * d[n][k/32] * (nib(n, k) - 8)
 //
@@ -8,37 +7,38 @@
 //  * K is cut into segments of 512 (when K / 256 is odd the last segment is
 //    256 long).  The cut depends on K only.
 //  * Inside a segment, for every 32-k block b in ascending order, the block
-//    partial P_b is one chain of two K=16 tensor-core MMAs (fp32 accumulator,
-//    the first starting from zero) of A = q = code - 8 (bf16, exact) and B =
-//    column j of x (bf16); then s = fma(d_b, P_b, s) with s starting at +0.
+//    partial P_b is one chain of two m16n8k16 bf16 MMAs whose A operand is the
+//    code c = q + 8 plus 128 (exactly representable) and whose C operand starts
+//    at -136 * sum_{k in b} x[j][k] (column j's block sum in fp32, its four
+//    8-k chunks summed in k order and then in chunk order), so P_b = sum q x up
+//    to MMA rounding; then s = fma(d_b, P_b, s) with s starting at +0.
 //  * The segment sums are folded in ascending order: y = ((s_0 + s_1) + s_2)...
-// Column j's P_b depends only on A and on B column j: the MMA's N (the number
-// of columns a pass carries, 16 or 80) does not change it, and unused columns
-// are zero.  Which CTA handles a column, and where a CTA's share of the work
-// starts and ends, is scheduling that may depend on the call; the arithmetic
-// above never does.
+// The MMA instruction stream is the same for every column tile and column j's
+// result depends only on A, on B column j and on C column j; unused columns
+// are zero, never a different instruction.  Which CTA, warp or column tile
+// handles a column, and where a CTA's share of the work starts and ends, is
+// scheduling that may depend on the call; the arithmetic above never does.
 //
-// Execution: a persistent grid of one CTA per SM over (128-row tile x
-// K-segment) units dealt out in equal contiguous ranges (stream-K).  Per CTA:
-//  * a TMA warp streams each 256-k stage into a ring of shared-memory slots:
-//    the int4 codes (128 rows x 128 bytes, 128-byte swizzle), the fp16 scales
-//    and the pass's activation columns (four 64-k x NP-row boxes, 128-byte
-//    swizzle: the MMA's B operand as it lands; columns past n_cols arrive as
-//    zeros);
-//  * eight dequantising warps (two per TMEM lane quarter, alternate blocks)
-//    turn each block's codes into bf16 q and store them into one of eight
-//    TMEM A buffers (lane = weight row);
-//  * one thread issues the two MMAs of each block into one of several TMEM
-//    accumulator buffers and commits them to mbarriers;
-//  * eight epilogue warps (thread = weight row, half of the columns each) load
-//    each block's accumulator from TMEM and apply the scale FMA in registers,
-//    keep the tile's segment fold in TMEM and write y.
-// A tile covered by one CTA is written directly.  A tile shared by several
-// CTAs: the CTAs holding its later segments store their segment sums and count
-// themselves in, without waiting; the CTA holding the leading segments folds
-// them in segment order once all have arrived (the usual case when it gets
-// there), else leaves its prefix for whichever CTA arrives last.  No CTA waits
-// for another; the counters end at zero.
+// Execution: a persistent grid of one CTA per SM, each with eight consumer
+// warps (16 weight rows each, 128 rows per tile) and one TMA warp.  The
+// (128-row tile x K-segment) units are dealt out in equal contiguous ranges
+// (stream-K), so every SM streams the same number of bytes.  The TMA warp's
+// lane 0 issues cp.async.bulk.tensor copies of each stage -- the int4 codes
+// (128-row x 128-byte boxes, 128B swizzle) and the fp16 scales -- into a ring
+// of mbarrier-guarded stages.  Passes of up to 16 columns use 512-k stages and
+// two activation warps, which read the stage's activation columns from L2,
+// write them in MMA B-fragment order together with the block sums and hand the
+// stage on.  The 80-column pass uses 256-k stages (a segment is two stages;
+// only the delivery changes, not the arithmetic); its activations are packed
+// into that same layout once per call by xpack_kernel and copied in with the
+// stage by one cp.async.bulk.  Consumers issue only ldmatrix, 4 LOP3 + 3
+// shifts per 8 weights, lds and mma.sync.  A tile covered by one CTA is folded
+// in registers and written directly.  A tile shared by several CTAs: the CTAs
+// holding its later segments store their segment sums and count themselves
+// in, without waiting; the CTA holding the leading segments folds them in
+// segment order once all have arrived (the usual case when it gets there),
+// else leaves its prefix for whichever CTA arrives last.  No CTA waits for
+// another; the counters end at zero.
 //
 // The weight format (int4 block 32, fp16 scale, even k in the low nibble) is
 // the stand-in for the block-quantised formats named in ramgpt.org, "When
@@ -51,44 +51,50 @@
 namespace {
 
 constexpr int SEG_K = 512;                   // k per K-segment (the invariant reduction unit)
-constexpr int KS = 256;                      // k per stage
-constexpr int NBLK = KS / 32;                // 32-k blocks per stage
-constexpr int BM = 128;                      // weight rows per tile (= TMEM lanes)
-constexpr int NEW = 8;                       // epilogue warps 0..7
-constexpr int NQW = 8;                       // dequantising warps 8..15
-constexpr int W_TMA = NEW + NQW;             // warp 16
-constexpr int W_MMA = W_TMA + 1;             // warp 17 (also owns the TMEM allocation)
-constexpr int THREADS = (W_MMA + 1) * 32;
-constexpr int W_BYTES = BM * 128;            // one stage of codes
-constexpr int S_BYTES = BM * NBLK * 2;       // one stage of scales
+constexpr int BM = 128;                      // weight rows per tile
+constexpr int NCW = 8;                       // consumer warps (16 rows each)
+constexpr int W_BOX = BM * 128;              // one 128-row x 128-byte code box (256 k)
+constexpr int MAX_NT = 10;                   // column tiles per pass (80 columns)
 constexpr int SMEM_BUDGET = 226 * 1024;
-constexpr int MAX_NP = 80;                   // columns per pass, at most
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t YCOL = 288;               // TMEM columns of the running segment fold
-constexpr uint32_t ACOL = 384;               // TMEM columns of the eight A buffers (16 each)
+// Arrival counters of a call lie in the workspace's first 4 x tiles bytes; no
+// call has more than CNT_LIMIT / 4 tiles.  A call's stored sums and prefixes
+// that lie below CNT_LIMIT are cleared once read, so every call finds its
+// counters at zero whatever calls of other shapes used the workspace before.
+constexpr size_t CNT_LIMIT = 64 * 1024;
 
-template <int NP>
+// Narrow passes (<= 16 columns) stream 512-k stages and prepare each stage's
+// activations in the CTA (two activation warps).  The 80-column pass uses
+// 256-k stages (its activations are 5x larger); its activations are prepared
+// once per call by a small kernel (xpack_kernel) into the workspace, in the
+// very byte layout of a stage, and each stage's part is copied in by TMA.
+// The stage size only changes how a segment is delivered, never its arithmetic.
+template <int NT>
 struct Cfg {
-    static_assert(NP % 16 == 0 && NP >= 16 && NP <= MAX_NP, "columns per pass");
-    static constexpr int NH = NP / 2;                          // columns per epilogue thread
-    static constexpr int X_BOX = NP * 128;                     // 64 k of the pass's columns
-    static constexpr int S_OFF = W_BYTES, X_OFF = W_BYTES + S_BYTES;
-    static constexpr int STAGE = X_OFF + 4 * X_BOX;
-    static constexpr int NS_FIT = (SMEM_BUDGET - 2048) / STAGE;
-    static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;         // ring slots
-    static constexpr int ND = NP <= 32 ? 8 : 3;                // TMEM accumulator buffers
-    static constexpr uint32_t DP = NP <= 32 ? 32 : 96;         // their column pitch
-    static constexpr int NBAR = 2 * NS + 2 * NBLK + 2 * ND + 1;
-    static constexpr int SMEM = 1024 + NS * STAGE + NBAR * 8 + 64;
-    static constexpr uint32_t IDESC = dev::mma_idesc_bf16(BM, NP);
-    static_assert(ND * DP <= YCOL && YCOL + NP <= ACOL && ACOL + 16 * NBLK <= TMEM_COLS, "TMEM map");
-    static_assert(STAGE % 1024 == 0 && X_OFF % 1024 == 0 && X_BOX % 1024 == 0, "swizzle atoms 1024-aligned");
+    static constexpr int KS = NT >= 10 ? 256 : 512;         // k per stage
+    static constexpr int NBLK = KS / 32;                    // 32-k blocks per stage
+    static constexpr int NWBOX = KS / 256;                  // code boxes per stage
+    static constexpr bool XPACK = NT >= 10;                 // activations pre-packed per call
+    static constexpr int NXW = XPACK ? 0 : 2;               // activation warps
+    static constexpr int THREADS = (NCW + 1 + NXW) * 32;    // + TMA warp
+    static constexpr int W_BYTES = NWBOX * W_BOX;
+    static constexpr int S_BYTES = BM * NBLK * 2;
+    static constexpr int X_BOX = 8 * NT * 128;              // 64 k of the pass's activation columns
+    static constexpr int X_BYTES = (NBLK / 2) * X_BOX;
+    static constexpr int CI_BYTES = NBLK * 8 * NT * 4;      // [blocks][8 NT slots] fp32
+    // stage layout: codes | scales | activations (B-fragment order) | -136 x block sums
+    static constexpr int S_OFF = W_BYTES, X_OFF = W_BYTES + S_BYTES, CI_OFF = X_OFF + X_BYTES;
+    static constexpr int XC_BYTES = X_BYTES + CI_BYTES;     // one stage of packed activations
+    static constexpr int RAW = W_BYTES + X_BYTES + S_BYTES + CI_BYTES;
+    static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
+    static constexpr int NS = (SMEM_BUDGET / STAGE) > 6 ? 6 : (SMEM_BUDGET / STAGE);
+    static constexpr int SMEM = 1024 + NS * STAGE + 3 * NS * 8 + 64;
     static_assert(NS >= 2, "at least two stages");
+    static_assert(X_OFF % 128 == 0 && XC_BYTES % 16 == 0, "activation area alignment");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// the pass width used for the columns col0 .. n_cols - 1 that remain
-inline int pass_np(int remaining) { return remaining <= 16 ? 16 : MAX_NP; }
+// 32-k blocks per stage of a pass with nt column tiles (the scale box width)
+inline int stage_blocks(int nt) { return nt >= MAX_NT ? Cfg<MAX_NT>::NBLK : nt == 2 ? Cfg<2>::NBLK : Cfg<1>::NBLK; }
 
 // number of K-segments of length seg_k (the last may be shorter)
 inline int n_segments(int K, int seg_k) { return (K + seg_k - 1) / seg_k; }
@@ -101,490 +107,523 @@ struct Sched {
     __device__ int cta_of(long long u) const { return (int)(((u + 1) * G - 1) / U); }
 };
 
-// The 32 codes of one block of one weight row (16 bytes, byte i = k 2i in the
-// low nibble, k 2i+1 in the high one) -> 16 bf16x2 registers of q = code - 8,
-// register m = (k 2m, k 2m+1), exact.
-__device__ __forceinline__ void codes_to_q(const uint4 &w4, uint32_t (&a)[16]) {
-    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+// nibble codes (k = 8t .. 8t+7 of a block) -> (128 + code_m, 128 + code_{m+4}), exact
+__device__ __forceinline__ void codes_to_bf16(uint32_t w, uint32_t (&o)[4]) {
+    o[0] = dev::lop3_and_or(w, 0x000F000Fu, 0x43004300u);
+    o[1] = dev::lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);
+    o[2] = dev::lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);
+    o[3] = dev::lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);
+}
+
+// The activations of one (32-k block, column) pair of a stage: four 16-byte
+// chunks of k = kb .. kb + 31 of column col (zero past K or n_cols).
+__device__ __forceinline__ void load_pair(uint4 (&v)[4], const uint16_t *__restrict__ x, int ldx, int K, int n_cols,
+                                          int col, int kb) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        const uint32_t u = w[t] >> 4;   // byte i of u holds k 8t+2i+1 in its low nibble
+    for (int q = 0; q < 4; ++q) {
+        v[q] = make_uint4(0, 0, 0, 0);
+        if (col < n_cols && kb + 8 * q < K) v[q] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)col * ldx + kb + 8 * q));
+    }
+}
+
+// Writes pair (blk, c) of a stage: the bf16 values in MMA B-fragment order into
+// the stage's activation area xs, and -136 x the block sum into ci (the block
+// sum is the four 8-k chunk sums, each summed in k order, added in chunk order).
+template <int NT>
+__device__ __forceinline__ void put_pair(const uint4 (&v)[4], int blk, int c, uint8_t *xs, float *ci) {
+    uint8_t *row = xs + (blk >> 1) * Cfg<NT>::X_BOX + c * 128;
+    float sum = 0.f;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            // byte 0 <- byte m of w (k 8t+2m), byte 2 <- byte m of u (k 8t+2m+1)
-            const uint32_t p = dev::prmt(w[t], u, 0x0400u + 0x0101u * (uint32_t)m);
-            const uint32_t b = dev::lop3_and_or(p, 0x000F000Fu, 0x43004300u);   // 128 + code, two bf16
-            uint32_t r;
-            asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(0x3F803F80u), "r"(0xC308C308u));   // - 136
-            a[4 * t + m] = r;
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+        float cs = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            cs += __uint_as_float(w4[e] << 16);
+            cs += __uint_as_float(w4[e] & 0xFFFF0000u);
         }
+        sum = (q == 0) ? cs : sum + cs;
+        uint4 o;
+        o.x = dev::prmt(w4[0], w4[2], 0x5410);   // (x0, x4)
+        o.y = dev::prmt(w4[0], w4[2], 0x7632);   // (x1, x5)
+        o.z = dev::prmt(w4[1], w4[3], 0x5410);   // (x2, x6)
+        o.w = dev::prmt(w4[1], w4[3], 0x7632);   // (x3, x7)
+        const int chunk = (((blk & 1) * 4 + q) ^ (c & 7)) << 4;
+        *reinterpret_cast<uint4 *>(row + chunk) = o;
     }
+    // MMA column slot g carries activation column pi(g) = (g & 1) * 4 + g / 2
+    const int cc = c & 7, slot = (cc & 3) * 2 + (cc >> 2);
+    ci[blk * 8 * NT + (c & ~7) + slot] = -136.0f * sum;
 }
 
-// TMEM <-> registers for one epilogue thread's NH columns
-template <int NH>
-__device__ __forceinline__ void tm_load(uint32_t taddr, float (&v)[NH]) {
-    if constexpr (NH == 8) {
-        dev::tmem_ld8(taddr, v);
-    } else {
-        static_assert(NH == 40, "epilogue width");
-        dev::tmem_ld32(taddr, v);
-        float t[8];
-        dev::tmem_ld8(taddr + 32, t);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[32 + j] = t[j];
-    }
+// Packs the activations of one pass (columns col0 .. col0 + 8 NT - 1) for every
+// stage of K into out: stage st occupies out[st * XC_BYTES ...] in the byte
+// layout of a stage's activation and block-sum areas.
+template <int NT>
+__global__ void __launch_bounds__(256) xpack_kernel(const uint16_t *__restrict__ x, int ldx, int K, int n_cols, int col0,
+                                                    uint8_t *__restrict__ out) {
+    using C = Cfg<NT>;
+    dev::pdl_wait();   // x is the preceding kernel's output; out may still be read by it
+    dev::pdl_launch_dependents();
+    constexpr int PAIRS = C::NBLK * 8 * NT;   // per stage
+    const long long p = blockIdx.x * 256ll + threadIdx.x;
+    const int st = (int)(p / PAIRS), pr = (int)(p % PAIRS);
+    if (st * C::KS >= K) return;
+    const int blk = pr / (8 * NT), c = pr % (8 * NT);
+    uint4 v[4];
+    load_pair(v, x, ldx, K, n_cols, col0 + c, st * C::KS + 32 * blk);
+    uint8_t *base = out + (size_t)st * C::XC_BYTES;
+    put_pair<NT>(v, blk, c, base, reinterpret_cast<float *>(base + C::X_BYTES));
 }
 
-template <int NH>
-__device__ __forceinline__ void tm_store(uint32_t taddr, const float (&v)[NH]) {
-    if constexpr (NH == 8) {
-        dev::tmem_st8(taddr, v);
-    } else {
-        dev::tmem_st32(taddr, v);
-        dev::tmem_st8(taddr + 32, v + 32);
-    }
+__device__ __forceinline__ void named_sync_consumers() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
 }
 
-__device__ __forceinline__ void named_sync_epilogue() {
-    asm volatile("bar.sync 1, %0;" ::"n"(NEW * 32) : "memory");
-}
-
-// all lanes agree: every lane's wait succeeded
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, dev::mbar_wait(bar, parity)) != 0;
-}
-
-template <int NP, bool OUT_BF16>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int NT, bool OUT_BF16>
+__global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ts,
-           const __grid_constant__ CUtensorMap tx, int N, int K, int n_cols, int col0, void *__restrict__ y, int ldy,
+           const uint16_t *__restrict__ x, int ldx, int N, int K, int n_cols, int col0, void *__restrict__ y, int ldy,
            int accumulate, Sched sch, float *__restrict__ wsp_prefix, float *__restrict__ wsp_seg,
-           int *__restrict__ counters, int32_t *dev_err) {
-    using C = Cfg<NP>;
-    constexpr int NH = C::NH;
+           int *__restrict__ counters, const uint8_t *__restrict__ xpk, int32_t *dev_err) {
+    using C = Cfg<NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NS * C::STAGE);
-    uint64_t *empty = full + C::NS;
-    uint64_t *afull = empty + C::NS;
-    uint64_t *aempty = afull + NBLK;
-    uint64_t *dfull = aempty + NBLK;
-    uint64_t *dempty = dfull + C::ND;
-    uint64_t *done = dempty + C::ND;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
-    int *flag = reinterpret_cast<int *>(tslot + 2);
+    uint64_t *ready = full + C::NS;
+    uint64_t *empty = ready + C::NS;
+    int *flag = reinterpret_cast<int *>(empty + C::NS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nst_total = K / KS;                     // stages of K
+    const int nst_total = (K + C::KS - 1) / C::KS;   // stages of this pass's size
     const int seg_st = sch.seg_st, ks = sch.ks;       // stages per segment, segments
     const long long ua = sch.begin(blockIdx.x), ub = sch.begin(blockIdx.x + 1);
+    constexpr int TILE_ELEMS = BM * 8 * NT;     // one tile's values for this pass
+    // Partial sums in the workspace keep the accumulator fragments as the
+    // consumer threads hold them: [column tile][warp][lane][4] floats, so every
+    // store and load is a coalesced 16-byte access by the thread that owns it.
+    const int frag = ((warp * 32 + (threadIdx.x & 31)) * 4);   // + ct * NCW * 128
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NS; ++s) {
             dev::mbar_init(&full[s], 1);
-            dev::mbar_init(&empty[s], NQW + NEW + 1);   // codes, scales and (by commit) activations read
+            dev::mbar_init(&ready[s], 1);
+            dev::mbar_init(&empty[s], NCW);
         }
-        for (int b = 0; b < NBLK; ++b) {
-            dev::mbar_init(&afull[b], 4);               // the four lane quarters of the A buffer
-            dev::mbar_init(&aempty[b], 1);
-        }
-        for (int d = 0; d < C::ND; ++d) {
-            dev::mbar_init(&dfull[d], 1);
-            dev::mbar_init(&dempty[d], NEW);
-        }
-        dev::mbar_init(done, 1);
         dev::fence_barrier_init();
     }
-    if (warp == W_MMA) dev::tmem_alloc(tslot, TMEM_COLS);
-    dev::tc_fence_before();
     __syncthreads();
-    dev::tc_fence_after();
-    const uint32_t tmem = *tslot;
     // The weights and scales are constant inputs: the TMA warp starts streaming
     // them at once, overlapping the tail of the preceding kernel on the stream.
     // Activations are read, and anything global is written, only after that
     // kernel has finished (pdl_wait).
     dev::pdl_launch_dependents();
 
-    // stage sequence of this CTA: units ua..ub-1, each 1 or 2 stages (seg_st for the non-invariant variant)
+    // stage sequence of this CTA: units ua..ub-1, each 1 or 2 stages
     auto unit_stages = [&](long long u) { return min(seg_st, nst_total - (int)(u % ks) * seg_st); };
 
-    if (warp == W_TMA) {
+    if (warp == NCW) {
         // ============================ TMA warp ============================
+        // lane 0 streams the codes (two 128-row x 128-byte boxes per 512-k stage)
+        // and the scales of every stage of this CTA, NS stages ahead of the
+        // consumers, reusing a slot once its consumers have released it.
         if (lane == 0) {
             dev::prefetch_tmap(&tw);
             dev::prefetch_tmap(&ts);
-            dev::prefetch_tmap(&tx);
-            auto load_x = [&](int slot, int k0) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    dev::tma_load_2d(smem + slot * C::STAGE + C::X_OFF + c * C::X_BOX, &tx, k0 + 64 * c, col0,
-                                     &full[slot]);
-            };
             long long iu = ua;
-            int ist = 0, issued = 0;
-            int k0s[C::NS];   // the first NS stages: their activations follow the preceding kernel
+            int ist = 0;
+            int k0s[C::NS];   // packed-activation pass: stages whose activations are still to be copied
             bool x_sent = false;
+            int issued = 0;
             for (; iu < ub; ++issued) {
                 const int s = issued % C::NS;
+                if (issued == C::NS && C::XPACK) {
+                    x_sent = true;
+                    // the first NS stages' weights are on their way; the packed activations
+                    // are written by the preceding kernel, so wait for it before copying them
+                    dev::pdl_wait();
+                    for (int j = 0; j < C::NS; ++j)
+                        dev::bulk_load(smem + j * C::STAGE + C::X_OFF, xpk + (size_t)(k0s[j] / C::KS) * C::XC_BYTES,
+                                       C::XC_BYTES, &full[j]);
+                }
                 if (issued >= C::NS && !dev::mbar_wait(&empty[s], ((issued / C::NS) - 1) & 1)) {
                     dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     break;
                 }
                 const int tile = (int)(iu / ks);
-                const int k0 = ((int)(iu % ks) * seg_st + ist) * KS;
+                const int k0 = ((int)(iu % ks) * seg_st + ist) * C::KS;
                 uint8_t *base = smem + s * C::STAGE;
-                dev::mbar_arrive_expect_tx(&full[s], W_BYTES + S_BYTES + 4 * C::X_BOX);
-                dev::tma_load_2d(base, &tw, k0 / 2, tile * BM, &full[s]);
+                dev::mbar_arrive_expect_tx(&full[s], C::W_BYTES + C::S_BYTES + (C::XPACK ? C::XC_BYTES : 0));
+#pragma unroll
+                for (int b = 0; b < C::NWBOX; ++b)
+                    dev::tma_load_2d(base + b * W_BOX, &tw, k0 / 2 + 128 * b, tile * BM, &full[s]);
                 dev::tma_load_2d(base + C::S_OFF, &ts, k0 / 32, tile * BM, &full[s]);
-                if (x_sent) {
-                    load_x(s, k0);
-                } else {
-                    k0s[issued] = k0;
-                    if (issued + 1 == C::NS) {
-                        dev::pdl_wait();
-                        for (int j = 0; j < C::NS; ++j) load_x(j, k0s[j]);
-                        x_sent = true;
-                    }
+                if (C::XPACK) {
+                    if (issued < C::NS)
+                        k0s[issued] = k0;
+                    else
+                        dev::bulk_load(base + C::X_OFF, xpk + (size_t)(k0 / C::KS) * C::XC_BYTES, C::XC_BYTES, &full[s]);
                 }
                 if (++ist == unit_stages(iu)) {
                     ist = 0;
                     ++iu;
                 }
             }
-            if (!x_sent) {
+            if (C::XPACK && !x_sent) {
+                // no more stages than slots: copy the activations of all of them now
                 dev::pdl_wait();
-                for (int j = 0; j < issued; ++j) load_x(j, k0s[j]);
+                for (int j = 0; j < issued; ++j)
+                    dev::bulk_load(smem + j * C::STAGE + C::X_OFF, xpk + (size_t)(k0s[j] / C::KS) * C::XC_BYTES,
+                                   C::XC_BYTES, &full[j]);
             }
-            // no copy may still be landing in shared memory when the CTA ends
-            for (int j = issued > C::NS ? issued - C::NS : 0; j < issued; ++j)
-                (void)dev::mbar_wait(&full[j % C::NS], (j / C::NS) & 1);
         }
-    } else if (warp == W_MMA) {
-        // ============================ MMA issue ============================
-        if (lane == 0) {
-            long long u = ua;
-            int i = 0;
-            bool ok = true;
-            for (; u < ub && ok; ++u) {
-                const int nstg = unit_stages(u);
-                for (int st = 0; st < nstg && ok; ++st, ++i) {
-                    const int s = i % C::NS;
-                    if (!dev::mbar_wait(&full[s], (i / C::NS) & 1)) {
+        return;
+    }
+    if constexpr (!C::XPACK) {
+    if (warp > NCW) {
+        // ======================== activation warps ========================
+        // warp NCW + 1 + h prepares stages i with i % C::NXW == h: it reads the
+        // stage's activation columns from L2 (all loads of a group in flight),
+        // writes them in B-fragment order with their block sums, waits for the
+        // stage's TMA bytes, then hands the stage to the consumers.
+        const int h = warp - NCW - 1;
+        dev::pdl_wait();   // x may be the preceding kernel's output
+        bool ok = true;
+        long long pu = ua;
+        int pst = 0;
+        for (int i = 0; pu < ub; ++i) {
+            const int k0 = ((int)(pu % ks) * seg_st + pst) * C::KS;
+            if (++pst == unit_stages(pu)) {
+                pst = 0;
+                ++pu;
+            }
+            if (i % C::NXW != h) continue;
+            const int s = i % C::NS;
+            bool slot_free = (i < C::NS);   // the slot's previous stage must be released before writing
+            uint8_t *xs = smem + s * C::STAGE + C::X_OFF;
+            float *ci = reinterpret_cast<float *>(smem + s * C::STAGE + C::CI_OFF);
+            // (block, column) pairs p = lane + 32 j
+            constexpr int PAIRS = C::NBLK * 8 * NT / 32;   // per lane
+            constexpr int GROUP = 4;                  // pairs whose loads are in flight together
+#pragma unroll 1
+            for (int j0 = 0; j0 < PAIRS; j0 += GROUP) {
+                uint4 v[GROUP][4];
+#pragma unroll
+                for (int jj = 0; jj < GROUP; ++jj) {
+                    const int p = lane + 32 * (j0 + jj);
+                    const int blk = p / (8 * NT), c = p % (8 * NT);
+                    load_pair(v[jj], x, ldx, K, n_cols, col0 + c, k0 + 32 * blk);
+                }
+                if (!slot_free) {   // loads are in flight; now wait for the consumers' release
+                    int got = 1;
+                    if (lane == 0 && ok) got = dev::mbar_wait(&empty[s], ((i / C::NS) - 1) & 1) ? 1 : 0;
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got && ok) {
+                        if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                         ok = false;
-                        break;
                     }
-                    dev::tc_fence_after();
-                    const uint32_t xb = dev::smem_u32(smem + s * C::STAGE + C::X_OFF);
-                    for (int b = 0; b < NBLK; ++b) {
-                        const int g = i * NBLK + b, db = g % C::ND;
-                        if (!dev::mbar_wait(&afull[b], i & 1) ||
-                            !dev::mbar_wait(&dempty[db], ((g / C::ND) & 1) ^ 1)) {
-                            ok = false;
-                            break;
-                        }
-                        dev::tc_fence_after();
-                        const uint32_t d = tmem + db * C::DP, a = tmem + ACOL + 16 * b;
-                        const uint32_t bx = xb + (b >> 1) * C::X_BOX + (b & 1) * 64;
-                        dev::mma_bf16_tmem_a(d, a, dev::sw128_kmajor_desc(bx), C::IDESC, 0u);
-                        dev::mma_bf16_tmem_a(d, a + 8, dev::sw128_kmajor_desc(bx + 32), C::IDESC, 1u);
-                        dev::tc_commit(&aempty[b]);
-                        dev::tc_commit(&dfull[db]);
-                    }
-                    if (ok) dev::tc_commit(&empty[s]);
+                    slot_free = true;
+                }
+#pragma unroll
+                for (int jj = 0; jj < GROUP; ++jj) {
+                    const int p = lane + 32 * (j0 + jj);
+                    put_pair<NT>(v[jj], p / (8 * NT), p % (8 * NT), xs, ci);
                 }
             }
-            if (!ok) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
-            // every MMA is complete before the TMEM is released
-            dev::tc_commit(done);
-            (void)dev::mbar_wait(done, 0);
+            int got = 1;
+            if (lane == 0 && ok) got = dev::mbar_wait(&full[s], (i / C::NS) & 1) ? 1 : 0;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got && ok) {
+                if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                ok = false;
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(&ready[s]);
         }
-    } else if (warp >= NEW) {
-        // ======================== dequantising warps ========================
-        const int q = warp & 3, h = (warp - NEW) >> 2;
-        const int row = 32 * q + lane;
-        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + ACOL;
-        long long u = ua;
-        int i = 0;
-        bool ok = true;
-        for (; u < ub && ok; ++u) {
+        return;
+    }
+    }
+
+    // ============================ consumers ============================
+    dev::pdl_wait();   // y (accumulate), the workspace and y writes follow the preceding kernel
+    const int r = lane >> 2, t = lane & 3;
+    const int wrow = warp * 16;
+    const int g = lane >> 2;
+    const int xcol = (g & 1) * 4 + (g >> 1);   // activation column of this lane's B fragment
+    float yrun[NT][4];
+    int i = 0;
+    bool ok = true;
+    long long u = ua;
+    int nh_tile = -1, nh_prev = 0, nh_touch = 0;   // thread 0: this CTA's later-segment part, if any
+
+    // y for this thread's fragments of `tile` from yrun
+    auto store_tile = [&](int tile) {
+        auto store_y = [&](int c, int row, float v) {
+            const int col = col0 + c, n = tile * BM + row;
+            if (col < n_cols && n < N) {
+                if (OUT_BF16) {
+                    reinterpret_cast<__nv_bfloat16 *>(y)[(size_t)col * ldy + n] = __float2bfloat16_rn(v);
+                } else {
+                    float *yp = reinterpret_cast<float *>(y) + (size_t)col * ldy + n;
+                    *yp = accumulate ? (*yp + v) : v;
+                }
+            }
+        };
+#pragma unroll
+        for (int ct = 0; ct < NT; ++ct) {
+            store_y(ct * 8 + t, wrow + r, yrun[ct][0]);
+            store_y(ct * 8 + t + 4, wrow + r, yrun[ct][1]);
+            store_y(ct * 8 + t, wrow + r + 8, yrun[ct][2]);
+            store_y(ct * 8 + t + 4, wrow + r + 8, yrun[ct][3]);
+        }
+    };
+    // yrun holds the fold of segments 0 .. seg_from-1 of `tile`: add the stored
+    // sums of segments seg_from .. ks-1 in ascending order, write y and reset the
+    // tile's counter.  Each stored sum is zeroed once read, so the partial-sum
+    // area is left zero-filled: a later call whose counters lie where this call
+    // kept sums (it has more tiles) finds them at zero.
+    // zero a stored float4 of the workspace if it lies where a call's counters may be
+    auto clear_low = [&](float *p, bool used) {
+        if (used && (size_t)(reinterpret_cast<const uint8_t *>(p) - reinterpret_cast<const uint8_t *>(counters)) <
+                        CNT_LIMIT)
+            __stcg(reinterpret_cast<float4 *>(p), make_float4(0.f, 0.f, 0.f, 0.f));
+    };
+    auto fold_tile = [&](int tile, int seg_from) {
+        float *p0 = wsp_seg + (size_t)tile * ks * TILE_ELEMS + frag;
+        constexpr int SG = NT >= 8 ? 2 : (NT >= 2 ? 4 : 8);   // segments whose loads are in flight together
+        int sg = seg_from;
+        for (; sg + SG <= ks; sg += SG) {
+            float4 l[SG][NT];
+#pragma unroll
+            for (int q = 0; q < SG; ++q)
+#pragma unroll
+                for (int ct = 0; ct < NT; ++ct)
+                    l[q][ct] = (col0 + ct * 8 < n_cols)
+                                   ? __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)(sg + q) * TILE_ELEMS +
+                                                                             ct * NCW * 128))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < SG; ++q)
+#pragma unroll
+                for (int ct = 0; ct < NT; ++ct) {
+                    yrun[ct][0] += l[q][ct].x;
+                    yrun[ct][1] += l[q][ct].y;
+                    yrun[ct][2] += l[q][ct].z;
+                    yrun[ct][3] += l[q][ct].w;
+                }
+        }
+        for (; sg < ks; ++sg) {
+#pragma unroll
+            for (int ct = 0; ct < NT; ++ct) {
+                if (col0 + ct * 8 < n_cols) {
+                    const float4 l = __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)sg * TILE_ELEMS +
+                                                                             ct * NCW * 128));
+                    yrun[ct][0] += l.x, yrun[ct][1] += l.y, yrun[ct][2] += l.z, yrun[ct][3] += l.w;
+                }
+            }
+        }
+        store_tile(tile);
+        if (threadIdx.x == 0) counters[tile] = 0;
+        // every sum is read: clear those a later call could take for counters
+        // (after all loads, so none waits behind these stores)
+        for (sg = seg_from; sg < ks; ++sg)
+#pragma unroll
+            for (int ct = 0; ct < NT; ++ct)
+                clear_low(p0 + (size_t)sg * TILE_ELEMS + ct * NCW * 128, col0 + ct * 8 < n_cols);
+    };
+
+    while (u < ub) {
+        const int tile = (int)(u / ks);
+        const long long tile_u0 = (long long)tile * ks;
+        const long long u_end = min(ub, tile_u0 + ks);     // this CTA's units of this tile
+        const bool head = (u == tile_u0);
+        const bool whole = head && (u_end == tile_u0 + ks);
+#pragma unroll
+        for (int ct = 0; ct < NT; ++ct) yrun[ct][0] = yrun[ct][1] = yrun[ct][2] = yrun[ct][3] = 0.f;
+        for (; u < u_end; ++u) {
+            const int seg = (int)(u - tile_u0);
             const int nstg = unit_stages(u);
+            float acc[NT][4];
+#pragma unroll
+            for (int ct = 0; ct < NT; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
             for (int st = 0; st < nstg; ++st, ++i) {
                 const int s = i % C::NS;
-                if (!warp_wait(&full[s], (i / C::NS) & 1)) {
+                if (ok && !dev::mbar_wait(C::XPACK ? &full[s] : &ready[s], (i / C::NS) & 1)) {
+                    dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     ok = false;
-                    break;
                 }
-                const uint32_t wrow = dev::smem_u32(smem + s * C::STAGE) + row * 128;
-                for (int b = h; b < NBLK; b += 2) {
-                    if (!warp_wait(&aempty[b], (i & 1) ^ 1)) {
-                        ok = false;
-                        break;
+                const uint32_t wbase = dev::smem_u32(smem + s * C::STAGE);
+                const uint32_t xbase = wbase + C::X_OFF;
+                const uint32_t sbase = wbase + C::S_OFF;
+                const uint32_t cbase = wbase + C::CI_OFF;
+                constexpr int BP_UNROLL = NT > 4 ? 1 : C::NBLK / 2;
+#pragma unroll BP_UNROLL
+                for (int bp = 0; bp < C::NBLK / 2; ++bp) {
+                    uint32_t wv[4];
+                    {
+                        // blocks 2bp, 2bp+1: box bp/4 (256 k each), 16-byte chunk (2bp + m/2) % 8
+                        const int m = lane >> 3, rr = lane & 7;
+                        const int row = wrow + (m & 1) * 8 + rr;
+                        const int blk = 2 * bp + (m >> 1);
+                        dev::ldmatrix_x4(wv[0], wv[1], wv[2], wv[3],
+                                         wbase + (blk >> 3) * W_BOX + row * 128 + (((blk & 7) ^ (row & 7)) << 4));
                     }
-                    uint4 w4;
-                    dev::lds128(w4.x, w4.y, w4.z, w4.w, wrow + ((b ^ (row & 7)) << 4));
-                    uint32_t a[16];
-                    codes_to_q(w4, a);
-                    dev::tmem_st16(ta + 16 * b, a);
-                    dev::tmem_wait_st();
-                    dev::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) dev::mbar_arrive(&afull[b]);
+                    uint32_t s2, s28;   // the two fp16 scales of blocks 2bp, 2bp+1 for rows r and r+8
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2) : "r"(sbase + (wrow + r) * (2 * C::NBLK) + bp * 4));
+                    asm volatile("ld.shared.u32 %0, [%1];"
+                                 : "=r"(s28)
+                                 : "r"(sbase + (wrow + r + 8) * (2 * C::NBLK) + bp * 4));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int blk = 2 * bp + h;
+                        uint32_t ar[4], ar8[4];
+                        codes_to_bf16(wv[2 * h], ar);
+                        codes_to_bf16(wv[2 * h + 1], ar8);
+                        const float d_r = __half2float(__ushort_as_half((unsigned short)(s2 >> (16 * h))));
+                        const float d_r8 = __half2float(__ushort_as_half((unsigned short)(s28 >> (16 * h))));
+#pragma unroll
+                        for (int ct = 0; ct < NT; ++ct) {
+                            const int xrow = ct * 8 + xcol;
+                            const int chunk = ((blk & 1) * 4 + t) ^ (xrow & 7);
+                            uint32_t b00, b01, b10, b11;
+                            dev::lds128(b00, b01, b10, b11, xbase + (blk >> 1) * C::X_BOX + xrow * 128 + (chunk << 4));
+                            float c0, c1;
+                            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                                         : "=f"(c0), "=f"(c1)
+                                         : "r"(cbase + (blk * 8 * NT + ct * 8 + 2 * t) * 4));
+                            const float cinit[4] = {c0, c1, c0, c1};
+                            float p[4];
+                            dev::mma_bf16(p, ar[0], ar8[0], ar[1], ar8[1], b00, b01, cinit);
+                            dev::mma_bf16(p, ar[2], ar8[2], ar[3], ar8[3], b10, b11, p);
+                            acc[ct][0] = fmaf(d_r, p[0], acc[ct][0]);
+                            acc[ct][1] = fmaf(d_r, p[1], acc[ct][1]);
+                            acc[ct][2] = fmaf(d_r8, p[2], acc[ct][2]);
+                            acc[ct][3] = fmaf(d_r8, p[3], acc[ct][3]);
+                        }
+                    }
                 }
-                if (!ok) break;
                 __syncwarp();
                 if (lane == 0) dev::mbar_arrive(&empty[s]);
             }
-        }
-        if (!ok && lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
-    } else {
-        // ============================ epilogue ============================
-        const int q = warp & 3, e = warp >> 2;
-        const int row = 32 * q + lane;
-        const int cbeg = e * NH;                                   // this thread's first column of the pass
-        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-        float *seg_base = wsp_seg + (size_t)row * NP + cbeg;        // + (tile * ks + seg) * BM * NP
-        dev::pdl_wait();   // y (accumulate), the workspace and y writes follow the preceding kernel
-        float acc[NH];
-        float yr[NH];
-        int i = 0;
-        bool ok = true;
-        long long u = ua;
-        int nh_tile = -1, nh_prev = 0, nh_touch = 0;   // thread 0: this CTA's later-segment part, if any
-
-        auto store_tile = [&](int tile) {
-            const int n = tile * BM + row;
-            if (n >= N) return;
+            if (head) {
+                // this CTA holds the tile's leading segments: fold them in order
 #pragma unroll
-            for (int j = 0; j < NH; ++j) {
-                const int col = col0 + cbeg + j;
-                if (col < n_cols) {
-                    if (OUT_BF16) {
-                        reinterpret_cast<__nv_bfloat16 *>(y)[(size_t)col * ldy + n] = __float2bfloat16_rn(yr[j]);
-                    } else {
-                        float *yp = reinterpret_cast<float *>(y) + (size_t)col * ldy + n;
-                        *yp = accumulate ? (*yp + yr[j]) : yr[j];
-                    }
-                }
-            }
-        };
-        // yr holds the fold of segments 0 .. seg_from-1 of `tile`: add the stored
-        // sums of segments seg_from .. ks-1 in ascending order, write y and reset
-        // the tile's counter.  Each stored sum is zeroed once read, so the whole
-        // workspace is left zero-filled: a later call whose counters lie where
-        // this call kept sums finds them at zero.
-        auto fold_tile = [&](int tile, int seg_from) {
-            for (int sg = seg_from; sg < ks; ++sg) {
-                float4 *p = reinterpret_cast<float4 *>(seg_base + ((size_t)tile * ks + sg) * BM * NP);
-                float4 l[NH / 4];
+                for (int ct = 0; ct < NT; ++ct)
 #pragma unroll
-                for (int j = 0; j < NH / 4; ++j) l[j] = __ldcg(p + j);
-#pragma unroll
-                for (int j = 0; j < NH / 4; ++j) __stcg(p + j, make_float4(0.f, 0.f, 0.f, 0.f));
-#pragma unroll
-                for (int j = 0; j < NH / 4; ++j) {
-                    yr[4 * j] += l[j].x;
-                    yr[4 * j + 1] += l[j].y;
-                    yr[4 * j + 2] += l[j].z;
-                    yr[4 * j + 3] += l[j].w;
-                }
-            }
-            store_tile(tile);
-            if (threadIdx.x == 0) counters[tile] = 0;
-        };
-        auto load_y_fold = [&]() {
-            if (ok) {
-                tm_load<NH>(tq + YCOL + cbeg, yr);
-                dev::tmem_wait_ld();
+                    for (int e = 0; e < 4; ++e) yrun[ct][e] = (seg == 0) ? acc[ct][e] : yrun[ct][e] + acc[ct][e];
             } else {
+                // a later CTA's segment: store its sum for the final fold
+                float *ps = wsp_seg + ((size_t)tile * ks + seg) * TILE_ELEMS + frag;
 #pragma unroll
-                for (int j = 0; j < NH; ++j) yr[j] = 0.f;
+                for (int ct = 0; ct < NT; ++ct)
+                    if (col0 + ct * 8 < n_cols)
+                        __stcg(reinterpret_cast<float4 *>(ps + ct * NCW * 128),
+                               make_float4(acc[ct][0], acc[ct][1], acc[ct][2], acc[ct][3]));
             }
-        };
-
-        while (u < ub) {
-            const int tile = (int)(u / ks);
-            const long long tile_u0 = (long long)tile * ks;
-            const long long u_end = min(ub, tile_u0 + ks);     // this CTA's units of this tile
-            const bool head = (u == tile_u0);
-            const bool whole = head && (u_end == tile_u0 + ks);
-            for (; u < u_end; ++u) {
-                const int seg = (int)(u - tile_u0);
-                const int nstg = unit_stages(u);
-#pragma unroll
-                for (int j = 0; j < NH; ++j) acc[j] = 0.f;
-                for (int st = 0; st < nstg; ++st, ++i) {
-                    const int s = i % C::NS;
-                    if (ok && !warp_wait(&full[s], (i / C::NS) & 1)) ok = false;
-                    uint4 sc = make_uint4(0, 0, 0, 0);
-                    if (ok)
-                        dev::lds128(sc.x, sc.y, sc.z, sc.w,
-                                    dev::smem_u32(smem + s * C::STAGE + C::S_OFF) + row * (2 * NBLK));
-                    const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
-#pragma unroll 1
-                    for (int b = 0; b < NBLK; ++b) {
-                        const int g = i * NBLK + b, db = g % C::ND;
-                        if (ok && !warp_wait(&dfull[db], (g / C::ND) & 1)) ok = false;
-                        if (ok) {
-                            dev::tc_fence_after();
-                            float v[NH];
-                            tm_load<NH>(tq + db * C::DP + cbeg, v);
-                            dev::tmem_wait_ld();
-                            dev::tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) dev::mbar_arrive(&dempty[db]);
-                            const float d =
-                                __half2float(__ushort_as_half((unsigned short)(scw[b >> 1] >> (16 * (b & 1)))));
-#pragma unroll
-                            for (int j = 0; j < NH; ++j) acc[j] = fmaf(d, v[j], acc[j]);
-                        }
-                    }
-                    __syncwarp();
-                    if (ok && lane == 0) dev::mbar_arrive(&empty[s]);
-                }
-                if (head) {
-                    // this CTA holds the tile's leading segments: fold them in order (in TMEM)
-                    if (seg == 0) {
-#pragma unroll
-                        for (int j = 0; j < NH; ++j) yr[j] = acc[j];
-                    } else {
-                        load_y_fold();
-#pragma unroll
-                        for (int j = 0; j < NH; ++j) yr[j] = yr[j] + acc[j];
-                    }
-                    if (ok) {
-                        tm_store<NH>(tq + YCOL + cbeg, yr);
-                        dev::tmem_wait_st();
-                    }
-                } else {
-                    // a later CTA's segment: store its sum for the final fold
-                    float4 *ps = reinterpret_cast<float4 *>(wsp_seg + ((size_t)tile * ks + seg) * BM * NP +
-                                                            (size_t)row * NP + cbeg);
-#pragma unroll
-                    for (int j = 0; j < NH / 4; ++j)
-                        __stcg(ps + j, make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
-                }
-            }
-            // ---------------- finish this CTA's part of the tile ----------------
-            if (whole) {
-                load_y_fold();
-                store_tile(tile);
-                continue;
-            }
-            const int touch = sch.cta_of(tile_u0 + ks - 1) - sch.cta_of(tile_u0) + 1;   // CTAs sharing the tile
-            if (!head) {
-                // Later segments of a shared tile: publish their sums and move on.  Whether
-                // this CTA was the last to arrive is looked at only after all its units.
-                named_sync_epilogue();             // all partial stores of this CTA are issued
-                if (threadIdx.x == 0) {
-                    __threadfence();               // ... and visible device-wide before the counter moves
-                    nh_prev = atomicAdd(&counters[tile], 1);
-                    nh_tile = tile;
-                    nh_touch = touch;
-                }
-                continue;
-            }
-            // Leading segments of a shared tile (the end of this CTA's range).  Usually
-            // every other CTA has arrived long ago: then fold at once.
-            load_y_fold();
+        }
+        // ---------------- finish this CTA's part of the tile ----------------
+        if (whole) {
+            store_tile(tile);
+            continue;
+        }
+        const int touch = sch.cta_of(tile_u0 + ks - 1) - sch.cta_of(tile_u0) + 1;   // CTAs sharing the tile
+        if (!head) {
+            // Later segments of a shared tile: publish their sums and move on.  Whether
+            // this CTA was the last to arrive is looked at only after all its units.
+            named_sync_consumers();             // all partial stores of this CTA are issued
             if (threadIdx.x == 0) {
-                int seen;
-                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(counters + tile) : "memory");
-                flag[0] = (seen == touch - 1) ? 1 : 0;
+                __threadfence();                // ... and visible device-wide before the counter moves
+                nh_prev = atomicAdd(&counters[tile], 1);
+                nh_tile = tile;
+                nh_touch = touch;
             }
-            named_sync_epilogue();
-            int fold_now = flag[0];
-            if (!fold_now) {
-                // not yet: leave the prefix for whichever CTA arrives last
-                float4 *pp = reinterpret_cast<float4 *>(wsp_prefix + ((size_t)tile * BM + row) * NP + cbeg);
+            continue;
+        }
+        // Leading segments of a shared tile (the end of this CTA's range).  Usually
+        // every other CTA has arrived long ago: then fold at once from registers.
+        if (threadIdx.x == 0) {
+            int seen;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(counters + tile) : "memory");
+            flag[0] = (seen == touch - 1) ? 1 : 0;
+        }
+        named_sync_consumers();
+        int fold_now = flag[0];
+        if (!fold_now) {
+            // not yet: leave the prefix for whichever CTA arrives last
+            float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS + frag;
 #pragma unroll
-                for (int j = 0; j < NH / 4; ++j)
-                    __stcg(pp + j, make_float4(yr[4 * j], yr[4 * j + 1], yr[4 * j + 2], yr[4 * j + 3]));
-                named_sync_epilogue();             // prefix stores issued; flag[0] read by all
-                if (threadIdx.x == 0) {
-                    __threadfence();
-                    const int prev = atomicAdd(&counters[tile], 1);
-                    if (prev == touch - 1) __threadfence();
-                    flag[0] = (prev == touch - 1) ? 1 : 0;
-                }
-                named_sync_epilogue();
-                fold_now = flag[0];
-                if (fold_now) {
-                    // this part arrived last after all: its prefix is not needed, clear it
-#pragma unroll
-                    for (int j = 0; j < NH / 4; ++j) __stcg(pp + j, make_float4(0.f, 0.f, 0.f, 0.f));
-                }
+            for (int ct = 0; ct < NT; ++ct)
+                if (col0 + ct * 8 < n_cols)
+                    __stcg(reinterpret_cast<float4 *>(pp + ct * NCW * 128),
+                           make_float4(yrun[ct][0], yrun[ct][1], yrun[ct][2], yrun[ct][3]));
+            named_sync_consumers();             // prefix stores issued; flag[0] read by all
+            if (threadIdx.x == 0) {
+                __threadfence();
+                const int prev = atomicAdd(&counters[tile], 1);
+                if (prev == touch - 1) __threadfence();
+                flag[0] = (prev == touch - 1) ? 1 : 0;
             }
+            named_sync_consumers();
+            fold_now = flag[0];
             if (fold_now) {
+                // this part arrived last after all: fold, then clear the prefix it left
                 const long long head_end = min(sch.begin(blockIdx.x + 1), tile_u0 + ks);
                 fold_tile(tile, (int)(head_end - tile_u0));
-            }
-            named_sync_epilogue();   // flag[0] is read by everyone before it is reused
-        }
-
-        // A later-segment part that turned out to arrive last folds its tile now,
-        // the prefix and every segment sum coming from the workspace.
-        if (threadIdx.x == 0) {
-            flag[0] = (nh_tile >= 0 && nh_prev == nh_touch - 1) ? 1 : 0;
-            flag[1] = nh_tile;
-            if (flag[0]) __threadfence();
-        }
-        named_sync_epilogue();
-        if (flag[0]) {
-            const int tile = flag[1];
-            const long long tile_u0 = (long long)tile * ks;
-            const int head_cta = sch.cta_of(tile_u0);
-            const long long head_end = min(sch.begin(head_cta + 1), tile_u0 + ks);
-            float4 *pp = reinterpret_cast<float4 *>(wsp_prefix + ((size_t)tile * BM + row) * NP + cbeg);
 #pragma unroll
-            for (int j = 0; j < NH / 4; ++j) {
-                const float4 v = __ldcg(pp + j);
-                yr[4 * j] = v.x, yr[4 * j + 1] = v.y, yr[4 * j + 2] = v.z, yr[4 * j + 3] = v.w;
+                for (int ct = 0; ct < NT; ++ct) clear_low(pp + ct * NCW * 128, col0 + ct * 8 < n_cols);
+                fold_now = 0;
             }
-#pragma unroll
-            for (int j = 0; j < NH / 4; ++j) __stcg(pp + j, make_float4(0.f, 0.f, 0.f, 0.f));
+        }
+        if (fold_now) {
+            const long long head_end = min(sch.begin(blockIdx.x + 1), tile_u0 + ks);
             fold_tile(tile, (int)(head_end - tile_u0));
         }
-        if (!ok && lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+        named_sync_consumers();   // flag[0] is read by everyone before it is reused
     }
 
-    // ============================ teardown ============================
-    dev::tc_fence_before();
-    __syncthreads();
-    if (warp == W_MMA) {
-        __syncwarp();
-        dev::tc_fence_after();
-        dev::tmem_dealloc(tmem, TMEM_COLS);
+    // A later-segment part that turned out to arrive last folds its tile now,
+    // the prefix and every segment sum coming from the workspace.
+    if (threadIdx.x == 0) {
+        flag[0] = (nh_tile >= 0 && nh_prev == nh_touch - 1) ? 1 : 0;
+        flag[1] = nh_tile;
+        if (flag[0]) __threadfence();
+    }
+    named_sync_consumers();
+    if (flag[0]) {
+        const int tile = flag[1];
+        const long long tile_u0 = (long long)tile * ks;
+        const int head_cta = sch.cta_of(tile_u0);
+        const long long head_end = min(sch.begin(head_cta + 1), tile_u0 + ks);
+        float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS + frag;
+#pragma unroll
+        for (int ct = 0; ct < NT; ++ct) {
+            if (col0 + ct * 8 < n_cols) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp + ct * NCW * 128));
+                yrun[ct][0] = v.x, yrun[ct][1] = v.y, yrun[ct][2] = v.z, yrun[ct][3] = v.w;
+            }
+        }
+        fold_tile(tile, (int)(head_end - tile_u0));
+#pragma unroll
+        for (int ct = 0; ct < NT; ++ct) clear_low(pp + ct * NCW * 128, col0 + ct * 8 < n_cols);
     }
 }
 
 // seg512: segment length in units of 512 k (1 for the invariant entry points)
-template <int NP, bool OUT_BF16>
-spec_status launch_np(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N, int K,
+template <int NT, bool OUT_BF16>
+spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N, int K,
                       int n_cols, int col0, void *y, int ldy, int accumulate, int seg512, void *workspace,
                       int32_t *dev_err, cudaStream_t stream) {
-    using C = Cfg<NP>;
-    auto kern = qmm_kernel<NP, OUT_BF16>;
+    using C = Cfg<NT>;
+    auto kern = qmm_kernel<NT, OUT_BF16>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return spec::cuda_status(e, "cudaFuncSetAttribute(qmm smem)");
         configured = true;
     }
-    CUtensorMap tx;
-    {
-        // the activations: rows = columns j of the product, K contiguous bf16 each
-        uint64_t dims[2] = {(uint64_t)K, (uint64_t)n_cols};
-        uint64_t strides[1] = {(uint64_t)ldx * 2};
-        uint32_t box[2] = {64, (uint32_t)NP};
-        if (!spec::encode_tiled(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, x, dims, strides, box,
-                                CU_TENSOR_MAP_SWIZZLE_128B))
-            return SPEC_ERR_CUDA;
-    }
     const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
     Sched sch;
-    sch.seg_st = seg512 * (SEG_K / KS);
+    sch.seg_st = seg512 * (SEG_K / C::KS);
     sch.ks = n_segments(K, seg512 * SEG_K);
     sch.tiles = (N + BM - 1) / BM;
     sch.U = (long long)sch.tiles * sch.ks;
@@ -593,10 +632,18 @@ spec_status launch_np(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     const size_t cnt_bytes = ((tiles * sizeof(int)) + 255) & ~size_t(255);
     int *counters = reinterpret_cast<int *>(workspace);
     float *prefix = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + cnt_bytes);
-    float *segs = prefix + tiles * BM * NP;
+    float *segs = prefix + tiles * BM * 8 * NT;
+    const uint8_t *xpk = reinterpret_cast<const uint8_t *>(segs + tiles * sch.ks * BM * 8 * NT);
+    if constexpr (C::XPACK) {
+        // this pass's activations, packed once for every CTA (into the workspace after the partial sums)
+        const long long pairs = (long long)(K / C::KS) * C::NBLK * 8 * NT;
+        cudaError_t e = spec::launch_pdl(xpack_kernel<NT>, dim3((unsigned)((pairs + 255) / 256)), dim3(256), 0, stream,
+                                         x, ldx, K, n_cols, col0, const_cast<uint8_t *>(xpk));
+        if (e != cudaSuccess) return spec::cuda_status(e, "qmm activation pack launch");
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sch.G);
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -604,20 +651,23 @@ spec_status launch_np(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tw, ts, tx, N, K, n_cols, col0, y, ldy, accumulate, sch, prefix,
-                                       segs, counters, dev_err);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, sch, prefix,
+                                       segs, counters, xpk, dev_err);
     return spec::cuda_status(e, "qmm launch");
 }
 
-size_t ws_bytes_for(int N, int K, int np, int seg512) {
+int pass_nt(int n_cols) { return n_cols <= 8 ? 1 : (n_cols <= 16 ? 2 : MAX_NT); }
+
+size_t ws_bytes_for(int N, int K, int nt, int seg512) {
     const size_t tiles = (size_t)(N + BM - 1) / BM;
     const size_t cnt = ((tiles * sizeof(int)) + 255) & ~size_t(255);
-    return cnt + tiles * (1 + (size_t)n_segments(K, seg512 * SEG_K)) * BM * np * sizeof(float);
+    // the 80-column pass also keeps its packed activations: K / 256 stages of XC_BYTES
+    const size_t packed = nt >= MAX_NT ? (size_t)(K / Cfg<MAX_NT>::KS) * Cfg<MAX_NT>::XC_BYTES : 0;
+    return cnt + tiles * (1 + (size_t)n_segments(K, seg512 * SEG_K)) * BM * 8 * nt * sizeof(float) + packed;
 }
 
-// np_force: 0 = pick each pass's width from the columns left, else that width for every pass
 spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
-                    void *y, spec_dtype y_dt, int ldy, int accumulate, int seg512, int np_force, void *workspace,
+                    void *y, spec_dtype y_dt, int ldy, int accumulate, int seg512, int nt, void *workspace,
                     int32_t *dev_err, cudaStream_t stream) {
     CUtensorMap tw, ts;
     {
@@ -631,35 +681,28 @@ spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const u
     {
         uint64_t dims[2] = {(uint64_t)K / 32, (uint64_t)N};
         uint64_t strides[1] = {(uint64_t)K / 32 * 2};
-        uint32_t box[2] = {(uint32_t)NBLK, BM};
+        uint32_t box[2] = {(uint32_t)stage_blocks(nt), BM};
         if (!spec::encode_tiled(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, ws, dims, strides, box,
                                 CU_TENSOR_MAP_SWIZZLE_NONE))
             return SPEC_ERR_CUDA;
     }
     const bool bf = (y_dt == SPEC_BF16);
-    // passes run back to back on the stream
-    for (int col0 = 0; col0 < n_cols;) {
-        const int np = np_force ? np_force : pass_np(n_cols - col0);
+    // one pass per group of 8 nt columns; passes run back to back on the stream
+    for (int col0 = 0; col0 < n_cols; col0 += 8 * nt) {
         spec_status st;
-#define SPEC_QMM_CASE(NPV)                                                                                         \
-    st = bf ? launch_np<NPV, true>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err, stream) \
-            : launch_np<NPV, false>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace, dev_err, \
+#define SPEC_QMM_CASE(NTV)                                                                                         \
+    st = bf ? launch_nt<NTV, true>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err, stream) \
+            : launch_nt<NTV, false>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace, dev_err, \
                                     stream)
-        if (np == 16) {
-            SPEC_QMM_CASE(16);
-        } else {
-            SPEC_QMM_CASE(MAX_NP);
+        switch (nt) {
+        case 1: SPEC_QMM_CASE(1); break;
+        case 2: SPEC_QMM_CASE(2); break;
+        default: SPEC_QMM_CASE(MAX_NT);
         }
 #undef SPEC_QMM_CASE
         if (st != SPEC_OK) return st;
-        col0 += np;
     }
     return SPEC_OK;
-}
-
-// workspace bytes for any pass of a call with n_cols columns (the widest pass it may run)
-size_t ws_bytes_call(int N, int K, int n_cols, int seg512) {
-    return ws_bytes_for(N, K, pass_np(n_cols), seg512);
 }
 
 spec_status check_args(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
@@ -673,6 +716,8 @@ spec_status check_args(const uint8_t *wq, const uint16_t *ws, int N, int K, cons
     SPEC_CHECK_ARG(spec::aligned16(wq) && spec::aligned16(ws) && spec::aligned16(x),
                    "qmatmul: wq, ws and x must be 16-byte aligned");
     SPEC_CHECK_ARG((long long)N * (K / 2) < (1ll << 40), "qmatmul: matrix too large");
+    SPEC_CHECK_ARG((size_t)(N + BM - 1) / BM * sizeof(int) <= CNT_LIMIT, "qmatmul: N must be <= %d (N=%d)",
+                   (int)(CNT_LIMIT / sizeof(int)) * BM, N);
     return SPEC_OK;
 }
 
@@ -688,7 +733,7 @@ spec_status check_ws(const void *workspace, size_t ws_bytes, size_t need) {
 extern "C" size_t spec_qmatmul_workspace(int N, int K, int n_cols) {
     if (N <= 0 || K < 256 || n_cols <= 0) return 0;
     // the largest layout either entry point may use for this shape (one-stage segments)
-    return ws_bytes_call(N, K, n_cols, 1);
+    return ws_bytes_for(N, K, pass_nt(n_cols), 1);
 }
 
 extern "C" spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,
@@ -699,9 +744,10 @@ extern "C" spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N
     SPEC_CHECK_ARG(y_dt == SPEC_F32 || y_dt == SPEC_BF16, "qmatmul: y_dt must be SPEC_F32 or SPEC_BF16");
     SPEC_CHECK_ARG(!(accumulate && y_dt != SPEC_F32), "qmatmul: accumulate needs SPEC_F32 output");
     if (n_cols == 0) return SPEC_OK;
-    st = check_ws(workspace, ws_bytes, ws_bytes_call(N, K, n_cols, 1));
+    const int nt = pass_nt(n_cols);
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
     if (st != SPEC_OK) return st;
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, 0, workspace, dev_err,
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, nt, workspace, dev_err,
                    (cudaStream_t)stream);
 }
 
@@ -723,24 +769,25 @@ extern "C" spec_status spec_qmatmul_noninvariant(const uint8_t *wq, const uint16
     }
     SPEC_CHECK_ARG(seg >= 1, "qmatmul_noninvariant: seg_stages must be >= 0");
     if (seg > nst) seg = nst;
-    st = check_ws(workspace, ws_bytes, ws_bytes_call(N, K, n_cols, seg));
+    const int nt = pass_nt(n_cols);
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, seg));
     if (st != SPEC_OK) return st;
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, seg, 0, workspace, nullptr,
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, seg, nt, workspace, nullptr,
                    (cudaStream_t)stream);
 }
 
-// Test hook: run the invariant kernel with an explicit pass width so the tests
-// can show the per-column result does not depend on it.
+// Test hook: run the invariant kernel with an explicit column-tile width so the
+// tests can show the per-column result does not depend on it.
 extern "C" spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,
                                              int n_cols, int ldx, float *y, int ldy, int nt, void *workspace,
                                              size_t ws_bytes, spec_stream_t stream) {
     spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
     if (st != SPEC_OK) return st;
-    SPEC_CHECK_ARG(nt == 2 || nt == MAX_NP / 8, "nt must be 2 (16 columns per pass) or 10 (80)");
+    SPEC_CHECK_ARG(nt == 1 || nt == 2 || nt == MAX_NT, "nt must be 1, 2 or 10");
     if (n_cols == 0) return SPEC_OK;
-    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, 8 * nt, 1));
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
     if (st != SPEC_OK) return st;
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, 1, 8 * nt, workspace, nullptr,
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, 1, nt, workspace, nullptr,
                    (cudaStream_t)stream);
 }
 
@@ -750,7 +797,7 @@ extern "C" spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // 16 MiB per device
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
 constexpr int kMaxDevices = 64;
 
 // One scratch area per device (module-scope __device__ storage is per device).
@@ -790,7 +837,8 @@ extern "C" spec_status spec_qmatmul_static_scratch(const uint8_t *wq, const uint
     SPEC_CHECK_ARG(y_dt == SPEC_F32 || y_dt == SPEC_BF16, "qmatmul: y_dt must be SPEC_F32 or SPEC_BF16");
     SPEC_CHECK_ARG(!(accumulate && y_dt != SPEC_F32), "qmatmul: accumulate needs SPEC_F32 output");
     if (n_cols == 0) return SPEC_OK;
-    const size_t need = ws_bytes_call(N, K, n_cols, 1);
+    const int nt = pass_nt(n_cols);
+    const size_t need = ws_bytes_for(N, K, nt, 1);
     if (need > kStaticScratchBytes)
         return spec::fail(SPEC_ERR_WORKSPACE,
                           "qmatmul_static_scratch: N=%d K=%d n_cols=%d needs %zu bytes of scratch, more than the "
@@ -803,6 +851,6 @@ extern "C" spec_status spec_qmatmul_static_scratch(const uint8_t *wq, const uint
     const size_t tiles = (size_t)(N + BM - 1) / BM;
     cudaError_t e = cudaMemsetAsync(scratch, 0, tiles * sizeof(int), (cudaStream_t)stream);
     if (e != cudaSuccess) return spec::cuda_status(e, "cudaMemsetAsync(qmatmul scratch counters)");
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, 0, scratch, dev_err,
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, nt, scratch, dev_err,
                    (cudaStream_t)stream);
 }

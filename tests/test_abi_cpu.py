@@ -40,6 +40,7 @@ FAKE = 1 << 20  # a 16-byte aligned non-NULL pointer value; never dereferenced b
     (dict(ldx=500), "ldx"),
     (dict(x=FAKE + 4), "16-byte aligned"),
     (dict(y_dt=1), "y_dt"),
+    (dict(N=2097152 + 1, ldy=2097152 + 1), "N must be <= 2097152"),
 ])
 def test_qmatmul_host_validation(kw, msg):
     import invariant_speculative_verification_gb300 as L
