@@ -93,11 +93,15 @@ const char *spec_last_error(void);
  *   y    [n_cols][ldy] of y_dt (SPEC_F32 or SPEC_BF16), ldy >= N.
  *        accumulate != 0 adds into y (SPEC_F32 only): y = fp32(y + result).
  *   workspace  at least spec_qmatmul_workspace(N, K, n_cols) bytes, 16-byte
- *        aligned, zero-filled before its first use (cudaMemset once).  Every
- *        call that returns SPEC_OK and reports no SPEC_DEVERR_TIMEOUT leaves it
- *        zero-filled again, so one workspace serves any sequence of calls on
- *        one stream; calls that overlap on the GPU need separate workspaces.
- *   K % 256 == 0, N >= 1, n_cols >= 0 (0 launches nothing).
+ *        aligned, zero-filled before its first use (cudaMemset once).  A call
+ *        keeps one arrival counter per 128 rows in the first 4 ceil(N/128)
+ *        bytes; every call that returns SPEC_OK and reports no
+ *        SPEC_DEVERR_TIMEOUT leaves the first 64 KB zero again (counters reset,
+ *        consumed partial sums cleared), so one workspace serves any sequence
+ *        of calls of any shapes on one stream; calls that overlap on the GPU
+ *        need separate workspaces.
+ *   K % 256 == 0, 1 <= N <= 2097152 (counters fit in 64 KB), n_cols >= 0
+ *   (0 launches nothing).
  *   The kernel is launched with programmatic dependent launch: it may start
  *   reading wq and ws while the preceding kernel on the stream is still
  *   running (weights are treated as constant inputs); x, y and the workspace

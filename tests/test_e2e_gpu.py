@@ -38,11 +38,15 @@ def test_speculative_equals_width1_small_decoder(use_graph):
     assert s4 < s1
 
 
-def test_layers_and_logits_match_oracle():
+@pytest.mark.parametrize("cfg,P,layers", [(SMALL, 20, None), (synth.E2E_DECODER, 16, 2)],
+                         ids=["small", "full_size_2_layers"])
+def test_layers_and_logits_match_oracle(cfg, P, layers):
+    """Each layer's update and the logits vs the oracle, the layer fed the GPU's own
+    input.  At full size the int4 matmuls split tiles across CTAs and calls of 24 to
+    250 tiles share one workspace, in the decoder's own call order."""
     from invariant_speculative_verification_gb300.decoder import Decoder
-    w = synth.decoder_weights(2024, SMALL)
-    P = 20
-    toks = synth.prompts(2025, 1, P, SMALL.vocab)[0]
+    w = synth.decoder_weights(2024, cfg)
+    toks = synth.prompts(2025, 1, P, cfg.vocab)[0]
     dec = Decoder(w, 1, 64, max_rows=P)
     od = oracle.Decoder(w, 1, 64)
     d = "cuda"
@@ -51,7 +55,7 @@ def test_layers_and_logits_match_oracle():
     ctx = torch.zeros(1, dtype=torch.int32, device=d)
     dec.embed(t, P)
     assert np.array_equal(host(dec.h[:P]), od.embed(toks))
-    for li in range(SMALL.layers):
+    for li in range(layers or cfg.layers):
         h_in = host(dec.h[:P]).copy()
         for c_gpu, c_or in ((dec.k_cache[li], od.k_cache[li]), (dec.v_cache[li], od.v_cache[li])):
             c_or[...] = host(c_gpu, np.uint16)
