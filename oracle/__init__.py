@@ -51,6 +51,8 @@ def lib():
             c = _lib
             vp, i32, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
             c.oracle_qmatmul.argtypes = [vp, vp, i32, i32, vp, i32, i32, vp]
+            c.oracle_qmatmul_sb.argtypes = [vp, vp, i32, i32, vp, i32, i32, vp]
+            c.oracle_sb_record.argtypes = [vp, vp, vp]
             c.oracle_attention.argtypes = [vp, i32, i32, i32, i32, dbl, vp, vp, vp, i32, vp, vp, i32, vp, vp]
             c.oracle_verify_greedy.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp]
             c.oracle_verify_greedy.restype = i32
@@ -107,6 +109,43 @@ def qmatmul(wq, ws, x, N: int, K: int, n_cols: int | None = None, ldx: int | Non
     y = np.zeros((n_cols, N), dtype=np.float64)
     lib().oracle_qmatmul(_p(wq), _p(ws), N, K, _p(x), n_cols, ldx, _p(y))
     return y
+
+
+def sb_pitch(K: int) -> int:
+    """Bytes of super-block scale records per weight row: ceil(K/512) pairs of 8-byte records."""
+    return (K + 511) // 512 * 16
+
+
+def sb_record(rec) -> tuple[list[int], float]:
+    """Decode one 8-byte super-block record into its eight 6-bit block scales and its fp16 super-scale."""
+    rec = _c(np.frombuffer(bytes(rec), dtype=np.uint8), np.uint8)
+    assert rec.size == 8
+    s = np.zeros(8, dtype=np.int32)
+    D = np.zeros(1, dtype=np.float64)
+    lib().oracle_sb_record(_p(rec), _p(s), _p(D))
+    return [int(v) for v in s], float(D[0])
+
+
+def qmatmul_sb(wq, sbr, x, N: int, K: int, n_cols: int | None = None, ldx: int | None = None) -> np.ndarray:
+    """y[j][n] = sum_k x[j][k] D[n][k/256] s[n][k/32] q[n][k] (two-level scales); float64 [n_cols][N]."""
+    wq = _c(wq, np.uint8)
+    sbr = _c(sbr, np.uint8)
+    x = _c(x, np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    n_cols = x.shape[0] if n_cols is None else n_cols
+    ldx = x.shape[1] if ldx is None else ldx
+    y = np.zeros((n_cols, N), dtype=np.float64)
+    lib().oracle_qmatmul_sb(_p(wq), _p(sbr), N, K, _p(x), n_cols, ldx, _p(y))
+    return y
+
+
+def qmatmul_sb_rows(wq, sbr, x, K: int, rows) -> np.ndarray:
+    """qmatmul_sb restricted to output features ``rows``."""
+    rows = np.asarray(rows, dtype=np.int64)
+    wq_s = _c(np.asarray(wq).reshape(-1, K // 2)[rows], np.uint8)
+    sb_s = _c(np.asarray(sbr).reshape(-1, sb_pitch(K))[rows], np.uint8)
+    return qmatmul_sb(wq_s, sb_s, x, len(rows), K)
 
 
 def qmatmul_rows(wq, ws, x, K: int, rows) -> np.ndarray:

@@ -124,6 +124,56 @@ void oracle_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
 }
 
 /* ---------------------------------------------------------------------------
+ * 1b. the same product with two-level (super-block) scales
+ *
+ * [T] "Why the math checks out and the text still flips" names Q4_K / Q6_K
+ * (llama.cpp K-quants, scales in two levels) and [R] "Quantized Matrix
+ * Multiplication Shows the Same Class of Failure" names IQ3_S / IQ4_XS; the
+ * pages define none of them, so this format is self-defined in their spirit:
+ * the same 4-bit codes, and per row and per 256-k super-block one 8-byte record
+ * (read as a little-endian 64-bit word):
+ *
+ *   bits 6j .. 6j+5   s_j in 0 .. 63, the scale of 32-k block j of the super-block
+ *   bits 48 .. 63     D, an fp16 super-scale
+ *
+ * Block b's scale is D * s_(b mod 8).  A row holds ceil(K/512) pairs of records
+ * (16 bytes each; when K/256 is odd the last record is padding):
+ *
+ *   y[j][n] = sum_k x[j][k] * D[n][k/256] * s[n][k/32] * (nibble(n, k) - 8)
+ * ------------------------------------------------------------------------- */
+void oracle_sb_record(const uint8_t *rec, int32_t *s, double *D)
+{
+    uint64_t w = 0;
+    for (int i = 7; i >= 0; --i) w = (w << 8) | rec[i];   /* little-endian */
+    for (int j = 0; j < 8; ++j) s[j] = (int32_t)((w >> (6 * j)) & 63u);
+    *D = or_f16_to_double((uint16_t)(w >> 48));
+}
+
+void oracle_qmatmul_sb(const uint8_t *wq, const uint8_t *sbr, int N, int K,
+                       const uint16_t *x, int n_cols, int ldx, double *y)
+{
+    const int pitch = (K + 511) / 512 * 16;   /* bytes of records per row */
+    for (int j = 0; j < n_cols; ++j) {
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int sb = 0; sb < K / 256; ++sb) {
+                int32_t s[8];
+                double D;
+                oracle_sb_record(sbr + (size_t)n * pitch + 8 * sb, s, &D);
+                for (int k = 256 * sb; k < 256 * sb + 256; ++k) {
+                    uint8_t byte = wq[(size_t)n * (K / 2) + k / 2];
+                    int nib = (k % 2 == 0) ? (byte & 0x0f) : (byte >> 4);
+                    double d = D * (double)s[(k / 32) % 8];
+                    double xv = or_bf16_to_double(x[(size_t)j * ldx + k]);
+                    acc += xv * d * (double)(nib - 8);   /* exact in double */
+                }
+            }
+            y[(size_t)j * N + n] = acc;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------
  * 2. causal softmax attention over a paged KV cache
  *
  * [R] "Flash Attention Changes Geometry With Batch Width": attention for the

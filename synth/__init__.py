@@ -127,6 +127,51 @@ def activations_bf16(seed: int, n_cols: int, K: int, ldx: int | None = None, std
     return f32_to_bf16_bits(x)
 
 
+def pack_sb_records(s, D16) -> np.ndarray:
+    """Pack 6-bit block scales s ([N][K/32], 0..63) and fp16 super-scales D16 (uint16 bits,
+    [N][K/256]) into the super-block record layout: per row ceil(K/512) pairs of 8-byte
+    little-endian words, s_j at bits 6j, D at bits 48..63, the unused last record zero."""
+    s = np.asarray(s, dtype=np.uint64)
+    D16 = np.asarray(D16, dtype=np.uint16)
+    N, nb = s.shape
+    nsb = nb // 8
+    assert D16.shape == (N, nsb) and s.max(initial=0) <= 63
+    words = np.zeros((N, (nsb + 1) // 2 * 2), dtype=np.uint64)
+    sj = s.reshape(N, nsb, 8)
+    for j in range(8):
+        words[:, :nsb] |= sj[:, :, j] << np.uint64(6 * j)
+    words[:, :nsb] |= D16.astype(np.uint64) << np.uint64(48)
+    return np.ascontiguousarray(words.astype("<u8").view(np.uint8))
+
+
+def quantize_q4_superblock(w) -> tuple[np.ndarray, np.ndarray]:
+    """Encode float32 [N][K] (K % 256 == 0) as 4-bit codes with two-level scales: per 256-k
+    super-block an fp16 D = max block scale / 63, per 32-k block s = round(block scale / D)."""
+    w = np.asarray(w, dtype=np.float32)
+    N, K = w.shape
+    assert K % 256 == 0
+    blocks = w.reshape(N, K // 32, 32)
+    want = np.abs(blocks).max(axis=2) / np.float32(7.0)               # ideal block scales
+    D16 = (want.reshape(N, K // 256, 8).max(axis=2) / np.float32(63.0)).astype(np.float16)
+    D = np.repeat(D16.astype(np.float32), 8, axis=1)
+    s = np.where(D > 0, np.clip(np.rint(want / np.where(D > 0, D, 1)), 0, 63), 0).astype(np.int64)
+    d = D * s
+    safe = np.where(d == 0, np.float32(1.0), d)
+    q = np.clip(np.rint(blocks / safe[:, :, None]), -8, 7)
+    q[d == 0] = 0
+    nib = (q.astype(np.int32) + 8).astype(np.uint8).reshape(N, K)
+    wq = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    return np.ascontiguousarray(wq), pack_sb_records(s, D16.view(np.uint16))
+
+
+def qmatmul_sb_case(seed: int, N: int, K: int, n_cols: int, ldx: int | None = None) -> QMatmulCase:
+    """A QMatmulCase whose ``ws`` holds super-block scale records (uint8 [N][ceil(K/512)*16])."""
+    g = rng(seed)
+    wq, sbr = quantize_q4_superblock(g.normal(0.0, 0.02, size=(N, K)).astype(np.float32))
+    x = activations_bf16(seed + 7919, n_cols, K, ldx)
+    return QMatmulCase(N, K, wq, sbr, x, n_cols, x.shape[1])
+
+
 def qmatmul_case(seed: int, N: int, K: int, n_cols: int, ldx: int | None = None) -> QMatmulCase:
     wq, ws = qmatmul_weights(seed, N, K)
     x = activations_bf16(seed + 7919, n_cols, K, ldx)
