@@ -249,6 +249,44 @@ def qgemv_sweep(torch, L, hbm_peak):
     return out, inv_cases, inv_pass
 
 
+def qgemv_superblock(torch, L, hbm_peak):
+    """The same GEMV with two-level scales (spec_qmatmul_sb) on 17408 x 5120 at widths 1 and 8
+    (weight copies rotated over >= 4x L2), and width-8 == 8 width-1 calls bit for bit."""
+    dev = torch.device("cuda")
+    N, K = 17408, 5120
+    case = synth.qmatmul_sb_case(21, N, K, 8)
+    wbytes = case.wq.nbytes + case.ws.nbytes
+    copies = max(2, math.ceil(4 * 128e6 / wbytes))
+    wq = [torch.from_numpy(case.wq).to(dev)]
+    sb = [torch.from_numpy(case.ws).to(dev)]
+    for _ in range(copies - 1):
+        wq.append(wq[0].clone())
+        sb.append(sb[0].clone())
+    x = torch.from_numpy(case.x.view(np.int16)).to(dev)
+    y = torch.zeros((8, N), dtype=torch.float32, device=dev)
+    wsb = L.spec_qmatmul_workspace(N, K, 8)
+    wsp = torch.zeros(wsb // 4 + 64, dtype=torch.int32, device=dev)
+    out = {"shape": f"{N}x{K}", "scale_bytes_per_row": int(case.ws.shape[1]),
+           "algorithmic_bytes": "N (K/2 + ceil(K/512) 16) + 2 n K + 4 n N"}
+    for n in (1, 8):
+        def body(_n=n):
+            for i in range(copies):
+                L.spec_qmatmul_sb(wq[i], sb[i], N, K, x, _n, K, y, L.SPEC_F32, N, 0, wsp, wsb, None)
+        t = graph_time(torch, body, copies)
+        algo = N * (K / 2 + case.ws.shape[1]) + 2 * n * K + 4 * n * N
+        out[str(n)] = {"us": round(t * 1e6, 2), "GBps": round(algo / t / 1e9, 1),
+                       "frac": round(algo / t / 1e9 / hbm_peak, 3)}
+    singles = torch.zeros((8, N), dtype=torch.float32, device=dev)
+    for j in range(8):
+        L.spec_qmatmul_sb(wq[0], sb[0], N, K, x[j:j + 1], 1, K, singles[j:j + 1], L.SPEC_F32, N, 0, wsp, wsb, None)
+    L.spec_qmatmul_sb(wq[0], sb[0], N, K, x, 8, K, y, L.SPEC_F32, N, 0, wsp, wsb, None)
+    torch.cuda.synchronize()
+    out["width8_equals_width1_calls"] = bool(torch.equal(y.view(torch.int32), singles.view(torch.int32)))
+    del wq, sb
+    torch.cuda.empty_cache()
+    return out
+
+
 def attention_invariance(torch, L):
     """Width-n verify rows vs width-1 evaluation at each position (40/8 heads of 128, bf16)."""
     dev = torch.device("cuda")
@@ -560,6 +598,7 @@ def run_ours(args):
     # ---- GEMV sweep + invariance ----
     sweep, qc, qp = qgemv_sweep(torch, L, hbm_peak)
     kernels = kernel_rooflines(torch, L, hbm_peak)
+    kernels["qgemv_superblock"] = qgemv_superblock(torch, L, hbm_peak)
     ac, ap = attention_invariance(torch, L)
     inv_cases = qc + ac + N_SEQ
     inv_pass = qp + ap + equal_seqs

@@ -120,6 +120,30 @@ spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
                          void *workspace, size_t ws_bytes,
                          int32_t *dev_err, spec_stream_t stream);
 
+/* The same product with two-level (super-block) scales.  The pages name
+ * two-level formats -- tokenstrom.com, "'Lossless,' but not quite", section
+ * "Why the math checks out and the text still flips" (Q4_K / Q6_K); ramgpt.org,
+ * "When Lossless Speculation Stops Being Lossless on Blackwell", section
+ * "Quantized Matrix Multiplication Shows the Same Class of Failure" (IQ3_S /
+ * IQ4_XS) -- but define none, so this one is the library's own:
+ *
+ *   y[j][n] (+)= sum_k x[j][k] * D[n][k/256] * s[n][k/32] * (nib(n, k) - 8)
+ *
+ *   wq   as for spec_qmatmul.
+ *   sbr  uint8 [N][ceil(K/512) * 16], 16-byte aligned: per row and per 256-k
+ *        super-block one 8-byte record, read as a little-endian 64-bit word:
+ *        bits 6j .. 6j+5 = s_j in 0 .. 63, the scale of the super-block's
+ *        32-k block j; bits 48 .. 63 = D, an fp16 super-scale.  When K/256 is
+ *        odd each row's last record is padding (ignored).
+ * Block b's scale is D * s_(b mod 8) formed exactly in fp32; every other
+ * argument, the workspace (spec_qmatmul_workspace), the arithmetic and the
+ * batch invariance are those of spec_qmatmul. */
+spec_status spec_qmatmul_sb(const uint8_t *wq, const uint8_t *sbr, int N, int K,
+                            const uint16_t *x, int n_cols, int ldx,
+                            void *y, spec_dtype y_dt, int ldy, int accumulate,
+                            void *workspace, size_t ws_bytes,
+                            int32_t *dev_err, spec_stream_t stream);
+
 /* The same product with a K-segment length of seg_stages x 512 chosen per
  * call (seg_stages = 0: picked from the problem size and the GPU for speed),
  * so its reduction order depends on the call: NOT batch invariant.  It exists

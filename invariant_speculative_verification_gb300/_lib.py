@@ -33,6 +33,7 @@ _SIGS = {
     "spec_last_error": (ctypes.c_char_p, []),
     "spec_qmatmul_workspace": (_sz, [_i32, _i32, _i32]),
     "spec_qmatmul": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
+    "spec_qmatmul_sb": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "spec_qmatmul_noninvariant": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _sz, _vp]),
     "spec_qmatmul_debug_nt": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _sz, _vp]),
     "spec_qmatmul_static_scratch": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _vp]),
@@ -64,14 +65,14 @@ def library_path() -> str:
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
-    """Load libspec.so (building it first when it is absent and nvcc is present)."""
+    """Load libspec.so (building it first when it is absent or older than its sources)."""
     global _lib
     if _lib is not None:
         return _lib
     path = _build.LIB
-    if not os.path.exists(path):
+    if _build.is_stale():
         if not build_if_missing:
-            raise ImportError(f"libspec.so is not built ({path}); run __graft_entry__.build()")
+            raise ImportError(f"libspec.so is not built or is out of date ({path}); run __graft_entry__.build()")
         _build.build()
     lib = ctypes.CDLL(path)
     for name, (res, args) in _SIGS.items():
@@ -127,6 +128,13 @@ def spec_qmatmul(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, workspa
     _check("spec_qmatmul", load().spec_qmatmul(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx, _ptr(y), y_dt, ldy,
                                                int(accumulate), _ptr(workspace), int(ws_bytes), _ptr(dev_err),
                                                _stream(stream)))
+
+
+def spec_qmatmul_sb(wq, sbr, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, workspace, ws_bytes, dev_err=None,
+                    stream=None):
+    _check("spec_qmatmul_sb", load().spec_qmatmul_sb(_ptr(wq), _ptr(sbr), N, K, _ptr(x), n_cols, ldx, _ptr(y), y_dt,
+                                                     ldy, int(accumulate), _ptr(workspace), int(ws_bytes),
+                                                     _ptr(dev_err), _stream(stream)))
 
 
 def spec_qmatmul_noninvariant(wq, ws, N, K, x, n_cols, ldx, y, ldy, seg_stages, workspace, ws_bytes, stream=None):

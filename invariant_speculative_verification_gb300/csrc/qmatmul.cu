@@ -68,7 +68,13 @@ constexpr size_t CNT_LIMIT = 64 * 1024;
 // once per call by a small kernel (xpack_kernel) into the workspace, in the
 // very byte layout of a stage, and each stage's part is copied in by TMA.
 // The stage size only changes how a segment is delivered, never its arithmetic.
-template <int NT>
+// Scale formats: SC_BLOCK = one fp16 scale per 32-k block ([N][K/32]);
+// SC_SUPER = per 256-k super-block an 8-byte record of eight 6-bit block scales
+// and an fp16 super-scale, records in 16-byte pairs per row ([N][ceil(K/512) 16]
+// bytes); block b's scale is D * s_(b mod 8), formed exactly in fp32.
+constexpr int SC_BLOCK = 0, SC_SUPER = 1;
+
+template <int NT, int FMT = SC_BLOCK>
 struct Cfg {
     static constexpr int KS = NT >= 10 ? 256 : 512;         // k per stage
     static constexpr int NBLK = KS / 32;                    // 32-k blocks per stage
@@ -77,7 +83,8 @@ struct Cfg {
     static constexpr int NXW = XPACK ? 0 : 2;               // activation warps
     static constexpr int THREADS = (NCW + 1 + NXW) * 32;    // + TMA warp
     static constexpr int W_BYTES = NWBOX * W_BOX;
-    static constexpr int S_BYTES = BM * NBLK * 2;
+    // scales of a stage: fp16 per block, or the row's 16-byte record pair holding the stage
+    static constexpr int S_BYTES = FMT == SC_BLOCK ? BM * NBLK * 2 : BM * 16;
     static constexpr int X_BOX = 8 * NT * 128;              // 64 k of the pass's activation columns
     static constexpr int X_BYTES = (NBLK / 2) * X_BOX;
     static constexpr int CI_BYTES = NBLK * 8 * NT * 4;      // [blocks][8 NT slots] fp32
@@ -113,6 +120,14 @@ __device__ __forceinline__ void codes_to_bf16(uint32_t w, uint32_t (&o)[4]) {
     o[1] = dev::lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);
     o[2] = dev::lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);
     o[3] = dev::lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);
+}
+
+// Block j's scale from a super-block record (little-endian: s_j = bits 6j..6j+5,
+// fp16 D = bits 48..63): D * s_j, exact in fp32 (11 + 6 significant bits).
+__device__ __forceinline__ float super_scale(const uint2 &rec, int j) {
+    const uint64_t w = ((uint64_t)rec.y << 32) | rec.x;
+    const float D = __half2float(__ushort_as_half((unsigned short)(rec.y >> 16)));
+    return D * (float)(uint32_t)((w >> (6 * j)) & 63u);
 }
 
 // The activations of one (32-k block, column) pair of a stage: four 16-byte
@@ -180,13 +195,13 @@ __device__ __forceinline__ void named_sync_consumers() {
     asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
 }
 
-template <int NT, bool OUT_BF16>
-__global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
+template <int NT, bool OUT_BF16, int FMT>
+__global__ void __launch_bounds__(Cfg<NT, FMT>::THREADS, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ts,
            const uint16_t *__restrict__ x, int ldx, int N, int K, int n_cols, int col0, void *__restrict__ y, int ldy,
            int accumulate, Sched sch, float *__restrict__ wsp_prefix, float *__restrict__ wsp_seg,
            int *__restrict__ counters, const uint8_t *__restrict__ xpk, int32_t *dev_err) {
-    using C = Cfg<NT>;
+    using C = Cfg<NT, FMT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NS * C::STAGE);
@@ -257,7 +272,10 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
 #pragma unroll
                 for (int b = 0; b < C::NWBOX; ++b)
                     dev::tma_load_2d(base + b * W_BOX, &tw, k0 / 2 + 128 * b, tile * BM, &full[s]);
-                dev::tma_load_2d(base + C::S_OFF, &ts, k0 / 32, tile * BM, &full[s]);
+                if constexpr (FMT == SC_BLOCK)
+                    dev::tma_load_2d(base + C::S_OFF, &ts, k0 / 32, tile * BM, &full[s]);
+                else   // the 16-byte record pair holding this stage's super-block(s)
+                    dev::tma_load_2d(base + C::S_OFF, &ts, (k0 / 512) * 16, tile * BM, &full[s]);
                 if (C::XPACK) {
                     if (issued < C::NS)
                         k0s[issued] = k0;
@@ -456,6 +474,16 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                 const uint32_t xbase = wbase + C::X_OFF;
                 const uint32_t sbase = wbase + C::S_OFF;
                 const uint32_t cbase = wbase + C::CI_OFF;
+                // super-block scales: rows r and r+8's record pair of this stage (a 512-k stage
+                // uses both records, a 256-k stage the one its k offset selects)
+                uint2 rec_r[2] = {}, rec_r8[2] = {};
+                int rsel = 0;
+                if constexpr (FMT == SC_SUPER) {
+                    const uint2 *pr = reinterpret_cast<const uint2 *>(smem + s * C::STAGE + C::S_OFF + (wrow + r) * 16);
+                    const uint2 *pr8 = pr + 16;   // 8 rows further on
+                    rec_r[0] = pr[0], rec_r[1] = pr[1], rec_r8[0] = pr8[0], rec_r8[1] = pr8[1];
+                    rsel = ((((int)(u % ks) * seg_st + st) * C::KS) >> 8) & 1;
+                }
                 constexpr int BP_UNROLL = NT > 4 ? 1 : C::NBLK / 2;
 #pragma unroll BP_UNROLL
                 for (int bp = 0; bp < C::NBLK / 2; ++bp) {
@@ -468,19 +496,28 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                         dev::ldmatrix_x4(wv[0], wv[1], wv[2], wv[3],
                                          wbase + (blk >> 3) * W_BOX + row * 128 + (((blk & 7) ^ (row & 7)) << 4));
                     }
-                    uint32_t s2, s28;   // the two fp16 scales of blocks 2bp, 2bp+1 for rows r and r+8
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2) : "r"(sbase + (wrow + r) * (2 * C::NBLK) + bp * 4));
-                    asm volatile("ld.shared.u32 %0, [%1];"
-                                 : "=r"(s28)
-                                 : "r"(sbase + (wrow + r + 8) * (2 * C::NBLK) + bp * 4));
+                    uint32_t s2 = 0, s28 = 0;   // the two fp16 scales of blocks 2bp, 2bp+1 for rows r and r+8
+                    if constexpr (FMT == SC_BLOCK) {
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2) : "r"(sbase + (wrow + r) * (2 * C::NBLK) + bp * 4));
+                        asm volatile("ld.shared.u32 %0, [%1];"
+                                     : "=r"(s28)
+                                     : "r"(sbase + (wrow + r + 8) * (2 * C::NBLK) + bp * 4));
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int blk = 2 * bp + h;
                         uint32_t ar[4], ar8[4];
                         codes_to_bf16(wv[2 * h], ar);
                         codes_to_bf16(wv[2 * h + 1], ar8);
-                        const float d_r = __half2float(__ushort_as_half((unsigned short)(s2 >> (16 * h))));
-                        const float d_r8 = __half2float(__ushort_as_half((unsigned short)(s28 >> (16 * h))));
+                        float d_r, d_r8;
+                        if constexpr (FMT == SC_BLOCK) {
+                            d_r = __half2float(__ushort_as_half((unsigned short)(s2 >> (16 * h))));
+                            d_r8 = __half2float(__ushort_as_half((unsigned short)(s28 >> (16 * h))));
+                        } else {
+                            const int pi = C::KS == 512 ? (bp >> 2) : rsel;
+                            d_r = super_scale(pi ? rec_r[1] : rec_r[0], blk & 7);
+                            d_r8 = super_scale(pi ? rec_r8[1] : rec_r8[0], blk & 7);
+                        }
 #pragma unroll
                         for (int ct = 0; ct < NT; ++ct) {
                             const int xrow = ct * 8 + xcol;
@@ -609,12 +646,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
 }
 
 // seg512: segment length in units of 512 k (1 for the invariant entry points)
-template <int NT, bool OUT_BF16>
+template <int NT, bool OUT_BF16, int FMT>
 spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N, int K,
                       int n_cols, int col0, void *y, int ldy, int accumulate, int seg512, void *workspace,
                       int32_t *dev_err, cudaStream_t stream) {
-    using C = Cfg<NT>;
-    auto kern = qmm_kernel<NT, OUT_BF16>;
+    using C = Cfg<NT, FMT>;
+    auto kern = qmm_kernel<NT, OUT_BF16, FMT>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -666,9 +703,12 @@ size_t ws_bytes_for(int N, int K, int nt, int seg512) {
     return cnt + tiles * (1 + (size_t)n_segments(K, seg512 * SEG_K)) * BM * 8 * nt * sizeof(float) + packed;
 }
 
-spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
+// bytes of super-block scale records per weight row
+inline int super_pitch(int K) { return (K + 511) / 512 * 16; }
+
+spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
                     void *y, spec_dtype y_dt, int ldy, int accumulate, int seg512, int nt, void *workspace,
-                    int32_t *dev_err, cudaStream_t stream) {
+                    int32_t *dev_err, cudaStream_t stream, int fmt = SC_BLOCK) {
     CUtensorMap tw, ts;
     {
         uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)N};
@@ -678,11 +718,19 @@ spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const u
                                 CU_TENSOR_MAP_SWIZZLE_128B))
             return SPEC_ERR_CUDA;
     }
-    {
+    if (fmt == SC_BLOCK) {
         uint64_t dims[2] = {(uint64_t)K / 32, (uint64_t)N};
         uint64_t strides[1] = {(uint64_t)K / 32 * 2};
         uint32_t box[2] = {(uint32_t)stage_blocks(nt), BM};
         if (!spec::encode_tiled(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, ws, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_NONE))
+            return SPEC_ERR_CUDA;
+    } else {
+        // one 16-byte record pair per row and stage
+        uint64_t dims[2] = {(uint64_t)super_pitch(K), (uint64_t)N};
+        uint64_t strides[1] = {(uint64_t)super_pitch(K)};
+        uint32_t box[2] = {16, BM};
+        if (!spec::encode_tiled(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ws, dims, strides, box,
                                 CU_TENSOR_MAP_SWIZZLE_NONE))
             return SPEC_ERR_CUDA;
     }
@@ -690,22 +738,30 @@ spec_status qmm_run(const uint8_t *wq, const uint16_t *ws, int N, int K, const u
     // one pass per group of 8 nt columns; passes run back to back on the stream
     for (int col0 = 0; col0 < n_cols; col0 += 8 * nt) {
         spec_status st;
+#define SPEC_QMM_FMT(NTV, FMTV)                                                                                    \
+    st = bf ? launch_nt<NTV, true, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err,    \
+                                         stream)                                                                      \
+            : launch_nt<NTV, false, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace,    \
+                                          dev_err, stream)
 #define SPEC_QMM_CASE(NTV)                                                                                         \
-    st = bf ? launch_nt<NTV, true>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err, stream) \
-            : launch_nt<NTV, false>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace, dev_err, \
-                                    stream)
+    if (fmt == SC_BLOCK) {                                                                                         \
+        SPEC_QMM_FMT(NTV, SC_BLOCK);                                                                              \
+    } else {                                                                                                       \
+        SPEC_QMM_FMT(NTV, SC_SUPER);                                                                              \
+    }
         switch (nt) {
         case 1: SPEC_QMM_CASE(1); break;
         case 2: SPEC_QMM_CASE(2); break;
         default: SPEC_QMM_CASE(MAX_NT);
         }
 #undef SPEC_QMM_CASE
+#undef SPEC_QMM_FMT
         if (st != SPEC_OK) return st;
     }
     return SPEC_OK;
 }
 
-spec_status check_args(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
+spec_status check_args(const uint8_t *wq, const void *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
                        const void *y, int ldy) {
     SPEC_CHECK_ARG(N >= 1 && K >= 256 && n_cols >= 0, "qmatmul: need N >= 1, K >= 256, n_cols >= 0 (N=%d K=%d n_cols=%d)",
                    N, K, n_cols);
@@ -749,6 +805,21 @@ extern "C" spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N
     if (st != SPEC_OK) return st;
     return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, nt, workspace, dev_err,
                    (cudaStream_t)stream);
+}
+
+extern "C" spec_status spec_qmatmul_sb(const uint8_t *wq, const uint8_t *sbr, int N, int K, const uint16_t *x,
+                                       int n_cols, int ldx, void *y, spec_dtype y_dt, int ldy, int accumulate,
+                                       void *workspace, size_t ws_bytes, int32_t *dev_err, spec_stream_t stream) {
+    spec_status st = check_args(wq, sbr, N, K, x, n_cols, ldx, y, ldy);
+    if (st != SPEC_OK) return st;
+    SPEC_CHECK_ARG(y_dt == SPEC_F32 || y_dt == SPEC_BF16, "qmatmul_sb: y_dt must be SPEC_F32 or SPEC_BF16");
+    SPEC_CHECK_ARG(!(accumulate && y_dt != SPEC_F32), "qmatmul_sb: accumulate needs SPEC_F32 output");
+    if (n_cols == 0) return SPEC_OK;
+    const int nt = pass_nt(n_cols);
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
+    if (st != SPEC_OK) return st;
+    return qmm_run(wq, sbr, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, nt, workspace, dev_err,
+                   (cudaStream_t)stream, SC_SUPER);
 }
 
 extern "C" spec_status spec_qmatmul_noninvariant(const uint8_t *wq, const uint16_t *ws, int N, int K,
