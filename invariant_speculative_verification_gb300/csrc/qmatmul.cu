@@ -665,6 +665,9 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     sch.tiles = (N + BM - 1) / BM;
     sch.U = (long long)sch.tiles * sch.ks;
     sch.G = (int)(sch.U < sms ? sch.U : sms);
+    // Nearly one tile per SM: one whole tile per CTA costs at most 15 % more work
+    // per CTA than an even split and removes every split tile's publish and fold.
+    if (sch.ks > 1 && sch.tiles <= sms && (long long)sch.tiles * 100 >= 85ll * sms) sch.G = sch.tiles;
     const size_t tiles = (size_t)sch.tiles;
     const size_t cnt_bytes = ((tiles * sizeof(int)) + 255) & ~size_t(255);
     int *counters = reinterpret_cast<int *>(workspace);
