@@ -96,3 +96,31 @@ def test_zero_sized_calls_launch_nothing():
     import invariant_speculative_verification_gb300 as L
     L.spec_qmatmul(FAKE, FAKE, 64, 512, FAKE, 0, 512, FAKE, 0, 64, 0, None, 0, stream=0)
     L.spec_verify_greedy(FAKE, 0, 1000, FAKE, 0, 0, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, stream=0)
+
+
+def test_header_compiles_as_c_and_a_c_program_links_and_runs(tmp_path):
+    """include/spec.h is plain C: a C11 program that takes the address of every
+    declared entry point compiles, links against libspec.so and runs (the calls it
+    makes need no GPU)."""
+    import shutil
+    import subprocess
+    import invariant_speculative_verification_gb300 as L
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    names = declared_functions()
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "spec.h"\n'
+        "typedef void (*fp)(void);\n"
+        "static const fp table[] = {\n" + ",\n".join(f"    (fp){n}" for n in names) + "\n};\n"
+        "int main(void) {\n"
+        "    int n = 0;\n"
+        "    for (unsigned i = 0; i < sizeof(table) / sizeof(table[0]); ++i) n += table[i] != 0;\n"
+        '    printf("%d %s %s\\n", n, spec_status_string(SPEC_OK), spec_status_string(SPEC_ERR_WORKSPACE));\n'
+        "    return 0;\n}\n")
+    lib = L.library_path()
+    exe = tmp_path / "abi"
+    subprocess.check_call(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-o", str(exe), lib, "-Wl,-rpath," + os.path.dirname(lib)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert out == [str(len(names)), "SPEC_OK", "SPEC_ERR_WORKSPACE"]
