@@ -22,10 +22,12 @@
 // Execution: a persistent grid of one CTA per SM, each with eight consumer
 // warps (16 weight rows each, 128 rows per tile) and one TMA warp.  The
 // (128-row tile x K-segment) units are dealt out in equal contiguous ranges
-// (stream-K), so every SM streams the same number of bytes.  The TMA warp's
+// (stream-K), so every SM streams the same number of bytes; a matrix with
+// nearly one tile per SM gives each CTA one whole tile instead.  The TMA warp's
 // lane 0 issues cp.async.bulk.tensor copies of each stage -- the int4 codes
-// (128-row x 128-byte boxes, 128B swizzle) and the fp16 scales -- into a ring
-// of mbarrier-guarded stages.  Passes of up to 16 columns use 512-k stages and
+// (128-row x 128-byte boxes, 128B swizzle) and the scales (fp16 per block, or
+// the super-block records of spec_qmatmul_sb) -- into a ring of
+// mbarrier-guarded stages.  Passes of up to 16 columns use 512-k stages and
 // two activation warps, which read the stage's activation columns from L2,
 // write them in MMA B-fragment order together with the block sums and hand the
 // stage on.  The 80-column pass uses 256-k stages (a segment is two stages;
@@ -38,7 +40,8 @@
 // in, without waiting; the CTA holding the leading segments folds them in
 // segment order once all have arrived (the usual case when it gets there),
 // else leaves its prefix for whichever CTA arrives last.  No CTA waits for
-// another; the counters end at zero.
+// another; the counters end at zero, and consumed sums lying where a later
+// call keeps its counters (the workspace's first 64 KB) are cleared.
 //
 // The weight format (int4 block 32, fp16 scale, even k in the low nibble) is
 // the stand-in for the block-quantised formats named in ramgpt.org, "When
