@@ -31,6 +31,13 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _stamp(path: str, deps: list[str]) -> None:
+    """Give a fresh output an mtime no older than its newest input, so a machine
+    whose clock runs behind the sources' mtimes does not see it as stale forever."""
+    newest = max([os.path.getmtime(d) for d in deps] + [os.path.getmtime(path)])
+    os.utime(path, (newest, newest))
+
+
 def is_stale() -> bool:
     """True when libspec.so is absent or older than a source or header it is built from."""
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))]
@@ -64,6 +71,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+                src = cmd[cmd.index("-c") + 1]
+                _stamp(cmd[cmd.index("-o") + 1], [src] + headers)
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".{os.getpid()}.tmp"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
@@ -71,6 +80,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
         os.replace(tmp, LIB)
+        _stamp(LIB, objs + [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + headers)
     return LIB
 
 
