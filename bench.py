@@ -84,7 +84,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        out_dir = os.environ.get("SPEC_BENCH_LOG_DIR") or os.path.join(ROOT, "gpurun_out")
+        out_dir = os.environ.get("SPEC_BENCH_LOG_DIR") or os.path.join(ROOT, "bench_logs")
         self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
