@@ -54,6 +54,23 @@ def test_qmatmul_host_validation(kw, msg):
     assert msg in str(e.value) and e.value.status == 1
 
 
+@pytest.mark.parametrize("kw,msg,status", [
+    (dict(K=768 + 32), "multiple of 256", 1),
+    (dict(sbr=FAKE + 8), "16-byte aligned", 1),
+    (dict(N=0), "N >= 1", 1),
+    (dict(y_dt=1), "y_dt", 1),
+    (dict(ws_bytes=16), "workspace", 3),
+])
+def test_qmatmul_sb_host_validation(kw, msg, status):
+    import invariant_speculative_verification_gb300 as L
+    a = dict(wq=FAKE, sbr=FAKE, N=64, K=768, x=FAKE, n_cols=2, ldx=1024, y=FAKE, y_dt=0, ldy=64, ws_bytes=1 << 30)
+    a.update(kw)
+    with pytest.raises(L.SpecError) as e:
+        L.spec_qmatmul_sb(a["wq"], a["sbr"], a["N"], a["K"], a["x"], a["n_cols"], a["ldx"], a["y"], a["y_dt"], a["ldy"],
+                          0, FAKE, a["ws_bytes"], stream=0)
+    assert msg in str(e.value) and e.value.status == status
+
+
 def test_flash_decode_host_validation_and_workspace():
     import invariant_speculative_verification_gb300 as L
     ws = L.spec_flash_decode_workspace(10, 8, 128, 1000)
