@@ -109,6 +109,28 @@ def test_verify_and_compact_host_validation():
                           stream=0)
 
 
+@pytest.mark.parametrize("inv_temp", [0.0, -1.0, float("inf"), float("nan")])
+def test_verify_sample_rejects_temperatures_that_are_not_positive_and_finite(inv_temp):
+    import invariant_speculative_verification_gb300 as L
+    with pytest.raises(L.SpecError, match="inv_temperature") as e:
+        L.spec_verify_sample(FAKE, 0, 1000, FAKE, 2, 10, FAKE, FAKE, None, inv_temp, 7, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             1 << 20, stream=0)
+    assert e.value.status == 1
+
+
+def test_verify_sample_host_validation():
+    import invariant_speculative_verification_gb300 as L
+    with pytest.raises(L.SpecError, match="multiple of 8"):
+        L.spec_verify_sample(FAKE, 0, 1001, FAKE, 2, 10, FAKE, FAKE, None, 1.25, 7, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             1 << 20, stream=0)
+    with pytest.raises(L.SpecError, match="S <= R"):
+        L.spec_verify_sample(FAKE, 0, 1000, FAKE, 4, 3, FAKE, FAKE, None, 1.25, 7, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             1 << 20, stream=0)
+    with pytest.raises(L.SpecError, match="16-byte aligned"):
+        L.spec_verify_sample(FAKE + 4, 0, 1000, FAKE, 2, 10, FAKE, FAKE, None, 1.25, 7, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             1 << 20, stream=0)
+
+
 def test_zero_sized_calls_launch_nothing():
     import invariant_speculative_verification_gb300 as L
     L.spec_qmatmul(FAKE, FAKE, 64, 512, FAKE, 0, 512, FAKE, 0, 64, 0, None, 0, stream=0)
