@@ -163,3 +163,28 @@ def test_header_compiles_as_c_and_a_c_program_links_and_runs(tmp_path):
                            "-o", str(exe), lib, "-Wl,-rpath," + os.path.dirname(lib)])
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     assert out == [str(len(names)), "SPEC_OK", "SPEC_ERR_WORKSPACE"]
+
+
+def test_glue_host_validation():
+    """Each glue entry point rejects bad sizes, NULLs or misalignment on the host
+    (status 1, nothing launched)."""
+    import invariant_speculative_verification_gb300 as L
+    bad = [
+        ("embed: bad sizes", lambda: L.spec_embed(FAKE, 0, 64, FAKE, 4, FAKE, stream=0)),
+        ("embed: NULL", lambda: L.spec_embed(FAKE, 100, 64, None, 4, FAKE, stream=0)),
+        ("H % 4", lambda: L.spec_add_rmsnorm(FAKE, None, FAKE, 4, 66, 1e-6, FAKE, stream=0)),
+        ("add_rmsnorm", lambda: L.spec_add_rmsnorm(FAKE + 4, None, FAKE, 4, 64, 1e-6, FAKE, stream=0)),
+        ("rope_table", lambda: L.spec_rope_table(FAKE, 128, 63, 10000.0, stream=0)),
+        ("rope_table", lambda: L.spec_rope_table(FAKE, 128, 64, -1.0, stream=0)),
+        ("swiglu: bad sizes", lambda: L.spec_swiglu(FAKE, 4, 0, FAKE, stream=0)),
+        ("65535", lambda: L.spec_swiglu(FAKE, 65536, 64, FAKE, stream=0)),
+        ("cast_bf16", lambda: L.spec_cast_bf16(None, 8, FAKE, stream=0)),
+        ("ngram_draft: bad sizes", lambda: L.spec_ngram_draft(FAKE, 0, FAKE, 2, 4, FAKE, FAKE, stream=0)),
+        ("ngram_draft: NULL", lambda: L.spec_ngram_draft(FAKE, 64, FAKE, 2, 4, None, FAKE, stream=0)),
+        ("commit_accepted: bad sizes",
+         lambda: L.spec_commit_accepted(FAKE, 0, FAKE, FAKE, 4, FAKE, FAKE, FAKE, FAKE, 2, stream=0)),
+    ]
+    for msg, call in bad:
+        with pytest.raises(L.SpecError) as e:
+            call()
+        assert e.value.status == 1 and msg.split(":")[0] in str(e.value), (msg, str(e.value))
