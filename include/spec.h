@@ -369,6 +369,18 @@ spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *ws, int N, 
                                   int n_cols, int ldx, float *y, int ldy, int nt,
                                   void *workspace, size_t ws_bytes, spec_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Test hook for the bounded-wait error path (the pages have no counterpart:
+ * this exercises the library's own failure handling).  Launches one thread
+ * that arms an mbarrier for 16 transaction bytes, issues no copy (so nothing
+ * is in flight and the phase can never complete), and waits for it through
+ * the same bounded wait every kernel uses, limited to `polls` polls.  When the
+ * wait runs out the kernel ORs SPEC_DEVERR_TIMEOUT into *dev_err (device
+ * memory) and returns normally; the context stays usable and later calls on
+ * the stream run as usual.  polls must be in [1, 2^20]; dev_err non-NULL.
+ * ---------------------------------------------------------------------- */
+spec_status spec_debug_wait_timeout(uint32_t polls, int32_t *dev_err, spec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

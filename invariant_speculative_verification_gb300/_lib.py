@@ -55,6 +55,7 @@ _SIGS = {
     "spec_cast_bf16": (_i32, [_vp, _sz, _vp, _vp]),
     "spec_ngram_draft": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "spec_commit_accepted": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
+    "spec_debug_wait_timeout": (_i32, [ctypes.c_uint32, _vp, _vp]),
 }
 
 _lib = None
@@ -153,6 +154,10 @@ def spec_qmatmul_debug_nt(wq, ws, N, K, x, n_cols, ldx, y, ldy, nt, workspace, w
     _check("spec_qmatmul_debug_nt", load().spec_qmatmul_debug_nt(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx,
                                                                  _ptr(y), ldy, nt, _ptr(workspace), int(ws_bytes),
                                                                  _stream(stream)))
+
+
+def spec_debug_wait_timeout(polls, dev_err, stream=None):
+    _check("spec_debug_wait_timeout", load().spec_debug_wait_timeout(int(polls), _ptr(dev_err), _stream(stream)))
 
 
 def spec_flash_decode_workspace(R, Hq, D, max_kv_len) -> int:

@@ -93,3 +93,30 @@ extern "C" const char *spec_status_string(spec_status st) {
 }
 
 extern "C" const char *spec_last_error(void) { return spec::g_last_error; }
+
+// ---------------------------------------------------------------------------
+// Test hook for the bounded-wait error path.  One thread arms an mbarrier for
+// 16 transaction bytes and issues no copy, so the phase never completes and
+// nothing is in flight; it then waits through the same bounded wait every
+// kernel of the library uses, with `polls` polls, and reports
+// SPEC_DEVERR_TIMEOUT when the wait runs out.  The kernel returns normally and
+// the context stays usable.
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void wait_timeout_kernel(uint32_t polls, int32_t *dev_err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    dev::mbar_init(&bar, 1);
+    dev::fence_barrier_init();
+    dev::mbar_arrive_expect_tx(&bar, 16);
+    if (!dev::mbar_wait(&bar, 0, polls)) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+}
+}  // namespace
+
+extern "C" spec_status spec_debug_wait_timeout(uint32_t polls, int32_t *dev_err, spec_stream_t stream) {
+    SPEC_CHECK_ARG(dev_err, "debug_wait_timeout: dev_err is NULL");
+    SPEC_CHECK_ARG(polls >= 1 && polls <= (1u << 20), "debug_wait_timeout: polls must be in [1, 2^20] (polls=%u)",
+                   polls);
+    wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(polls, dev_err);
+    return spec::cuda_status(cudaGetLastError(), "debug_wait_timeout launch");
+}

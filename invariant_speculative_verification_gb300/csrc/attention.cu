@@ -468,12 +468,9 @@ spec_status launch_partial(const CUtensorMap &tk, const CUtensorMap &tv, const v
                            cudaStream_t st) {
     using C = ACfg<D>;
     auto kern = attn_partial_kernel<D, BF16>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return spec::cuda_status(e, "cudaFuncSetAttribute(attn smem)");
-        configured = true;
-    }
+    static spec::SmemOptIn opt_in;
+    spec_status so = spec::smem_opt_in(kern, C::SMEM, opt_in, "cudaFuncSetAttribute(attn smem)");
+    if (so != SPEC_OK) return so;
     dim3 grid(nc_max, Hkv, S);
     cudaError_t le = spec::launch_pdl(kern, grid, dim3(THREADS), C::SMEM, st, tk, tv, reinterpret_cast<const uint16_t *>(q),
                                       Hq, Hkv, scale * LOG2E, num_pages, bt, max_blocks, ctx, cu, R, max_kv_len, nc_max,

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/spec.h"
 
 // ---------------------------------------------------------------------------
@@ -43,6 +45,30 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
+// A kernel's dynamic shared-memory opt-in is per device: set it the first time
+// the kernel is launched on each device (thread-safe; one cache per kernel).
+constexpr int kMaxDevices = 64;
+struct SmemOptIn {
+    std::mutex mu;
+    bool done[kMaxDevices] = {};
+};
+
+template <typename K>
+spec_status smem_opt_in(K kern, int bytes, SmemOptIn &cache, const char *what) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(SPEC_ERR_UNSUPPORTED, "%s: device ordinal %d >= %d", what, dev,
+                                                   kMaxDevices);
+    std::lock_guard<std::mutex> lock(cache.mu);
+    if (!cache.done[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return cuda_status(e, what);
+        cache.done[dev] = true;
+    }
+    return SPEC_OK;
 }
 
 }  // namespace spec
@@ -99,9 +125,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait: returns false (and the caller reports a timeout) if the phase
-// did not complete within kMaxPolls polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kMaxPolls; ++i)
+// did not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = kMaxPolls) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
@@ -216,5 +242,87 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void report(int32_t *dev_err, int32_t bits) {
     if (dev_err) atomicOr(dev_err, bits);
 }
+
+// ---------------------------------------------------------------------------
+// 5th-generation tensor cores (tcgen05) and tensor memory (TMEM)
+// ---------------------------------------------------------------------------
+// TMEM addresses: lane in bits 31..16, 32-bit column in bits 15..0.  A warp may
+// access only the 32 lanes 32 (warp % 4) .. 32 (warp % 4) + 31.
+
+// Allocates ncols columns (a power of two >= 32) for this CTA and writes the
+// base address to *slot; executed by one whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Releases what tmem_alloc took (the same warp, after every TMEM access has completed).
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Order tcgen05 operations against thread synchronisation (mbarrier, bar.sync).
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// One arrival on `bar` once every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte-swizzle
+// layout: rows of 128 bytes, 8-row groups 1024 bytes apart, groups 1024-byte
+// aligned; `addr` may step along K inside the 128-byte row (32 bytes per K = 16).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4)   // start address
+           | ((uint64_t)1 << 16)                // leading byte offset (unused by this layout)
+           | ((uint64_t)(1024 >> 4) << 32)      // stride byte offset: next 8-row group
+           | ((uint64_t)1 << 46)                // descriptor version
+           | ((uint64_t)2 << 61);               // 128-byte swizzle
+}
+
+// Instruction descriptor of a kind::f16 MMA: bf16 A and B, both K-major, fp32 D, M x N.
+__host__ __device__ constexpr uint32_t mma_idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM, fp32) = A (TMEM, bf16) x B (shared memory, bf16) + (accumulate ? D : 0); issued by one thread.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Warp-wide TMEM <-> register copies, shape 32x32b: each lane moves its own
+// lane's consecutive columns.  Loads are complete after tmem_wait_ld, stores
+// after tmem_wait_st.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                 "%13, %14, %15, %16};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace dev

@@ -81,29 +81,44 @@ class Decoder:
     def embed(self, tokens, R):
         L.spec_embed(self.emb, self.V, self.H, tokens, R, self.h, self.dev_err)
 
-    def layer(self, li, R, cu_rows, ctx, S, max_kv_len=None):
+    def layer(self, li, R, cu_rows, ctx, S, max_kv_len=None, trace=None):
+        """Decoder layer li over R rows.  ``trace(name)``, if given, is called after
+        each step (norm1, qkv, rope, attn, o, norm2, gu, swiglu, down) so a caller
+        can read the step's output buffer; it launches nothing itself."""
         lay, H, F, D = self.layers[li], self.H, self.F, self.D
         max_kv_len = max_kv_len or self.max_len
+        tr = trace or (lambda name: None)
         L.spec_add_rmsnorm(self.h, None, lay["norm1"], R, H, self.cfg.eps, self.a)
+        tr("norm1")
         L.spec_qmatmul(lay["qkv"][0], lay["qkv"][1], self.nqkv, H, self.a, R, H, self.qkv, L.SPEC_F32,
                        self.nqkv, 0, self.qws, self.qws_bytes, self.dev_err)
+        tr("qkv")
         L.spec_rope_append(self.qkv, R, self.Hq, self.Hkv, D, self.rope, self.max_len, cu_rows, ctx, S, self.q,
                            self.k_cache[li], self.v_cache[li], self.pages, self.block_table, self.max_blocks,
                            None, None, self.dev_err)
+        tr("rope")
         L.spec_flash_decode(self.q, L.SPEC_BF16, self.Hq, self.Hkv, D, 1.0 / math.sqrt(D), self.k_cache[li],
                             self.v_cache[li], self.pages, self.block_table, self.max_blocks, ctx, cu_rows, S, R,
                             max_kv_len, self.attn, L.SPEC_BF16, self.attn_ws, self.ws_bytes, self.dev_err)
+        tr("attn")
         L.spec_qmatmul(lay["o"][0], lay["o"][1], H, self.Hq * D, self.attn, R, self.Hq * D, self.h, L.SPEC_F32, H, 1,
                        self.qws, self.qws_bytes, self.dev_err)
+        tr("o")
         L.spec_add_rmsnorm(self.h, None, lay["norm2"], R, H, self.cfg.eps, self.a)
+        tr("norm2")
         L.spec_qmatmul(lay["gu"][0], lay["gu"][1], 2 * F, H, self.a, R, H, self.gu, L.SPEC_F32, 2 * F,
                        0, self.qws, self.qws_bytes, self.dev_err)
+        tr("gu")
         L.spec_swiglu(self.gu, R, F, self.act)
+        tr("swiglu")
         L.spec_qmatmul(lay["down"][0], lay["down"][1], H, F, self.act, R, F, self.h, L.SPEC_F32, H, 1,
                        self.qws, self.qws_bytes, self.dev_err)
+        tr("down")
 
-    def head(self, R):
+    def head(self, R, trace=None):
         L.spec_add_rmsnorm(self.h, None, self.final_norm, R, self.H, self.cfg.eps, self.a)
+        if trace:
+            trace("final_norm")
         L.spec_qmatmul(self.lm[0], self.lm[1], self.V, self.H, self.a, R, self.H, self.logits, L.SPEC_F32,
                        self.V, 0, self.qws, self.qws_bytes, self.dev_err)
 

@@ -339,6 +339,53 @@ def verify_case(seed: int, draft_lens, V: int, dt: int = DT_F32, sigma: float = 
     return VerifyCase(V, dt, np.ascontiguousarray(logits), cu, drafts, ctx, top, ties)
 
 
+def verify_case_natural(seed: int, draft_lens, V: int, sigma: float = 2.0, tie_frac: float = 0.01,
+                        edges=(), ctx_range=(256, 8192)) -> VerifyCase:
+    """bf16 logits whose row maxima are decided by the raw N(0, sigma) draws (no
+    planted top), with planted competitors on a tie_frac share of the rows.  A
+    planted row copies its largest value v (first occurrence at p) to another
+    index t, chosen in turn as: an exact tie at a lower index t < p; the same at
+    the element just before one of `edges` (a scan-split boundary of the
+    consumer) with p moved to just after it; a value one bf16 ulp below v at a
+    lower index; an exact tie at a higher index.  `planted_top` is -1 (the
+    answer is left to the oracle) and the drafts are uniform random tokens
+    (tests derive matching drafts from the oracle's answer)."""
+    g = rng(seed)
+    L = np.asarray(draft_lens, dtype=np.int32)
+    S = len(L)
+    cu = np.zeros(S + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(L + 1)
+    R = int(cu[-1])
+    bits = f32_to_bf16_bits(g.normal(0.0, sigma, size=(R, V)).astype(np.float32))
+    ties = g.random(R) < tie_frac
+    edges = [int(e) for e in edges if 0 < int(e) < V]
+    kind = 0
+    for r in np.nonzero(ties)[0]:
+        row = bf16_bits_to_f32(bits[r])
+        p = int(np.argmax(row))            # first occurrence of the row's largest value
+        top = bits[r, p]
+        k = kind % 4
+        kind += 1
+        if k == 1 and edges:
+            e = edges[(kind // 4) % len(edges)]
+            # move the maximum to just after the boundary, its exact copy to just before it
+            bits[r, p] = bits[r, e]
+            bits[r, e] = top
+            bits[r, e - 1] = top
+        elif k == 0 or k == 1:
+            if p > 0:
+                bits[r, int(g.integers(0, p))] = top
+        elif k == 2:
+            if p > 0:
+                bits[r, int(g.integers(0, p))] = _bf16_next_down(top)
+        else:
+            if p < V - 1:
+                bits[r, int(g.integers(p + 1, V))] = top
+    drafts = g.integers(0, V, size=R - S).astype(np.int32)
+    ctx = g.integers(ctx_range[0], ctx_range[1] + 1, size=S).astype(np.int32)
+    return VerifyCase(V, DT_BF16, np.ascontiguousarray(bits), cu, drafts, ctx, np.full(R, -1, np.int32), ties)
+
+
 def _bf16_next_down(b):
     b = int(b)
     if b & 0x8000:

@@ -40,3 +40,32 @@ def rel_err_rows(got: np.ndarray, ref: np.ndarray) -> float:
 
 
 TOL = 2e-3  # max abs error relative to the output row's max-abs (fp32-accumulated 16-bit math)
+
+
+def bf16_round(x) -> np.ndarray:
+    """float64 values rounded to bfloat16 (8 significant bits, ties to even), as float64."""
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def bf16_rounding_ok(got_bits: np.ndarray, ref: np.ndarray, slack) -> bool:
+    """A bf16 output that rounds a quantity whose exact value is ``ref``, computed
+    on the device within ``slack`` (absolute, per element) of it: every element
+    equals ref rounded to bf16, except where ref lies within slack of a rounding
+    midpoint, where either neighbour is right."""
+    got = bits_to_f64(got_bits)
+    ref = np.asarray(ref, np.float64)
+    slack = np.broadcast_to(np.asarray(slack, np.float64), ref.shape)
+    exp = bf16_round(ref)
+    bad = got != exp
+    if not bad.any():
+        return True
+    lo, hi = bf16_round(ref[bad] - slack[bad]), bf16_round(ref[bad] + slack[bad])
+    g = got[bad]
+    return bool(np.all((g == lo) | (g == hi)))
+
+
+def bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(bits).view(np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)

@@ -96,11 +96,13 @@ def test_long_context_gqa_parity_and_width_invariance(L):
         out = d.call()
         for i in range(n):
             assert bits_equal(d.single_row(0, i), out[i]), (L, n, i)
-        # oracle on sampled (row, head) pairs; all of them at the shortest length
+        # oracle on every (row, head) pair at the shortest length; at the longer ones on
+        # the block's first and last rows with all 40 heads, plus sampled pairs
         want = np.zeros((n, 40), np.uint8)
         if L == 1024:
             want[:] = 1
         else:
+            want[0, :] = want[n - 1, :] = 1
             g = np.random.default_rng(L + n)
             want[g.integers(0, n, 6), g.integers(0, 40, 6)] = 1
         ref = oracle.attention(case, want=want)

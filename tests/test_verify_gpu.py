@@ -58,6 +58,40 @@ def test_ragged_bf16_large_vocab():
     assert np.array_equal(got["argmax"], case.planted_top)
 
 
+@pytest.mark.parametrize("R_seqs", [64, 8])
+def test_ragged_bf16_natural_rows_and_lower_index_ties(R_seqs):
+    """Rows whose maximum comes from the raw N(0, 2) bf16 draws, 5 % of them with a
+    planted competitor: exact ties at a lower index (within a scan split and across
+    every candidate split boundary), one-ulp-lower values at a lower index, and ties
+    at a higher index.  The drafts copy the oracle's argmax with probability 0.7.
+    tokenstrom.com, "'Lossless,' but not quite", section "Why the math checks out and
+    the text still flips": near ties decide the token, so the tie rule must hold."""
+    V = 152064
+    g = np.random.default_rng(1044 + R_seqs)
+    L = g.integers(1, 8, size=R_seqs)
+    nvec = V // 8
+    edges = sorted({8 * (nvec * k // sp) for sp in range(2, 9) for k in range(1, sp)})
+    case = synth.verify_case_natural(1044 + R_seqs, L, V, sigma=2.0, tie_frac=0.05, edges=edges)
+    # drafts from the oracle's own argmax (probability 0.7), else uniform
+    am = oracle.verify_greedy(case.logits, case.dt, V, case.cu_rows, case.drafts, case.ctx_start)["argmax"]
+    drafts = case.drafts.copy()
+    for s in range(case.S):
+        for i in range(int(L[s])):
+            if g.random() < 0.7:
+                drafts[case.cu_rows[s] - s + i] = am[case.cu_rows[s] + i]
+    got, ref = check_exact(case, drafts=drafts)
+    assert got["err"] == 0
+    assert ref["accepted"].sum() > 0
+    # the planted lower-index ties really decide some rows
+    tie_rows = np.nonzero(case.tie_rows)[0]
+    assert len(tie_rows) > 0
+    lower = 0
+    for r in tie_rows:
+        row = synth.bf16_bits_to_f32(case.logits[r])
+        lower += int(np.sum(row == row[am[r]]) > 1 and am[r] == np.flatnonzero(row == row.max())[0])
+    assert lower > 0
+
+
 def test_width1_rows_and_all_or_nothing_acceptance():
     case = synth.verify_case(33, [0, 3, 0, 7, 1], 4096, DT_BF16, sigma=2.0, tie_frac=0.3)
     check_exact(case)
