@@ -92,7 +92,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -188,7 +188,7 @@ def qgemv_sweep(torch, L, hbm_peak):
         wsp = torch.zeros(wsb // 4 + 64, dtype=torch.int32, device=dev)
         res = {}
 
-        def timed(n, fn_one, reps=3):
+        def timed(n, fn_one, reps=10):
             # a graph of `copies` launches, each on another weight copy
             s = torch.cuda.Stream()
             s.wait_stream(torch.cuda.current_stream())
@@ -669,11 +669,12 @@ def qmatmul_step_roofline(torch, L, w, hbm_peak, peak_kind):
     g.replay()
     torch.cuda.synchronize()
     ts = []
-    for _ in range(10):
+    stream = torch.cuda.current_stream()
+    for _ in range(100):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+        e0.record(stream)
         g.replay()
-        e1.record()
+        e1.record(stream)
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1) / 1e3)
     t = statistics.median(ts)
@@ -707,29 +708,135 @@ def recorded_traffic(kernel: str):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_step_sample(w, prompts, pads, ctx_tokens=4):
-    """One speculative verify step of ONE sequence through the CPU oracle decoder:
-    a short context (ctx_tokens prompt tokens, prefilled before timing), then the
-    last token + 4 n-gram drafts verified in one 5-row pass.  Returns (tokens, s)."""
+CPU_CTX = PROMPT - 1   # the verify block's first position in the timed GPU steps' regime (128-token prompts)
+
+
+def _threads():
+    return max(1, os.cpu_count() or 1)
+
+
+def _pool_map(fn, items, threads):
+    """fn over items on `threads` host threads (the oracle's C code runs with the GIL released)."""
+    import concurrent.futures as cf
+    if threads <= 1:
+        return [fn(it) for it in items]
+    with cf.ThreadPoolExecutor(threads) as ex:
+        return list(ex.map(fn, items))
+
+
+def oracle_e2e_step(w, prompts, pads, threads, n_seqs=N_SEQ):
+    """One speculative verify step of n_seqs sequences through the CPU oracle decoder:
+    each sequence's last prompt token + 4 n-gram drafts (5 rows) at positions
+    CPU_CTX .. CPU_CTX + 4 over a CPU_CTX-token context, then greedy verification.
+    The context's K/V pages are seeded bf16 N(0, 1) values (a prefill of 16 x 127
+    tokens would take minutes on the host).  Sequences are split over `threads`
+    host threads, each running the unchanged oracle on its own sequence.
+    Returns (generated tokens, seconds)."""
     import oracle
-    dec = oracle.Decoder(w, 1, ctx_tokens + WIDTH + 16)
-    p = prompts[0, :ctx_tokens]
-    dec.forward(p[:-1], np.zeros(1, np.int32), np.array([0, ctx_tokens - 1], np.int32))
-    d, _ = oracle.ngram_draft(p, WIDTH, pads[0, 0])
-    block = np.concatenate([[p[-1]], d]).astype(np.int32)
+    cfg = w.cfg
+    dec = oracle.Decoder(w, n_seqs, CPU_CTX + WIDTH + 16)
+    g = np.random.default_rng(1010)
+    npos = CPU_CTX
+    for li in range(cfg.layers):
+        for cache in (dec.k_cache[li], dec.v_cache[li]):
+            vals = synth.f32_to_bf16_bits(g.normal(0, 1, (n_seqs, npos, cfg.kv_heads, cfg.head_dim)).astype(np.float32))
+            for s in range(n_seqs):
+                for p_ in range(npos):
+                    cache[dec.block_table[s, p_ // 16], :, p_ % 16] = vals[s, p_]
+    blocks, drafts = [], []
+    for s in range(n_seqs):
+        hist = prompts[s, :CPU_CTX + 1]
+        d, _ = oracle.ngram_draft(hist, WIDTH, pads[0, s])   # pads: [step][sequence][slot]
+        blocks.append(np.concatenate([[hist[-1]], d]).astype(np.int32))
+        drafts.append(np.asarray(d, np.int32))
+    cu = np.array([0, WIDTH + 1], np.int32)
+    ctx = np.array([CPU_CTX], np.int32)
+
+    def one(s):
+        lg = dec.forward(blocks[s], ctx, cu, seqs=[s])
+        res = oracle.verify_greedy(lg, synth.DT_F32, cfg.vocab, cu, drafts[s], ctx)
+        return int(res["accepted"][0]) + 1
+
     t0 = time.perf_counter()
-    lg = dec.forward(block, np.array([ctx_tokens - 1], np.int32), np.array([0, WIDTH + 1], np.int32))
-    res = oracle.verify_greedy(lg, synth.DT_F32, w.cfg.vocab, np.array([0, WIDTH + 1], np.int32), d,
-                               np.array([ctx_tokens - 1], np.int32))
-    t = time.perf_counter() - t0
-    return int(res["accepted"][0]) + 1, t
+    toks = _pool_map(one, list(range(n_seqs)), threads)
+    return int(sum(toks)), time.perf_counter() - t0
+
+
+def oracle_kernel_times(threads):
+    """The oracle's time per call on the hot path's kernels, 1 host thread and
+    `threads` threads (independent units split: weight rows for the matmul,
+    (row, head) pairs for attention, sequences for verification and compaction)."""
+    import oracle
+    out = {}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    # int4 GEMV 17408 x 5120 at widths 1 and 8 (weight rows split)
+    N, K = 17408, 5120
+    wq, ws = synth.qmatmul_weights(1002 + K % 97, N, K)
+    x = synth.activations_bf16(7, 8, K)
+    for n in (1, 8):
+        def run(th, _n=n):
+            ch = [(i * N // th, (i + 1) * N // th) for i in range(th)]
+            _pool_map(lambda c: oracle.qmatmul(wq[c[0]:c[1]], ws[c[0]:c[1]], x[:_n], c[1] - c[0], K), ch, th)
+        out[f"qgemv_17408x5120_w{n}"] = {"cpu_us_1t": round(timed(lambda: run(1)) * 1e6, 1),
+                                          f"cpu_us_{threads}t": round(timed(lambda: run(threads)) * 1e6, 1)}
+    # attention: one row at KV 16384, 40/8 heads x 128 ((row, head) pairs split)
+    c = synth.attention_case(1003 + 16384 + 10, rows=[1], ctx=[16383], Hq=40, Hkv=8, D=128, dt=synth.DT_BF16,
+                             q_std=1 / math.sqrt(128), scale=1.0)
+
+    def att(th):
+        def part(h0h1):
+            want = np.zeros((1, 40), np.uint8)
+            want[0, h0h1[0]:h0h1[1]] = 1
+            return oracle.attention(c, want=want)
+        _pool_map(part, [(i * 40 // th, (i + 1) * 40 // th) for i in range(th)], th)
+    out["attention_L16384_w1"] = {"cpu_us_1t": round(timed(lambda: att(1)) * 1e6, 1),
+                                  f"cpu_us_{threads}t": round(timed(lambda: att(threads)) * 1e6, 1)}
+    # greedy verification: 64 sequences, V = 152064 bf16 (sequences split)
+    g = np.random.default_rng(1004)
+    dl = g.integers(1, 8, size=64)
+    vc = synth.verify_case(1004, dl, 152064, synth.DT_BF16, sigma=2.0, tie_frac=0.01)
+
+    def ver(th):
+        def part(sr):
+            s0, s1 = sr
+            r0, r1 = int(vc.cu_rows[s0]), int(vc.cu_rows[s1])
+            return oracle.verify_greedy(vc.logits[r0:r1], vc.dt, vc.V, vc.cu_rows[s0:s1 + 1] - r0,
+                                        vc.drafts[r0 - s0:r1 - s1], vc.ctx_start[s0:s1])
+        _pool_map(part, [(i * 64 // th, (i + 1) * 64 // th) for i in range(th)], th)
+    out["verify_64seqs_V152064"] = {"cpu_us_1t": round(timed(lambda: ver(1)) * 1e6, 1),
+                                    f"cpu_us_{threads}t": round(timed(lambda: ver(threads)) * 1e6, 1)}
+    # KV compaction: the same 64 sequences, 32 heads x 128 (sequences split)
+    res = oracle.verify_greedy(vc.logits, vc.dt, vc.V, vc.cu_rows, vc.drafts, vc.ctx_start)
+    # (short contexts: the compaction work does not depend on them, and the oracle copies the cache per call)
+    cc = synth.compact_case(1005, dl, Hkv=32, D=128, ctx_range=(16, 64), accepted=res["accepted"])
+
+    def comp(th):
+        def part(sr):
+            s0, s1 = sr
+            r0, r1 = int(cc.cu_rows[s0]), int(cc.cu_rows[s1])
+            return oracle.kv_compact(cc.k_stage[r0:r1], cc.v_stage[r0:r1], cc.k_cache, cc.v_cache, 32, 128,
+                                     cc.block_table[s0:s1], cc.ctx_start[s0:s1], cc.accepted[s0:s1],
+                                     cc.cu_rows[s0:s1 + 1] - r0)
+        _pool_map(part, [(i * 64 // th, (i + 1) * 64 // th) for i in range(th)], th)
+    out["kv_compact_64seqs"] = {"cpu_us_1t": round(timed(lambda: comp(1)) * 1e6, 1),
+                                f"cpu_us_{threads}t": round(timed(lambda: comp(threads)) * 1e6, 1)}
+    return out
 
 
 def cpu_baseline(w, prompts, pads):
-    tokens, t = oracle_step_sample(w, prompts, pads)
-    return {"value": round(tokens / t, 4), "unit": "tok/s", "cores": 1, "kind": "oracle",
-            "sample": "one verify step (5 rows: last token + 4 n-gram drafts) of one sequence with a 4-token "
-                      f"context through the full 8-layer decoder + LM head + verify; {t:.1f} s on 1 host core"}
+    th = _threads()
+    tokens, t = oracle_e2e_step(w, prompts, pads, th)
+    return {"value": round(tokens / t, 4), "unit": "tok/s", "cores": th, "kind": "oracle",
+            "sample": f"one speculative verify step of all {N_SEQ} sequences (5 rows each: last prompt token + "
+                      f"{WIDTH} n-gram drafts) at positions {CPU_CTX}..{CPU_CTX + WIDTH} over a {CPU_CTX}-token "
+                      f"context (seeded K/V pages), through the 8-layer oracle decoder + LM head + verify; "
+                      f"sequences split over {th} host threads; {t:.1f} s",
+            "kernels": oracle_kernel_times(th)}
 
 
 def run_reference(args):
@@ -740,23 +847,25 @@ def run_reference(args):
     w = synth.decoder_weights(1005, cfg)
     prompts = synth.prompts(1006, N_SEQ, PROMPT, cfg.vocab)
     pads = synth.pad_tokens(1007, N_SEQ, 8, WIDTH, cfg.vocab).transpose(1, 0, 2).copy()
+    th = _threads()
     for _ in range(args.warmup):
-        oracle_step_sample(w, prompts, pads, ctx_tokens=2)
+        oracle_e2e_step(w, prompts, pads, th)
     tot_tok, tot_t = 0, 0.0
     for _ in range(args.steps):
-        k, t = oracle_step_sample(w, prompts, pads, ctx_tokens=2)
+        k, t = oracle_e2e_step(w, prompts, pads, th)
         tot_tok += k
         tot_t += t
     v = tot_tok / tot_t
-    sample = ("each step: one 5-row speculative verify step of one sequence (2-token context) through the CPU "
-              "oracle decoder, single-threaded")
+    sample = (f"each step: one speculative verify step of all {N_SEQ} sequences (5 rows each) at a "
+              f"{CPU_CTX}-token context through the CPU oracle decoder + verify, sequences split over {th} host "
+              f"threads")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded random-init weights, random prompts)",
-        "config": {"workload": WORKLOAD, "global_batch": 1, "parallelism": "1 host core"},
-        "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "config": {"workload": WORKLOAD, "global_batch": N_SEQ, "parallelism": f"{th} host threads"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": th, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -769,7 +878,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     args = ap.parse_args()
     if args.impl == "reference":
-        args.steps = min(args.steps, 8)
+        # each step is seconds of host work: keep the whole run within a few minutes
+        args.steps = min(args.steps, 6)
+        args.warmup = min(args.warmup, 1)
         run_reference(args)
     else:
         run_ours(args)

@@ -52,6 +52,8 @@ def lib():
             vp, i32, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
             c.oracle_qmatmul.argtypes = [vp, vp, i32, i32, vp, i32, i32, vp]
             c.oracle_qmatmul_sb.argtypes = [vp, vp, i32, i32, vp, i32, i32, vp]
+            c.oracle_margin_gate.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+            c.oracle_margin_gate.restype = i32
             c.oracle_sb_record.argtypes = [vp, vp, vp]
             c.oracle_attention.argtypes = [vp, i32, i32, i32, i32, dbl, vp, vp, vp, i32, vp, vp, i32, vp, vp]
             c.oracle_verify_greedy.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp]
@@ -227,6 +229,19 @@ def verify_sample(logits, dt: int, V: int, cu_rows, drafts, ctx_start, inv_temp:
                                       seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF,
                                       _p(tok), _p(acc), _p(cor), _p(cn), _p(gap))
     return dict(token=tok, accepted=acc, correction=cor, ctx_new=cn, top2_gap=gap, nans=int(nans))
+
+
+def margin_gate(logits, err):
+    """Top-2 margin gate over fp32 logits [R][V] with per-row error bounds err[R]:
+    returns (top index [R], margin [R], recheck flags [R] as bool)."""
+    lg = _c(logits, np.float32)
+    R, V = lg.shape
+    e = _c(np.broadcast_to(np.asarray(err, np.float64), (R,)), np.float64)
+    top = np.zeros(R, np.int32)
+    margin = np.zeros(R, np.float64)
+    flag = np.zeros(R, np.uint8)
+    lib().oracle_margin_gate(_p(lg), R, V, _p(e), _p(top), _p(margin), _p(flag))
+    return top, margin, flag.astype(bool)
 
 
 def kv_compact(k_stage, v_stage, k_cache, v_cache, Hkv, D, block_table, ctx_start, accepted, cu_rows):

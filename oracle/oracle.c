@@ -647,3 +647,40 @@ int oracle_ngram_draft(const int32_t *hist, int len, int W, const int32_t *pad, 
         out[c] = pad[c];
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * 7. margin-gated re-check
+ *
+ * [T] "Why the math checks out and the text still flips" (MarginGate: only the
+ * steps whose top-2 margin is small can flip) and "What the big servers offer
+ * and what it costs" (re-check only the uncertain steps).  The pages give the
+ * idea, not a rule.  Reading: a row's logits come from a fast evaluation whose
+ * every entry lies within err[r] of the invariant evaluation's; the row is
+ * re-checked unless its top-2 margin exceeds 2 err[r] -- then no other entry can
+ * reach the top one in the invariant logits, so both argmaxes agree.
+ *
+ * For each row r of logits [R][V] (fp32): top = the largest entry (lowest index
+ * on ties), margin = top value - the largest value at any other index (0 on a
+ * tie), recheck = (margin <= 2 err[r]).  Returns the number of rows flagged.
+ * ------------------------------------------------------------------------- */
+int oracle_margin_gate(const float *logits, int R, int V, const double *err, int32_t *top, double *margin,
+                       uint8_t *recheck)
+{
+    int n = 0;
+    for (int r = 0; r < R; ++r) {
+        const float *row = logits + (size_t)r * V;
+        int best = 0;
+        for (int v = 1; v < V; ++v)
+            if (row[v] > row[best])
+                best = v;
+        double second = -INFINITY;
+        for (int v = 0; v < V; ++v)
+            if (v != best && (double)row[v] > second)
+                second = (double)row[v];
+        top[r] = best;
+        margin[r] = V > 1 ? (double)row[best] - second : INFINITY;
+        recheck[r] = margin[r] <= 2.0 * err[r] ? 1 : 0;
+        n += recheck[r];
+    }
+    return n;
+}
