@@ -120,6 +120,22 @@ spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
                          void *workspace, size_t ws_bytes,
                          int32_t *dev_err, spec_stream_t stream);
 
+/* The same product for a column count known only on the device: the first
+ * c = min(n_cols, *dev_cols) columns of x when *dev_cols >= min_cols, else
+ * nothing (y untouched).  dev_cols (device int32) is read after the preceding
+ * kernel on the stream has finished, so a kernel just before may write it; the
+ * call launches the same kernels whatever the count, which lets a captured CUDA
+ * graph re-evaluate a data-dependent number of rows.  n_cols is the most the
+ * call may compute (it sizes the workspace and the passes); every other
+ * argument and the arithmetic are those of spec_qmatmul, so a column's bits do
+ * not depend on the count. */
+spec_status spec_qmatmul_devcols(const uint8_t *wq, const uint16_t *ws, int N, int K,
+                                 const uint16_t *x, int n_cols, int ldx,
+                                 void *y, spec_dtype y_dt, int ldy, int accumulate,
+                                 const int32_t *dev_cols, int min_cols,
+                                 void *workspace, size_t ws_bytes,
+                                 int32_t *dev_err, spec_stream_t stream);
+
 /* The same product with two-level (super-block) scales.  The pages name
  * two-level formats -- tokenstrom.com, "'Lossless,' but not quite", section
  * "Why the math checks out and the text still flips" (Q4_K / Q6_K); ramgpt.org,
@@ -359,15 +375,54 @@ spec_status spec_commit_accepted(int32_t *hist, int hist_cap, int32_t *hist_len,
                                  int32_t *ctx, int S, int32_t *dev_err, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Test hook: spec_qmatmul with an explicit column-tile width nt in {1, 2, 10}
- * (columns per pass = 8 nt; the workspace must hold T * (1 + ceil(K/512))
- * * 128 * 8 nt floats after 256-byte-rounded T int counters, T = ceil(N/128),
- * and for nt = 10 another K/256 * 43520 bytes of packed activations).  The result of every column must not depend on
- * nt; the tests use this to show it.  y_dt is SPEC_F32.
+ * Test hook: spec_qmatmul with an explicit column-tile width nt in {1, 2, 10,
+ * 11} (columns per pass = 8 nt, 80 for 11; nt = 10 runs the 80-column pass on
+ * the mma.sync kernel, nt = 11 on the tcgen05 kernel; the workspace must hold
+ * T * (1 + ceil(K/512)) * 128 * 8 nt' floats after 256-byte-rounded T int
+ * counters, T = ceil(N/128), nt' = min(nt, 10), and for nt >= 10 another
+ * K/256 * 43520 bytes of packed activations).  The result of every column must
+ * not depend on nt; the tests use this to show it.  y_dt is SPEC_F32.
  * ---------------------------------------------------------------------- */
 spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,
                                   int n_cols, int ldx, float *y, int ldy, int nt,
                                   void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Margin-gated re-check of the LM head
+ *
+ * tokenstrom.com, "'Lossless,' but not quite", section "Why the math checks
+ * out and the text still flips" (only steps whose top-2 margin is small can
+ * flip) and section "What the big servers offer and what it costs" (re-check
+ * only the uncertain steps).  `logits` [R][V] fp32 come from a fast evaluation
+ * (e.g. spec_qmatmul_noninvariant) of y = W x_r whose entries differ from the
+ * invariant evaluation's (spec_qmatmul) by at most err_r = err_coef *
+ * ||x_r||_1 (x_r: the bf16 row of `x` [R][ldx], H entries; err_coef is the
+ * caller's summation-order bound for its matrix).  For each row:
+ *   top[r]   = argmax of logits[r] (lowest index on ties; NaN never wins and
+ *              sets SPEC_DEVERR_NAN);
+ *   flagged  unless top-2 margin > 2 err_r (a tie is always flagged).
+ * A row not flagged has the invariant evaluation's argmax.  The flagged rows
+ * are listed in row order: rows[0 .. min(count, capacity)) (device int32),
+ * their activations copied to x_gathered [capacity][H] bf16; *count = the
+ * number flagged, *overflow = R when it exceeds capacity, else 0 (device
+ * int32 each).  Re-evaluate with spec_qmatmul_devcols(x_gathered, n_cols =
+ * capacity, dev_cols = count) into y_gathered [capacity][V], copy those rows
+ * back with spec_gate_scatter, and (for overflow) spec_qmatmul_devcols over all
+ * R rows with dev_cols = overflow, min_cols = 1.  The result: every row's
+ * argmax equals the invariant argmax, with a fixed launch sequence.
+ *   V % 4 == 0, H % 8 == 0, ldx % 8 == 0; logits, x, x_gathered, workspace
+ *   16-byte aligned; workspace >= spec_margin_gate_workspace(R, V) bytes.
+ * ---------------------------------------------------------------------- */
+size_t spec_margin_gate_workspace(int R, int V);
+spec_status spec_margin_gate(const float *logits, int V, int R, const uint16_t *x, int H, int ldx, float err_coef,
+                             int32_t *top, int32_t *rows, int32_t *count, int32_t *overflow, int capacity,
+                             uint16_t *x_gathered, void *workspace, size_t ws_bytes, int32_t *dev_err,
+                             spec_stream_t stream);
+
+/* Copies y_gathered[s] ([capacity][V] fp32) into logits[rows[s]] for s <
+ * min(*count, capacity) (count, rows: device int32 from spec_margin_gate). */
+spec_status spec_gate_scatter(const float *y_gathered, int V, const int32_t *rows, const int32_t *count,
+                              int capacity, float *logits, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Test hook for the bounded-wait error path (the pages have no counterpart:

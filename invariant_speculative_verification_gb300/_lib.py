@@ -56,6 +56,12 @@ _SIGS = {
     "spec_ngram_draft": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "spec_commit_accepted": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
     "spec_debug_wait_timeout": (_i32, [ctypes.c_uint32, _vp, _vp]),
+    "spec_qmatmul_devcols": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _sz,
+                                    _vp, _vp]),
+    "spec_margin_gate_workspace": (_sz, [_i32, _i32]),
+    "spec_margin_gate": (_i32, [_vp, _i32, _i32, _vp, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _sz, _vp,
+                                _vp]),
+    "spec_gate_scatter": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp]),
 }
 
 _lib = None
@@ -129,6 +135,29 @@ def spec_qmatmul(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, workspa
     _check("spec_qmatmul", load().spec_qmatmul(_ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx, _ptr(y), y_dt, ldy,
                                                int(accumulate), _ptr(workspace), int(ws_bytes), _ptr(dev_err),
                                                _stream(stream)))
+
+
+def spec_qmatmul_devcols(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, dev_cols, min_cols, workspace,
+                         ws_bytes, dev_err=None, stream=None):
+    _check("spec_qmatmul_devcols", load().spec_qmatmul_devcols(
+        _ptr(wq), _ptr(ws), N, K, _ptr(x), n_cols, ldx, _ptr(y), y_dt, ldy, int(accumulate), _ptr(dev_cols),
+        int(min_cols), _ptr(workspace), int(ws_bytes), _ptr(dev_err), _stream(stream)))
+
+
+def spec_margin_gate_workspace(R, V) -> int:
+    return int(load().spec_margin_gate_workspace(R, V))
+
+
+def spec_margin_gate(logits, V, R, x, H, ldx, err_coef, top, rows, count, overflow, capacity, x_gathered, workspace,
+                     ws_bytes, dev_err=None, stream=None):
+    _check("spec_margin_gate", load().spec_margin_gate(
+        _ptr(logits), V, R, _ptr(x), H, ldx, float(err_coef), _ptr(top), _ptr(rows), _ptr(count), _ptr(overflow),
+        int(capacity), _ptr(x_gathered), _ptr(workspace), int(ws_bytes), _ptr(dev_err), _stream(stream)))
+
+
+def spec_gate_scatter(y_gathered, V, rows, count, capacity, logits, stream=None):
+    _check("spec_gate_scatter", load().spec_gate_scatter(_ptr(y_gathered), V, _ptr(rows), _ptr(count), int(capacity),
+                                                         _ptr(logits), _stream(stream)))
 
 
 def spec_qmatmul_sb(wq, sbr, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, workspace, ws_bytes, dev_err=None,

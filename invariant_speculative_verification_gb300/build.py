@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libspec.so")
-SOURCES = ["abi.cu", "qmatmul.cu", "attention.cu", "verify.cu", "glue.cu"]
+SOURCES = ["abi.cu", "qmatmul.cu", "qmatmul_tc.cu", "attention.cu", "verify.cu", "glue.cu", "gate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-Wno-deprecated-gpu-targets"]

@@ -85,6 +85,8 @@ namespace dev {
 
 // Bound on the number of try_wait polls of one mbarrier phase.  try_wait
 // suspends for a hardware-defined interval per poll, so this is seconds.
+// (An explicit suspend-time hint made waits on completed phases ~50 % slower
+// and did not speed the kernels up.)
 constexpr uint32_t kMaxPolls = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -197,6 +199,18 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
 
+// s_i = fma(d, p_i + c_i, s_i) for i = 0, 1 with one packed add and one packed
+// fma (add.rn.f32x2 / fma.rn.f32x2: each lane an IEEE-rounded fp32 operation,
+// bit-identical to the scalar instructions, at half the issue count).
+__device__ __forceinline__ void fma_add_f32x2(float &s0, float &s1, float d, float p0, float p1, float c0,
+                                              float c1) {
+    asm("{\n\t.reg .b64 p, c, t, dd, s;\n\t"
+        "mov.b64 p, {%2, %3};\n\tmov.b64 c, {%4, %5};\n\tmov.b64 dd, {%6, %6};\n\tmov.b64 s, {%0, %1};\n\t"
+        "add.rn.f32x2 t, p, c;\n\tfma.rn.f32x2 s, dd, t, s;\n\tmov.b64 {%0, %1}, s;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(p0), "f"(p1), "f"(c0), "f"(c1), "f"(d));
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -266,9 +280,13 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// One arrival on `bar` once every tcgen05 operation this thread issued so far has completed.
+// One arrival on `bar` once every tcgen05 operation issued so far by the
+// issuing thread has completed.  Executed by a whole warp with warp-uniform
+// operands; one elected lane issues it.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t"
+                 "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+                 ::"r"(smem_u32(bar))
                  : "memory");
 }
 
@@ -288,12 +306,16 @@ __host__ __device__ constexpr uint32_t mma_idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D (TMEM, fp32) = A (TMEM, bf16) x B (shared memory, bf16) + (accumulate ? D : 0); issued by one thread.
+// D (TMEM, fp32) = A (TMEM, bf16) x B (shared memory, bf16) + (accumulate ? D : 0).
+// Executed by a whole warp with warp-uniform operands; one elected lane issues
+// the MMA.  (Issued from a single lane in a divergent branch, one MMA measured
+// ~67 cycles on this GPU whatever N; issued this way, 40 cycles at M = 128,
+// N = 80, K = 16 and 28 at N = 16.)
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
                                                 uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        "{\n\t.reg .pred p, q;\n\telect.sync _|p, 0xffffffff;\n\tsetp.ne.b32 q, %4, 0;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n\t}"
         ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -304,6 +326,34 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d, uint32_t a, uint64_t
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                 "%13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                  : "r"(taddr)
                  : "memory");
 }

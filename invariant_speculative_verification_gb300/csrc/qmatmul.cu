@@ -7,11 +7,12 @@
 //  * K is cut into segments of 512 (when K / 256 is odd the last segment is
 //    256 long).  The cut depends on K only.
 //  * Inside a segment, for every 32-k block b in ascending order, the block
-//    partial P_b is one chain of two m16n8k16 bf16 MMAs whose A operand is the
-//    code c = q + 8 plus 128 (exactly representable) and whose C operand starts
-//    at -136 * sum_{k in b} x[j][k] (column j's block sum in fp32, its four
-//    8-k chunks summed in k order and then in chunk order), so P_b = sum q x up
-//    to MMA rounding; then s = fma(d_b, P_b, s) with s starting at +0.
+//    product T_b is one chain of two m16n8k16 bf16 MMAs from a zero
+//    accumulator whose A operand is the code c = q + 8 plus 128 (exactly
+//    representable); the block partial is P_b = T_b + (-136 * sum_{k in b}
+//    x[j][k]) in fp32 (column j's block sum in fp32, its four 8-k chunks
+//    summed in k order and then in chunk order), so P_b = sum q x up to
+//    rounding; then s = fma(d_b, P_b, s) with s starting at +0.
 //  * The segment sums are folded in ascending order: y = ((s_0 + s_1) + s_2)...
 // The MMA instruction stream is the same for every column tile and column j's
 // result depends only on A, on B column j and on C column j; unused columns
@@ -34,8 +35,8 @@
 // only the delivery changes, not the arithmetic); its activations are packed
 // into that same layout once per call by xpack_kernel and copied in with the
 // stage by one cp.async.bulk.  Consumers issue only ldmatrix, 4 LOP3 + 3
-// shifts per 8 weights, lds and mma.sync.  A tile covered by one CTA is folded
-// in registers and written directly.  A tile shared by several CTAs: the CTAs
+// shifts per 8 weights, lds, mma.sync and the FADD/FFMA of each block partial.
+// A tile covered by one CTA is folded in registers and written directly.  A tile shared by several CTAs: the CTAs
 // holding its later segments store their segment sums and count themselves
 // in, without waiting; the CTA holding the leading segments folds them in
 // segment order once all have arrived (the usual case when it gets there),
@@ -49,21 +50,14 @@
 // "Quantized Matrix Multiplication Shows the Same Class of Failure".
 #include <mutex>
 
-#include "common.cuh"
+#include "qmm_shared.cuh"
 
 namespace {
+using namespace qmm;
 
-constexpr int SEG_K = 512;                   // k per K-segment (the invariant reduction unit)
-constexpr int BM = 128;                      // weight rows per tile
 constexpr int NCW = 8;                       // consumer warps (16 rows each)
 constexpr int W_BOX = BM * 128;              // one 128-row x 128-byte code box (256 k)
 constexpr int MAX_NT = 10;                   // column tiles per pass (80 columns)
-constexpr int SMEM_BUDGET = 226 * 1024;
-// Arrival counters of a call lie in the workspace's first 4 x tiles bytes; no
-// call has more than CNT_LIMIT / 4 tiles.  A call's stored sums and prefixes
-// that lie below CNT_LIMIT are cleared once read, so every call finds its
-// counters at zero whatever calls of other shapes used the workspace before.
-constexpr size_t CNT_LIMIT = 64 * 1024;
 
 // Narrow passes (<= 16 columns) stream 512-k stages and prepare each stage's
 // activations in the CTA (two activation warps).  The 80-column pass uses
@@ -71,11 +65,6 @@ constexpr size_t CNT_LIMIT = 64 * 1024;
 // once per call by a small kernel (xpack_kernel) into the workspace, in the
 // very byte layout of a stage, and each stage's part is copied in by TMA.
 // The stage size only changes how a segment is delivered, never its arithmetic.
-// Scale formats: SC_BLOCK = one fp16 scale per 32-k block ([N][K/32]);
-// SC_SUPER = per 256-k super-block an 8-byte record of eight 6-bit block scales
-// and an fp16 super-scale, records in 16-byte pairs per row ([N][ceil(K/512) 16]
-// bytes); block b's scale is D * s_(b mod 8), formed exactly in fp32.
-constexpr int SC_BLOCK = 0, SC_SUPER = 1;
 
 template <int NT, int FMT = SC_BLOCK>
 struct Cfg {
@@ -106,16 +95,6 @@ struct Cfg {
 // 32-k blocks per stage of a pass with nt column tiles (the scale box width)
 inline int stage_blocks(int nt) { return nt >= MAX_NT ? Cfg<MAX_NT>::NBLK : nt == 2 ? Cfg<2>::NBLK : Cfg<1>::NBLK; }
 
-// number of K-segments of length seg_k (the last may be shorter)
-inline int n_segments(int K, int seg_k) { return (K + seg_k - 1) / seg_k; }
-
-struct Sched {
-    int G;          // CTAs
-    long long U;    // units = tiles * ks
-    int ks, tiles, seg_st;   // segments, tiles, stages per segment
-    __device__ long long begin(int c) const { return (long long)c * U / G; }
-    __device__ int cta_of(long long u) const { return (int)(((u + 1) * G - 1) / U); }
-};
 
 // nibble codes (k = 8t .. 8t+7 of a block) -> (128 + code_m, 128 + code_{m+4}), exact
 __device__ __forceinline__ void codes_to_bf16(uint32_t w, uint32_t (&o)[4]) {
@@ -179,10 +158,12 @@ __device__ __forceinline__ void put_pair(const uint4 (&v)[4], int blk, int c, ui
 // layout of a stage's activation and block-sum areas.
 template <int NT>
 __global__ void __launch_bounds__(256) xpack_kernel(const uint16_t *__restrict__ x, int ldx, int K, int n_cols, int col0,
-                                                    uint8_t *__restrict__ out) {
+                                                    uint8_t *__restrict__ out, const int32_t *dev_cols, int min_cols) {
     using C = Cfg<NT>;
     dev::pdl_wait();   // x is the preceding kernel's output; out may still be read by it
     dev::pdl_launch_dependents();
+    if (dev_cols) n_cols = gated_cols(n_cols, dev_cols, min_cols);
+    if (col0 >= n_cols) return;
     constexpr int PAIRS = C::NBLK * 8 * NT;   // per stage
     const long long p = blockIdx.x * 256ll + threadIdx.x;
     const int st = (int)(p / PAIRS), pr = (int)(p % PAIRS);
@@ -203,8 +184,15 @@ __global__ void __launch_bounds__(Cfg<NT, FMT>::THREADS, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ts,
            const uint16_t *__restrict__ x, int ldx, int N, int K, int n_cols, int col0, void *__restrict__ y, int ldy,
            int accumulate, Sched sch, float *__restrict__ wsp_prefix, float *__restrict__ wsp_seg,
-           int *__restrict__ counters, const uint8_t *__restrict__ xpk, int32_t *dev_err) {
+           int *__restrict__ counters, const uint8_t *__restrict__ xpk, int32_t *dev_err, const int32_t *dev_cols,
+           int min_cols) {
     using C = Cfg<NT, FMT>;
+    if (dev_cols) {
+        // the column count is the preceding kernel's output: no early streaming
+        dev::pdl_wait();
+        n_cols = gated_cols(n_cols, dev_cols, min_cols);
+    }
+    if (col0 >= n_cols) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NS * C::STAGE);
@@ -531,14 +519,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                             asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
                                          : "=f"(c0), "=f"(c1)
                                          : "r"(cbase + (blk * 8 * NT + ct * 8 + 2 * t) * 4));
-                            const float cinit[4] = {c0, c1, c0, c1};
+                            const float zero[4] = {0.f, 0.f, 0.f, 0.f};
                             float p[4];
-                            dev::mma_bf16(p, ar[0], ar8[0], ar[1], ar8[1], b00, b01, cinit);
+                            dev::mma_bf16(p, ar[0], ar8[0], ar[1], ar8[1], b00, b01, zero);
                             dev::mma_bf16(p, ar[2], ar8[2], ar[3], ar8[3], b10, b11, p);
-                            acc[ct][0] = fmaf(d_r, p[0], acc[ct][0]);
-                            acc[ct][1] = fmaf(d_r, p[1], acc[ct][1]);
-                            acc[ct][2] = fmaf(d_r8, p[2], acc[ct][2]);
-                            acc[ct][3] = fmaf(d_r8, p[3], acc[ct][3]);
+                            dev::fma_add_f32x2(acc[ct][0], acc[ct][1], d_r, p[0], p[1], c0, c1);
+                            dev::fma_add_f32x2(acc[ct][2], acc[ct][3], d_r8, p[2], p[3], c0, c1);
                         }
                     }
                 }
@@ -652,36 +638,23 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
 template <int NT, bool OUT_BF16, int FMT>
 spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N, int K,
                       int n_cols, int col0, void *y, int ldy, int accumulate, int seg512, void *workspace,
-                      int32_t *dev_err, cudaStream_t stream) {
+                      int32_t *dev_err, const int32_t *dev_cols, int min_cols, cudaStream_t stream) {
     using C = Cfg<NT, FMT>;
     auto kern = qmm_kernel<NT, OUT_BF16, FMT>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return spec::cuda_status(e, "cudaFuncSetAttribute(qmm smem)");
-        configured = true;
-    }
+    static spec::SmemOptIn opt_in;
+    spec_status so = spec::smem_opt_in(kern, C::SMEM, opt_in, "cudaFuncSetAttribute(qmm smem)");
+    if (so != SPEC_OK) return so;
     const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
-    Sched sch;
-    sch.seg_st = seg512 * (SEG_K / C::KS);
-    sch.ks = n_segments(K, seg512 * SEG_K);
-    sch.tiles = (N + BM - 1) / BM;
-    sch.U = (long long)sch.tiles * sch.ks;
-    sch.G = (int)(sch.U < sms ? sch.U : sms);
-    // Nearly one tile per SM: one whole tile per CTA costs at most 15 % more work
-    // per CTA than an even split and removes every split tile's publish and fold.
-    if (sch.ks > 1 && sch.tiles <= sms && (long long)sch.tiles * 100 >= 85ll * sms) sch.G = sch.tiles;
-    const size_t tiles = (size_t)sch.tiles;
-    const size_t cnt_bytes = ((tiles * sizeof(int)) + 255) & ~size_t(255);
-    int *counters = reinterpret_cast<int *>(workspace);
-    float *prefix = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + cnt_bytes);
-    float *segs = prefix + tiles * BM * 8 * NT;
-    const uint8_t *xpk = reinterpret_cast<const uint8_t *>(segs + tiles * sch.ks * BM * 8 * NT);
+    const Sched sch = make_sched(N, K, seg512, C::KS, sms);
+    const WsLayout wl = ws_layout(workspace, sch.tiles, sch.ks, BM * 8 * NT);
+    int *counters = wl.counters;
+    float *prefix = wl.prefix, *segs = wl.segs;
+    const uint8_t *xpk = wl.xpk;
     if constexpr (C::XPACK) {
         // this pass's activations, packed once for every CTA (into the workspace after the partial sums)
         const long long pairs = (long long)(K / C::KS) * C::NBLK * 8 * NT;
         cudaError_t e = spec::launch_pdl(xpack_kernel<NT>, dim3((unsigned)((pairs + 255) / 256)), dim3(256), 0, stream,
-                                         x, ldx, K, n_cols, col0, const_cast<uint8_t *>(xpk));
+                                         x, ldx, K, n_cols, col0, const_cast<uint8_t *>(xpk), dev_cols, min_cols);
         if (e != cudaSuccess) return spec::cuda_status(e, "qmm activation pack launch");
     }
     cudaLaunchConfig_t cfg = {};
@@ -695,8 +668,16 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, sch, prefix,
-                                       segs, counters, xpk, dev_err);
+                                       segs, counters, xpk, dev_err, dev_cols, min_cols);
     return spec::cuda_status(e, "qmm launch");
+}
+
+// The 80-column pass runs on the tcgen05 kernel when every SM gets at least two units.
+constexpr int WIDE_AUTO = 0, WIDE_TC = 1, WIDE_MMA_SYNC = 2;
+bool tc_wide_preferred(int N, int K, int seg512) {
+    const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
+    const long long units = (long long)((N + BM - 1) / BM) * n_segments(K, seg512 * SEG_K);
+    return units >= 2ll * sms;
 }
 
 int pass_nt(int n_cols) { return n_cols <= 8 ? 1 : (n_cols <= 16 ? 2 : MAX_NT); }
@@ -714,7 +695,8 @@ inline int super_pitch(int K) { return (K + 511) / 512 * 16; }
 
 spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
                     void *y, spec_dtype y_dt, int ldy, int accumulate, int seg512, int nt, void *workspace,
-                    int32_t *dev_err, cudaStream_t stream, int fmt = SC_BLOCK) {
+                    int32_t *dev_err, cudaStream_t stream, int fmt = SC_BLOCK, const int32_t *dev_cols = nullptr,
+                    int min_cols = 0, int wide = WIDE_AUTO) {
     CUtensorMap tw, ts;
     {
         uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)N};
@@ -746,9 +728,9 @@ spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint1
         spec_status st;
 #define SPEC_QMM_FMT(NTV, FMTV)                                                                                    \
     st = bf ? launch_nt<NTV, true, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err,    \
-                                         stream)                                                                      \
+                                         dev_cols, min_cols, stream)                                                  \
             : launch_nt<NTV, false, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace,    \
-                                          dev_err, stream)
+                                          dev_err, dev_cols, min_cols, stream)
 #define SPEC_QMM_CASE(NTV)                                                                                         \
     if (fmt == SC_BLOCK) {                                                                                         \
         SPEC_QMM_FMT(NTV, SC_BLOCK);                                                                              \
@@ -758,7 +740,15 @@ spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint1
         switch (nt) {
         case 1: SPEC_QMM_CASE(1); break;
         case 2: SPEC_QMM_CASE(2); break;
-        default: SPEC_QMM_CASE(MAX_NT);
+        default:
+            // the 80-column pass: block-fp16 scales on the 5th-generation tensor cores when the
+            // matrix gives every SM at least two (tile, segment) units; smaller matrices run the
+            // mma.sync pass, whose per-unit start-up is shorter.  Both give the same bits.
+            if (fmt == SC_BLOCK && (wide == WIDE_TC || (wide == WIDE_AUTO && tc_wide_preferred(N, K, seg512))))
+                st = tc_wide_pass(tw, ts, x, ldx, N, K, n_cols, col0, y, bf, ldy, accumulate, seg512, workspace,
+                                  dev_err, dev_cols, min_cols, stream);
+            else
+                SPEC_QMM_CASE(MAX_NT);
         }
 #undef SPEC_QMM_CASE
 #undef SPEC_QMM_FMT
@@ -813,6 +803,23 @@ extern "C" spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N
                    (cudaStream_t)stream);
 }
 
+extern "C" spec_status spec_qmatmul_devcols(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,
+                                            int n_cols, int ldx, void *y, spec_dtype y_dt, int ldy, int accumulate,
+                                            const int32_t *dev_cols, int min_cols, void *workspace, size_t ws_bytes,
+                                            int32_t *dev_err, spec_stream_t stream) {
+    spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
+    if (st != SPEC_OK) return st;
+    SPEC_CHECK_ARG(dev_cols, "qmatmul_devcols: dev_cols is NULL");
+    SPEC_CHECK_ARG(y_dt == SPEC_F32 || y_dt == SPEC_BF16, "qmatmul_devcols: y_dt must be SPEC_F32 or SPEC_BF16");
+    SPEC_CHECK_ARG(!(accumulate && y_dt != SPEC_F32), "qmatmul_devcols: accumulate needs SPEC_F32 output");
+    if (n_cols == 0) return SPEC_OK;
+    const int nt = pass_nt(n_cols);
+    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
+    if (st != SPEC_OK) return st;
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, nt, workspace, dev_err,
+                   (cudaStream_t)stream, SC_BLOCK, dev_cols, min_cols);
+}
+
 extern "C" spec_status spec_qmatmul_sb(const uint8_t *wq, const uint8_t *sbr, int N, int K, const uint16_t *x,
                                        int n_cols, int ldx, void *y, spec_dtype y_dt, int ldy, int accumulate,
                                        void *workspace, size_t ws_bytes, int32_t *dev_err, spec_stream_t stream) {
@@ -860,12 +867,15 @@ extern "C" spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *
                                              size_t ws_bytes, spec_stream_t stream) {
     spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
     if (st != SPEC_OK) return st;
-    SPEC_CHECK_ARG(nt == 1 || nt == 2 || nt == MAX_NT, "nt must be 1, 2 or 10");
+    SPEC_CHECK_ARG(nt == 1 || nt == 2 || nt == MAX_NT || nt == MAX_NT + 1, "nt must be 1, 2, 10 or 11");
     if (n_cols == 0) return SPEC_OK;
+    // 10: the 80-column pass on the mma.sync kernel, 11: on the tcgen05 kernel
+    const int wide = nt == MAX_NT + 1 ? WIDE_TC : WIDE_MMA_SYNC;
+    nt = nt > MAX_NT ? MAX_NT : nt;
     st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
     if (st != SPEC_OK) return st;
     return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, 1, nt, workspace, nullptr,
-                   (cudaStream_t)stream);
+                   (cudaStream_t)stream, SC_BLOCK, nullptr, 0, wide);
 }
 
 // ---------------------------------------------------------------------------
@@ -875,8 +885,6 @@ extern "C" spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
-constexpr int kMaxDevices = 64;
-
 // One scratch area per device (module-scope __device__ storage is per device).
 // Its front holds the per-tile arrival counters, which must be zero when a
 // launch starts; the rest holds partial sums that each call writes before it
@@ -884,7 +892,7 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_qmm_static_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+void *g_scratch_ptr[spec::kMaxDevices] = {};
 
 // Device address of this device's scratch; looked up on the first call made
 // with that device current.
@@ -892,7 +900,7 @@ spec_status static_scratch(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return spec::cuda_status(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) return spec::fail(SPEC_ERR_INVALID_ARG, "qmatmul_static_scratch: device %d", dev);
+    if (dev < 0 || dev >= spec::kMaxDevices) return spec::fail(SPEC_ERR_INVALID_ARG, "qmatmul_static_scratch: device %d", dev);
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_ptr[dev]) {
         void *p = nullptr;

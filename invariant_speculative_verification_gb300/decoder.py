@@ -55,6 +55,15 @@ class Decoder:
         shape = (self.pages, self.Hkv, 16, self.D)
         self.k_cache = [torch.zeros(shape, dtype=torch.int16, device=device) for _ in range(cfg.layers)]
         self.v_cache = [torch.zeros(shape, dtype=torch.int16, device=device) for _ in range(cfg.layers)]
+        # the LM head's summation-order bound per unit ||x||_1 (margin gate): two fp32
+        # evaluations of its K/32 block terms differ by at most 2 gamma_(2n) sum |t_b|,
+        # n = K/32, and |t_b| <= 9 max|d| ||x_b||_1 (|q| <= 8 plus rounding)
+        n_blk = cfg.hidden // 32
+        u = 2.0 ** -24
+        gamma = 2 * n_blk * u / (1 - 2 * n_blk * u)
+        d_max = float(np.abs(np.asarray(weights.lm[1], np.uint16).view(np.float16).astype(np.float64)).max())
+        self.gate_coef = 2 * gamma * 9 * d_max
+        self.gate = None
         self.rope = torch.empty((max_len, self.D // 2, 2), dtype=torch.float32, device=device)
         L.spec_rope_table(self.rope, max_len, self.D, cfg.rope_theta)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -115,12 +124,44 @@ class Decoder:
                        self.qws, self.qws_bytes, self.dev_err)
         tr("down")
 
+    def enable_gate(self, capacity: int = 16):
+        """Evaluate the LM head through the margin gate (tokenstrom.com, "'Lossless,'
+        but not quite", sections "Why the math checks out and the text still flips"
+        and "What the big servers offer and what it costs"): fast non-invariant
+        logits, then an invariant re-evaluation of only the rows whose top-2 margin
+        is within twice the summation-order bound (all rows when more than
+        `capacity` are).  Every row's argmax equals the invariant argmax."""
+        d, R, H, V = self.device, self.max_rows, self.H, self.V
+        cap = max(1, min(capacity, R))
+        g = {"cap": cap}
+        g["ws_bytes"] = L.spec_margin_gate_workspace(R, V)
+        g["ws"] = torch.empty(g["ws_bytes"] // 4 + 16, dtype=torch.float32, device=d)
+        g["top"] = torch.zeros(R, dtype=torch.int32, device=d)
+        g["rows"] = torch.zeros(cap, dtype=torch.int32, device=d)
+        g["count"] = torch.zeros(1, dtype=torch.int32, device=d)
+        g["overflow"] = torch.zeros(1, dtype=torch.int32, device=d)
+        g["xg"] = torch.zeros((cap, H), dtype=torch.int16, device=d)
+        g["yg"] = torch.zeros((cap, V), dtype=torch.float32, device=d)
+        self.gate = g
+
     def head(self, R, trace=None):
         L.spec_add_rmsnorm(self.h, None, self.final_norm, R, self.H, self.cfg.eps, self.a)
         if trace:
             trace("final_norm")
-        L.spec_qmatmul(self.lm[0], self.lm[1], self.V, self.H, self.a, R, self.H, self.logits, L.SPEC_F32,
-                       self.V, 0, self.qws, self.qws_bytes, self.dev_err)
+        if self.gate is None:
+            L.spec_qmatmul(self.lm[0], self.lm[1], self.V, self.H, self.a, R, self.H, self.logits, L.SPEC_F32,
+                           self.V, 0, self.qws, self.qws_bytes, self.dev_err)
+            return
+        g, H, V = self.gate, self.H, self.V
+        L.spec_qmatmul_noninvariant(self.lm[0], self.lm[1], V, H, self.a, R, H, self.logits, V, 0, self.qws,
+                                    self.qws_bytes)
+        L.spec_margin_gate(self.logits, V, R, self.a, H, H, self.gate_coef, g["top"], g["rows"], g["count"],
+                           g["overflow"], g["cap"], g["xg"], g["ws"], g["ws_bytes"], self.dev_err)
+        L.spec_qmatmul_devcols(self.lm[0], self.lm[1], V, H, g["xg"], g["cap"], H, g["yg"], L.SPEC_F32, V, 0,
+                               g["count"], 1, self.qws, self.qws_bytes, self.dev_err)
+        L.spec_gate_scatter(g["yg"], V, g["rows"], g["count"], g["cap"], self.logits)
+        L.spec_qmatmul_devcols(self.lm[0], self.lm[1], V, H, self.a, R, H, self.logits, L.SPEC_F32, V, 0,
+                               g["overflow"], 1, self.qws, self.qws_bytes, self.dev_err)
 
     def forward(self, tokens, cu_rows, ctx, S, R, max_kv_len=None):
         """Logits (fp32 [R][V], in self.logits) for a ragged verify batch whose rows

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from tests.gpu_util import TOL, bf16_rounding_ok, bits_to_f64, host, rel_err_rows
+from tests.gpu_util import TOL, bf16_rounding_ok, bf16_rounding_report, bits_to_f64, host, rel_err_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -108,7 +108,7 @@ def test_layer_steps_and_logits_match_oracle(cfg, P, layers):
                 ref = oracle.rope(v, r, cfg.rope_theta)
                 slack = 1e-6 * (np.abs(v) + np.abs(np.roll(v, D // 2))) + 1e-30
                 got = snap["q"][r, hh] if hh < Hq else snap["k"][r // 16, hh - Hq, r % 16]
-                assert bf16_rounding_ok(got, ref, slack), (li, "rope", r, hh)
+                assert bf16_rounding_ok(got, ref, slack), (li, "rope", r, hh, bf16_rounding_report(got, ref, slack))
             vv = qkv[r, (Hq + Hkv) * D:]
             for kh in range(Hkv):
                 assert bf16_rounding_ok(snap["v"][r // 16, kh, r % 16], vv[kh * D:(kh + 1) * D], 0.0), (li, "v", r)

@@ -12,7 +12,7 @@ misreadings' own closed forms.
 
 Source: ramgpt.org, "When Lossless Speculation Stops Being Lossless on
 Blackwell", section "Why Tiny Numerical Differences Can Change Entire
-Answers" (byte-identical output is judged on the decoder's result).
+Answers" (byte identity is a property of the decoder's output).
 """
 import math
 

@@ -52,7 +52,8 @@ def run(case_or_w, x_dev, n_cols, N, K, ldx=None, out_dt=0, y=None, accumulate=0
 
 def debug_nt_ws(N, K, nt):
     tiles = (N + 127) // 128
-    packed = (K // 256) * 43520 if nt == 10 else 0   # the 80-column pass's packed activations
+    packed = (K // 256) * 43520 if nt >= 10 else 0   # the 80-column pass's packed activations
+    nt = min(nt, 10)
     return ((tiles * 4 + 255) // 256) * 256 + tiles * (1 + (K + 511) // 512) * 128 * 8 * nt * 4 + packed
 
 
@@ -101,7 +102,7 @@ def test_column_placement_and_tile_width_do_not_change_bits(tiny):
             xs[pos] = probe[0]
             y = run(w, xs, n_cols, 512, 512)
             assert bits_equal(y[pos], ref), (n_cols, pos)
-            for nt in (1, 2, 10):
+            for nt in (1, 2, 10, 11):   # 10: 80-column pass on mma.sync, 11: on tcgen05
                 yy = torch.zeros((n_cols, 512), dtype=torch.float32, device="cuda")
                 wsp = workspace(debug_nt_ws(512, 512, nt))
                 L.spec_qmatmul_debug_nt(w[0], w[1], 512, 512, xs, n_cols, 512, yy, 512, nt, wsp, wsp.numel() * 4)
