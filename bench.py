@@ -599,6 +599,7 @@ def run_ours(args):
     sweep, qc, qp = qgemv_sweep(torch, L, hbm_peak)
     kernels = kernel_rooflines(torch, L, hbm_peak)
     kernels["qgemv_superblock"] = qgemv_superblock(torch, L, hbm_peak)
+    kernels["lm_head_gate"] = lm_head_gate(torch, L, w)
     ac, ap = attention_invariance(torch, L)
     inv_cases = qc + ac + N_SEQ
     inv_pass = qp + ap + equal_seqs
@@ -633,6 +634,50 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def lm_head_gate(torch, L, w):
+    """The LM head of one 80-row verify step, invariant against margin-gated (fast
+    non-invariant product, gate scan, invariant re-evaluation of up to 16 flagged rows,
+    scatter, and the all-rows fallback that runs only on overflow), each as a graph."""
+    from invariant_speculative_verification_gb300.decoder import margin_gate_coef
+    dev = torch.device("cuda")
+    cfg = w.cfg
+    R, H, V, cap = N_SEQ * (WIDTH + 1), cfg.hidden, cfg.vocab, 16
+    wq = torch.from_numpy(w.lm[0]).to(dev)
+    ws = torch.from_numpy(w.lm[1].view(np.int16)).to(dev)
+    a = torch.from_numpy(synth.activations_bf16(1009, R, H).view(np.int16)).to(dev)
+    logits = torch.zeros((R, V), dtype=torch.float32, device=dev)
+    qwb = L.spec_qmatmul_workspace(V, H, R)
+    qws = torch.zeros(qwb // 4 + 64, dtype=torch.int32, device=dev)
+    gwb = L.spec_margin_gate_workspace(R, V)
+    gws = torch.empty(gwb // 4 + 16, dtype=torch.float32, device=dev)
+    top = torch.zeros(R, dtype=torch.int32, device=dev)
+    rows = torch.zeros(cap, dtype=torch.int32, device=dev)
+    count = torch.zeros(1, dtype=torch.int32, device=dev)
+    over = torch.zeros(1, dtype=torch.int32, device=dev)
+    xg = torch.zeros((cap, H), dtype=torch.int16, device=dev)
+    yg = torch.zeros((cap, V), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    coef = margin_gate_coef(w.lm[1], H)
+
+    def invariant():
+        L.spec_qmatmul(wq, ws, V, H, a, R, H, logits, L.SPEC_F32, V, 0, qws, qwb, err)
+
+    def gated():
+        L.spec_qmatmul_noninvariant(wq, ws, V, H, a, R, H, logits, V, 0, qws, qwb)
+        L.spec_margin_gate(logits, V, R, a, H, H, coef, top, rows, count, over, cap, xg, gws, gwb, err)
+        L.spec_qmatmul_devcols(wq, ws, V, H, xg, cap, H, yg, L.SPEC_F32, V, 0, count, 1, qws, qwb, err)
+        L.spec_gate_scatter(yg, V, rows, count, cap, logits)
+        L.spec_qmatmul_devcols(wq, ws, V, H, a, R, H, logits, L.SPEC_F32, V, 0, over, 1, qws, qwb, err)
+
+    t_inv = graph_time(torch, invariant, 1, reps=20)
+    t_gate = graph_time(torch, gated, 1, reps=20)
+    gated()
+    torch.cuda.synchronize()
+    return {"workload": f"LM head {V}x{H}, {R} rows (bf16 N(0,1) inputs), capacity {cap}",
+            "invariant_us": round(t_inv * 1e6, 2), "gated_us": round(t_gate * 1e6, 2),
+            "rows_flagged": int(count.item()), "overflow": int(over.item()) > 0, "dev_err": int(err.item())}
 
 
 def qmatmul_step_roofline(torch, L, w, hbm_peak, peak_kind):
@@ -689,18 +734,34 @@ def qmatmul_step_roofline(torch, L, w, hbm_peak, peak_kind):
             "avg_launch_us": round(per_launch * 1e6, 2)}
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the kernel's device code: its .cu file and the headers it includes
+    from csrc/, with comments and blank space removed (a comment edit keeps it)."""
     import hashlib
+    csrc = os.path.join(ROOT, "invariant_speculative_verification_gb300", "csrc")
+    files = [f"{kernel}.cu", "qmm_shared.cuh", "common.cuh"]
+    h = hashlib.sha256()
+    for f in files:
+        p = os.path.join(csrc, f)
+        if not os.path.exists(p):
+            return ""
+        txt = open(p).read()
+        txt = re.sub(r"/\*.*?\*/", " ", txt, flags=re.S)
+        txt = re.sub(r"//[^\n]*", " ", txt)
+        h.update(" ".join(txt.split()).encode())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current device code (kernel_source_hash)."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
-    src = os.path.join(ROOT, "invariant_speculative_verification_gb300", "csrc", f"{kernel}.cu")
-    if not os.path.exists(p) or not os.path.exists(src):
+    if not os.path.exists(p):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     txt = open(p).read()
-    m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_sha = re.search(r"device_code_sha256_16:\s*([0-9a-f]+)", txt)
     m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)", txt)
-    if not m_sha or not m_b or m_sha.group(1) != sha:
+    if not m_sha or not m_b or m_sha.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_b.group(1))
 

@@ -672,13 +672,8 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     return spec::cuda_status(e, "qmm launch");
 }
 
-// The 80-column pass runs on the tcgen05 kernel when every SM gets at least two units.
+// Which kernel runs the 80-column pass (both give the same bits).
 constexpr int WIDE_AUTO = 0, WIDE_TC = 1, WIDE_MMA_SYNC = 2;
-bool tc_wide_preferred(int N, int K, int seg512) {
-    const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
-    const long long units = (long long)((N + BM - 1) / BM) * n_segments(K, seg512 * SEG_K);
-    return units >= 2ll * sms;
-}
 
 int pass_nt(int n_cols) { return n_cols <= 8 ? 1 : (n_cols <= 16 ? 2 : MAX_NT); }
 
@@ -741,10 +736,11 @@ spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint1
         case 1: SPEC_QMM_CASE(1); break;
         case 2: SPEC_QMM_CASE(2); break;
         default:
-            // the 80-column pass: block-fp16 scales on the 5th-generation tensor cores when the
-            // matrix gives every SM at least two (tile, segment) units; smaller matrices run the
-            // mma.sync pass, whose per-unit start-up is shorter.  Both give the same bits.
-            if (fmt == SC_BLOCK && (wide == WIDE_TC || (wide == WIDE_AUTO && tc_wide_preferred(N, K, seg512))))
+            // the 80-column pass: the mma.sync kernel unless the tcgen05 kernel is asked for.
+            // Both give the same bits; the tcgen05 kernel measured slower on every matrix of
+            // the decoder (its per-block accumulator round trip through tensor memory, with
+            // four accumulators in flight, sets its block rate), so it is not chosen by default.
+            if (fmt == SC_BLOCK && wide == WIDE_TC)
                 st = tc_wide_pass(tw, ts, x, ldx, N, K, n_cols, col0, y, bf, ldy, accumulate, seg512, workspace,
                                   dev_err, dev_cols, min_cols, stream);
             else

@@ -27,6 +27,18 @@ def _dev(a: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(a.copy()).to(device)
 
 
+def margin_gate_coef(scales, K: int) -> float:
+    """The margin gate's summation-order bound per unit ||x||_1 for an int4 block-32
+    matrix with fp16 scales `scales` (raw bits) and K inputs: two fp32 evaluations
+    of its n = K/32 block terms differ by at most 2 gamma_(2n) sum |t_b|, and
+    |t_b| <= 9 max|d| ||x_b||_1 (|q| <= 8, plus the rounding of the block partial)."""
+    n_blk = K // 32
+    u = 2.0 ** -24
+    gamma = 2 * n_blk * u / (1 - 2 * n_blk * u)
+    d_max = float(np.abs(np.asarray(scales, np.uint16).view(np.float16).astype(np.float64)).max())
+    return 2 * gamma * 9 * d_max
+
+
 class Decoder:
     """Device-resident decoder: weights, paged KV cache, activation buffers.
 
@@ -55,14 +67,7 @@ class Decoder:
         shape = (self.pages, self.Hkv, 16, self.D)
         self.k_cache = [torch.zeros(shape, dtype=torch.int16, device=device) for _ in range(cfg.layers)]
         self.v_cache = [torch.zeros(shape, dtype=torch.int16, device=device) for _ in range(cfg.layers)]
-        # the LM head's summation-order bound per unit ||x||_1 (margin gate): two fp32
-        # evaluations of its K/32 block terms differ by at most 2 gamma_(2n) sum |t_b|,
-        # n = K/32, and |t_b| <= 9 max|d| ||x_b||_1 (|q| <= 8 plus rounding)
-        n_blk = cfg.hidden // 32
-        u = 2.0 ** -24
-        gamma = 2 * n_blk * u / (1 - 2 * n_blk * u)
-        d_max = float(np.abs(np.asarray(weights.lm[1], np.uint16).view(np.float16).astype(np.float64)).max())
-        self.gate_coef = 2 * gamma * 9 * d_max
+        self.gate_coef = margin_gate_coef(weights.lm[1], cfg.hidden)
         self.gate = None
         self.rope = torch.empty((max_len, self.D // 2, 2), dtype=torch.float32, device=device)
         L.spec_rope_table(self.rope, max_len, self.D, cfg.rope_theta)
