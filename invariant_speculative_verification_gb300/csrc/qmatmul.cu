@@ -206,9 +206,9 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     const long long ua = sch.begin(blockIdx.x), ub = sch.begin(blockIdx.x + 1);
     constexpr int TILE_ELEMS = BM * 8 * NT;     // one tile's values for this pass
     // Partial sums in the workspace keep the accumulator fragments as the
-    // consumer threads hold them: [column tile][warp][lane][4] floats, so every
+    // consumer threads hold them: [fragment][warp][lane][4] floats, so every
     // store and load is a coalesced 16-byte access by the thread that owns it.
-    const int frag = ((warp * 32 + (threadIdx.x & 31)) * 4);   // + ct * NCW * 128
+    const int frag = ((warp * 32 + (threadIdx.x & 31)) * 4);   // + f * NCW * 128
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NS; ++s) {
@@ -356,7 +356,19 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     // ============================ consumers ============================
     dev::pdl_wait();   // y (accumulate), the workspace and y writes follow the preceding kernel
     const int r = lane >> 2, t = lane & 3;
-    const int wrow = warp * 16;
+    // A consumer warp owns RG 16-row groups x CT 8-column tiles (RG x CT = NT
+    // fragments f = rg * CT + ctl).  Narrow passes: one row group, all columns.
+    // The 80-column pass: 32 rows x 40 columns per warp, so that each activation
+    // fragment read from shared memory feeds two row groups' MMAs (with 16 rows
+    // x 80 columns the eight warps read 40 KB of activations per 32-k block).
+    // Which warp computes a fragment is scheduling: its operations are the same.
+    constexpr int RG = NT >= 10 ? 2 : 1;
+    constexpr int CT = NT / RG;
+    constexpr int RSLOTS = NCW / (NT >= 10 ? 2 : 1);   // warps along the rows
+    static_assert(RG * CT == NT && RSLOTS * 16 * RG == BM, "consumer mapping");
+    const int wrow0 = (warp % RSLOTS) * 16 * RG;         // row group rg starts at wrow0 + 16 rg
+    const int ctb = (warp / RSLOTS) * CT;                 // first column tile of this warp
+    auto fcol = [&](int f) { return col0 + (ctb + f % CT) * 8; };   // first column of fragment f
     const int g = lane >> 2;
     const int xcol = (g & 1) * 4 + (g >> 1);   // activation column of this lane's B fragment
     float yrun[NT][4];
@@ -379,11 +391,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             }
         };
 #pragma unroll
-        for (int ct = 0; ct < NT; ++ct) {
-            store_y(ct * 8 + t, wrow + r, yrun[ct][0]);
-            store_y(ct * 8 + t + 4, wrow + r, yrun[ct][1]);
-            store_y(ct * 8 + t, wrow + r + 8, yrun[ct][2]);
-            store_y(ct * 8 + t + 4, wrow + r + 8, yrun[ct][3]);
+        for (int f = 0; f < NT; ++f) {
+            const int c8 = (ctb + f % CT) * 8, wr = wrow0 + 16 * (f / CT);
+            store_y(c8 + t, wr + r, yrun[f][0]);
+            store_y(c8 + t + 4, wr + r, yrun[f][1]);
+            store_y(c8 + t, wr + r + 8, yrun[f][2]);
+            store_y(c8 + t + 4, wr + r + 8, yrun[f][3]);
         }
     };
     // yrun holds the fold of segments 0 .. seg_from-1 of `tile`: add the stored
@@ -407,7 +420,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             for (int q = 0; q < SG; ++q)
 #pragma unroll
                 for (int ct = 0; ct < NT; ++ct)
-                    l[q][ct] = (col0 + ct * 8 < n_cols)
+                    l[q][ct] = (fcol(ct) < n_cols)
                                    ? __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)(sg + q) * TILE_ELEMS +
                                                                              ct * NCW * 128))
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -424,7 +437,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
         for (; sg < ks; ++sg) {
 #pragma unroll
             for (int ct = 0; ct < NT; ++ct) {
-                if (col0 + ct * 8 < n_cols) {
+                if (fcol(ct) < n_cols) {
                     const float4 l = __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)sg * TILE_ELEMS +
                                                                              ct * NCW * 128));
                     yrun[ct][0] += l.x, yrun[ct][1] += l.y, yrun[ct][2] += l.z, yrun[ct][3] += l.w;
@@ -438,7 +451,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
         for (sg = seg_from; sg < ks; ++sg)
 #pragma unroll
             for (int ct = 0; ct < NT; ++ct)
-                clear_low(p0 + (size_t)sg * TILE_ELEMS + ct * NCW * 128, col0 + ct * 8 < n_cols);
+                clear_low(p0 + (size_t)sg * TILE_ELEMS + ct * NCW * 128, fcol(ct) < n_cols);
     };
 
     while (u < ub) {
@@ -465,52 +478,66 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                 const uint32_t xbase = wbase + C::X_OFF;
                 const uint32_t sbase = wbase + C::S_OFF;
                 const uint32_t cbase = wbase + C::CI_OFF;
-                // super-block scales: rows r and r+8's record pair of this stage (a 512-k stage
-                // uses both records, a 256-k stage the one its k offset selects)
-                uint2 rec_r[2] = {}, rec_r8[2] = {};
+                // super-block scales: rows r and r+8's record pair of this stage, per row group
+                // (a 512-k stage uses both records, a 256-k stage the one its k offset selects)
+                uint2 rec_r[RG][2] = {}, rec_r8[RG][2] = {};
                 int rsel = 0;
                 if constexpr (FMT == SC_SUPER) {
-                    const uint2 *pr = reinterpret_cast<const uint2 *>(smem + s * C::STAGE + C::S_OFF + (wrow + r) * 16);
-                    const uint2 *pr8 = pr + 16;   // 8 rows further on
-                    rec_r[0] = pr[0], rec_r[1] = pr[1], rec_r8[0] = pr8[0], rec_r8[1] = pr8[1];
+#pragma unroll
+                    for (int rg = 0; rg < RG; ++rg) {
+                        const uint2 *pr = reinterpret_cast<const uint2 *>(smem + s * C::STAGE + C::S_OFF +
+                                                                          (wrow0 + 16 * rg + r) * 16);
+                        const uint2 *pr8 = pr + 16;   // 8 rows further on
+                        rec_r[rg][0] = pr[0], rec_r[rg][1] = pr[1], rec_r8[rg][0] = pr8[0], rec_r8[rg][1] = pr8[1];
+                    }
                     rsel = ((((int)(u % ks) * seg_st + st) * C::KS) >> 8) & 1;
                 }
                 constexpr int BP_UNROLL = NT > 4 ? 1 : C::NBLK / 2;
 #pragma unroll BP_UNROLL
                 for (int bp = 0; bp < C::NBLK / 2; ++bp) {
-                    uint32_t wv[4];
-                    {
-                        // blocks 2bp, 2bp+1: box bp/4 (256 k each), 16-byte chunk (2bp + m/2) % 8
-                        const int m = lane >> 3, rr = lane & 7;
-                        const int row = wrow + (m & 1) * 8 + rr;
-                        const int blk = 2 * bp + (m >> 1);
-                        dev::ldmatrix_x4(wv[0], wv[1], wv[2], wv[3],
-                                         wbase + (blk >> 3) * W_BOX + row * 128 + (((blk & 7) ^ (row & 7)) << 4));
-                    }
-                    uint32_t s2 = 0, s28 = 0;   // the two fp16 scales of blocks 2bp, 2bp+1 for rows r and r+8
-                    if constexpr (FMT == SC_BLOCK) {
-                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(s2) : "r"(sbase + (wrow + r) * (2 * C::NBLK) + bp * 4));
-                        asm volatile("ld.shared.u32 %0, [%1];"
-                                     : "=r"(s28)
-                                     : "r"(sbase + (wrow + r + 8) * (2 * C::NBLK) + bp * 4));
+                    uint32_t wv[RG][4];
+                    uint32_t s2[RG] = {}, s28[RG] = {};   // fp16 scales of blocks 2bp, 2bp+1 for rows r and r+8
+#pragma unroll
+                    for (int rg = 0; rg < RG; ++rg) {
+                        const int wr = wrow0 + 16 * rg;
+                        {
+                            // blocks 2bp, 2bp+1: box bp/4 (256 k each), 16-byte chunk (2bp + m/2) % 8
+                            const int m = lane >> 3, rr = lane & 7;
+                            const int row = wr + (m & 1) * 8 + rr;
+                            const int blk = 2 * bp + (m >> 1);
+                            dev::ldmatrix_x4(wv[rg][0], wv[rg][1], wv[rg][2], wv[rg][3],
+                                             wbase + (blk >> 3) * W_BOX + row * 128 + (((blk & 7) ^ (row & 7)) << 4));
+                        }
+                        if constexpr (FMT == SC_BLOCK) {
+                            asm volatile("ld.shared.u32 %0, [%1];"
+                                         : "=r"(s2[rg])
+                                         : "r"(sbase + (wr + r) * (2 * C::NBLK) + bp * 4));
+                            asm volatile("ld.shared.u32 %0, [%1];"
+                                         : "=r"(s28[rg])
+                                         : "r"(sbase + (wr + r + 8) * (2 * C::NBLK) + bp * 4));
+                        }
                     }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int blk = 2 * bp + h;
-                        uint32_t ar[4], ar8[4];
-                        codes_to_bf16(wv[2 * h], ar);
-                        codes_to_bf16(wv[2 * h + 1], ar8);
-                        float d_r, d_r8;
-                        if constexpr (FMT == SC_BLOCK) {
-                            d_r = __half2float(__ushort_as_half((unsigned short)(s2 >> (16 * h))));
-                            d_r8 = __half2float(__ushort_as_half((unsigned short)(s28 >> (16 * h))));
-                        } else {
-                            const int pi = C::KS == 512 ? (bp >> 2) : rsel;
-                            d_r = super_scale(pi ? rec_r[1] : rec_r[0], blk & 7);
-                            d_r8 = super_scale(pi ? rec_r8[1] : rec_r8[0], blk & 7);
+                        uint32_t ar[RG][4], ar8[RG][4];
+                        float d_r[RG], d_r8[RG];
+#pragma unroll
+                        for (int rg = 0; rg < RG; ++rg) {
+                            codes_to_bf16(wv[rg][2 * h], ar[rg]);
+                            codes_to_bf16(wv[rg][2 * h + 1], ar8[rg]);
+                            if constexpr (FMT == SC_BLOCK) {
+                                d_r[rg] = __half2float(__ushort_as_half((unsigned short)(s2[rg] >> (16 * h))));
+                                d_r8[rg] = __half2float(__ushort_as_half((unsigned short)(s28[rg] >> (16 * h))));
+                            } else {
+                                const int pi = C::KS == 512 ? (bp >> 2) : rsel;
+                                d_r[rg] = super_scale(pi ? rec_r[rg][1] : rec_r[rg][0], blk & 7);
+                                d_r8[rg] = super_scale(pi ? rec_r8[rg][1] : rec_r8[rg][0], blk & 7);
+                            }
                         }
 #pragma unroll
-                        for (int ct = 0; ct < NT; ++ct) {
+                        for (int ctl = 0; ctl < CT; ++ctl) {
+                            const int ct = ctb + ctl;   // column tile of the pass
                             const int xrow = ct * 8 + xcol;
                             const int chunk = ((blk & 1) * 4 + t) ^ (xrow & 7);
                             uint32_t b00, b01, b10, b11;
@@ -520,11 +547,15 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                                          : "=f"(c0), "=f"(c1)
                                          : "r"(cbase + (blk * 8 * NT + ct * 8 + 2 * t) * 4));
                             const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-                            float p[4];
-                            dev::mma_bf16(p, ar[0], ar8[0], ar[1], ar8[1], b00, b01, zero);
-                            dev::mma_bf16(p, ar[2], ar8[2], ar[3], ar8[3], b10, b11, p);
-                            dev::fma_add_f32x2(acc[ct][0], acc[ct][1], d_r, p[0], p[1], c0, c1);
-                            dev::fma_add_f32x2(acc[ct][2], acc[ct][3], d_r8, p[2], p[3], c0, c1);
+#pragma unroll
+                            for (int rg = 0; rg < RG; ++rg) {
+                                float p[4];
+                                dev::mma_bf16(p, ar[rg][0], ar8[rg][0], ar[rg][1], ar8[rg][1], b00, b01, zero);
+                                dev::mma_bf16(p, ar[rg][2], ar8[rg][2], ar[rg][3], ar8[rg][3], b10, b11, p);
+                                float(&a4)[4] = acc[rg * CT + ctl];
+                                dev::fma_add_f32x2(a4[0], a4[1], d_r[rg], p[0], p[1], c0, c1);
+                                dev::fma_add_f32x2(a4[2], a4[3], d_r8[rg], p[2], p[3], c0, c1);
+                            }
                         }
                     }
                 }
@@ -542,7 +573,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                 float *ps = wsp_seg + ((size_t)tile * ks + seg) * TILE_ELEMS + frag;
 #pragma unroll
                 for (int ct = 0; ct < NT; ++ct)
-                    if (col0 + ct * 8 < n_cols)
+                    if (fcol(ct) < n_cols)
                         __stcg(reinterpret_cast<float4 *>(ps + ct * NCW * 128),
                                make_float4(acc[ct][0], acc[ct][1], acc[ct][2], acc[ct][3]));
             }
@@ -579,7 +610,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS + frag;
 #pragma unroll
             for (int ct = 0; ct < NT; ++ct)
-                if (col0 + ct * 8 < n_cols)
+                if (fcol(ct) < n_cols)
                     __stcg(reinterpret_cast<float4 *>(pp + ct * NCW * 128),
                            make_float4(yrun[ct][0], yrun[ct][1], yrun[ct][2], yrun[ct][3]));
             named_sync_consumers();             // prefix stores issued; flag[0] read by all
@@ -596,7 +627,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                 const long long head_end = min(sch.begin(blockIdx.x + 1), tile_u0 + ks);
                 fold_tile(tile, (int)(head_end - tile_u0));
 #pragma unroll
-                for (int ct = 0; ct < NT; ++ct) clear_low(pp + ct * NCW * 128, col0 + ct * 8 < n_cols);
+                for (int ct = 0; ct < NT; ++ct) clear_low(pp + ct * NCW * 128, fcol(ct) < n_cols);
                 fold_now = 0;
             }
         }
@@ -623,14 +654,14 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
         float *pp = wsp_prefix + (size_t)tile * TILE_ELEMS + frag;
 #pragma unroll
         for (int ct = 0; ct < NT; ++ct) {
-            if (col0 + ct * 8 < n_cols) {
+            if (fcol(ct) < n_cols) {
                 const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp + ct * NCW * 128));
                 yrun[ct][0] = v.x, yrun[ct][1] = v.y, yrun[ct][2] = v.z, yrun[ct][3] = v.w;
             }
         }
         fold_tile(tile, (int)(head_end - tile_u0));
 #pragma unroll
-        for (int ct = 0; ct < NT; ++ct) clear_low(pp + ct * NCW * 128, col0 + ct * 8 < n_cols);
+        for (int ct = 0; ct < NT; ++ct) clear_low(pp + ct * NCW * 128, fcol(ct) < n_cols);
     }
 }
 
