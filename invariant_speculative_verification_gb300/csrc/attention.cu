@@ -15,14 +15,19 @@
 // The other rows of the call only decide which warp, round or CTA handles a
 // row; sub-tiles past p are left out of the row's merge altogether.
 //
-// K2 (attn_partial_kernel): one CTA per (chunk, kv head, sequence).  A
-// producer thread copies the chunk's K and V pages (4-D TMA boxes, 128B
-// swizzle) into four resident 64-key slots; consumer warp w owns sub-tile w
+// K2 (attn_partial_kernel): a resident grid (at most one CTA per SM) walks
+// the (chunk, kv head, sequence) items, each CTA every G-th item.  A producer
+// warp copies an item's K pages and its V pages (4-D TMA boxes, 128B swizzle)
+// into four 64-key K slots and four V slots; consumer warp w owns sub-tile w
 // and, for each 16-row M-tile of (query row, grouped head) pairs, runs
 // S = Q K^T and O = P V on mma.sync m16n8k16 with fp32 accumulation (P enters
 // the PV product as a hi + lo pair of 16-bit values, rounding error ~2^-17),
 // leaving its (m_w, l_w, o_w) in shared memory; the four warps then merge
-// them and write the chunk partials.
+// them and write the chunk partials.  K and V are released separately (K
+// after the item's last S, V after its last P V), so the next item's K copy
+// runs under this item's P V and merge, and its V copy under the next S.
+// Which CTA computes an item, and when, is scheduling: an item's operations
+// are those of a CTA of its own.
 // K3 (attn_combine_kernel): one warp per (row, head).
 #include "common.cuh"
 
@@ -45,7 +50,8 @@ struct ACfg {
     static constexpr int PART = 16 * OSTR * 4 + 16 * 8;   // o and (m, l) of one (M-tile, sub-tile)
     static constexpr int PART_OFF = NCONS * SLOT;
     static constexpr int BAR_OFF = PART_OFF + MR * NCONS * PART;
-    static constexpr int SMEM = 1024 + BAR_OFF + NCONS * 8;
+    static constexpr int NBAR = 2 * NCONS + 2;              // kfull, vfull per slot; kfree, vfree
+    static constexpr int SMEM = 1024 + BAR_OFF + NBAR * 8;
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -93,283 +99,362 @@ __global__ void __launch_bounds__(THREADS, 1)
 attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                     const uint16_t *__restrict__ q, int Hq, int Hkv, float scale_log2, int num_pages,
                     const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_start,
-                    const int32_t *__restrict__ cu_rows, int R, int max_kv_len, int nc_max,
+                    const int32_t *__restrict__ cu_rows, int S, int R, int max_kv_len, int nc_max,
                     float2 *__restrict__ part_ml, float *__restrict__ part_o, int32_t *dev_err) {
     dev::pdl_wait();
     dev::pdl_launch_dependents();
     using C = ACfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *vfull = kfull + NCONS;
+    uint64_t *kfree = vfull + NCONS;   // every consumer warp is done with the item's K slots
+    uint64_t *vfree = kfree + 1;       // ... with its V slots
 
-    const int c = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r0 = cu_rows[s];
-    const int rows = cu_rows[s + 1] - r0;
-    const int ctx = ctx_start[s];
-    const int len = ctx + rows;
-    if (rows <= 0 || ctx < 0) return;
-    if (r0 < 0 || r0 + rows > R) {  // rows outside the workspace the host sized
-        if (threadIdx.x == 0 && c == 0 && kvh == 0) dev::report(dev_err, SPEC_DEVERR_LAYOUT);
-        return;
-    }
-    if (len > max_kv_len || len > max_blocks * PAGE) {
-        if (threadIdx.x == 0 && c == 0 && kvh == 0) dev::report(dev_err, SPEC_DEVERR_LENGTH);
-        return;
-    }
-    const int kbeg = c * CHUNK;
-    if (kbeg >= len) return;
-    const int kend = min(kbeg + CHUNK, len);
-    const int nsub = (kend - kbeg + SUB - 1) / SUB;
     const int G = Hq / Hkv;
-    const int i0 = max(0, kbeg - ctx);  // first row whose position reaches this chunk
-    const int mrows = (rows - i0) * G;
-    const int mtiles = (mrows + 15) / 16;
+    const long long nitems = (long long)nc_max * Hkv * S;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < NCONS; ++b) dev::mbar_init(&full[b], 1);
+        for (int b = 0; b < NCONS; ++b) {
+            dev::mbar_init(&kfull[b], 1);
+            dev::mbar_init(&vfull[b], 1);
+        }
+        dev::mbar_init(kfree, NCONS);
+        dev::mbar_init(vfree, NCONS);
         dev::fence_barrier_init();
     }
     __syncthreads();
 
-    if (warp == NCONS) {
-        // ---------------- producer: the chunk's sub-tiles into their slots ----------------
-        // The chunk's (at most 16) block-table entries are read by 16 lanes at once;
-        // lane 0 then issues every copy.
-        const int32_t *bt = block_table + (size_t)s * max_blocks;
-        const int pg_first = kbeg / PAGE, pg_end = (kend + PAGE - 1) / PAGE;
-        int my_phys = 0;
-        if (lane < pg_end - pg_first) {
-            my_phys = bt[pg_first + lane];
-            if (my_phys < 0 || my_phys >= num_pages) {
-                dev::report(dev_err, SPEC_DEVERR_BLOCK_TABLE);
-                my_phys = 0;
-            }
+    // Item `it` of the call: chunk c of kv head kvh of sequence s.  Every warp
+    // derives the same geometry from the same inputs, so producer and
+    // consumers skip the same items.
+    struct Item {
+        int c, kvh, s, r0, rows, ctx, len, kbeg, kend, nsub;
+    };
+    auto item = [&](long long it, Item &m) -> bool {
+        m.c = (int)(it % nc_max);
+        m.kvh = (int)((it / nc_max) % Hkv);
+        m.s = (int)(it / ((long long)nc_max * Hkv));
+        m.r0 = cu_rows[m.s];
+        m.rows = cu_rows[m.s + 1] - m.r0;
+        m.ctx = ctx_start[m.s];
+        m.len = m.ctx + m.rows;
+        if (m.rows <= 0 || m.ctx < 0) return false;
+        if (m.r0 < 0 || m.r0 + m.rows > R) {  // rows outside the workspace the host sized
+            if (threadIdx.x == 0 && m.c == 0 && m.kvh == 0) dev::report(dev_err, SPEC_DEVERR_LAYOUT);
+            return false;
         }
+        if (m.len > max_kv_len || m.len > max_blocks * PAGE) {
+            if (threadIdx.x == 0 && m.c == 0 && m.kvh == 0) dev::report(dev_err, SPEC_DEVERR_LENGTH);
+            return false;
+        }
+        m.kbeg = m.c * CHUNK;
+        if (m.kbeg >= m.len) return false;
+        m.kend = min(m.kbeg + CHUNK, m.len);
+        m.nsub = (m.kend - m.kbeg + SUB - 1) / SUB;
+        return true;
+    };
+
+    if (warp == NCONS) {
+        // ---------------- producer: each item's K, then its V, into the slots ----------------
+        // An item's (at most 16) block-table entries are read by 16 lanes at once;
+        // lane 0 then issues every copy, K once the previous item's K slots are
+        // released, V once its V slots are.
         if (lane == 0) {
             dev::prefetch_tmap(&tk);
             dev::prefetch_tmap(&tv);
         }
-        for (int w = 0; w < nsub; ++w) {
-            const int key0 = kbeg + w * SUB;
-            const int pg0 = key0 / PAGE;
-            const int pg1 = min(pg0 + SUB / PAGE, pg_end);
-            uint8_t *kdst = smem + w * C::SLOT;
-            uint8_t *vdst = kdst + C::KV_BYTES;
-            if (lane == 0)
-                dev::mbar_arrive_expect_tx(&full[w], (uint32_t)((pg1 - pg0) * C::HALVES * 2 * 2048));
-            for (int pg = pg0; pg < pg1; ++pg) {
-                const int phys = __shfl_sync(0xffffffffu, my_phys, pg - pg_first);
-                if (lane == 0) {
-                    const int off = (pg - pg0) * 2048;
-#pragma unroll
-                    for (int hh = 0; hh < C::HALVES; ++hh) {
-                        dev::tma_load_4d(kdst + hh * SUB * 128 + off, &tk, hh * 64, 0, kvh, phys, &full[w]);
-                        dev::tma_load_4d(vdst + hh * SUB * 128 + off, &tv, hh * 64, 0, kvh, phys, &full[w]);
-                    }
+        bool ok = true;
+        int jv = 0;   // valid items so far
+        for (long long it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+            Item m;
+            if (!item(it, m)) continue;
+            const int32_t *bt = block_table + (size_t)m.s * max_blocks;
+            const int pg_first = m.kbeg / PAGE, pg_end = (m.kend + PAGE - 1) / PAGE;
+            int my_phys = 0;
+            if (lane < pg_end - pg_first) {
+                my_phys = bt[pg_first + lane];
+                if (my_phys < 0 || my_phys >= num_pages) {
+                    dev::report(dev_err, SPEC_DEVERR_BLOCK_TABLE);
+                    my_phys = 0;
                 }
             }
-        }
-        // the CTA must not exit with copies in flight
-        if (lane == 0)
-            for (int w = 0; w < nsub; ++w)
-                if (!dev::mbar_wait(&full[w], 0)) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
-        return;
-    }
-
-    // ---------------- consumers: warp w owns sub-tile w ----------------
-    const int w = warp;
-    const int g = lane >> 2, t = lane & 3;
-    const int key0 = kbeg + w * SUB;
-    const bool has_sub = w < nsub;
-    bool ok = true;
-    uint8_t *kslot = smem + w * C::SLOT;
-    uint8_t *vslot = kslot + C::KV_BYTES;
-    bool waited = false;   // the slot is waited for after the first Q loads are in flight
-    const uint32_t kb = dev::smem_u32(kslot), vb = dev::smem_u32(vslot);
-
-    for (int mt0 = 0; mt0 < mtiles; mt0 += C::MR) {
-        // ---- each warp: (m_w, l_w, o_w) of its sub-tile for up to MR M-tiles ----
-        for (int j = 0; j < C::MR && mt0 + j < mtiles && has_sub && ok; ++j) {
-            const int mt = mt0 + j;
-            int pos[2];
-            bool valid[2];
-            size_t qoff[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int m = mt * 16 + g + 8 * h;
-                valid[h] = m < mrows;
-                const int i = i0 + (valid[h] ? m / G : 0);
-                const int gg = valid[h] ? m % G : 0;
-                pos[h] = ctx + i;
-                qoff[h] = ((size_t)(r0 + i) * Hq + kvh * G + gg) * D;
-            }
-            // Q fragments for all k-steps (A operand): row m0 / m1, d = 16 kk + 2t (+8), all loads in flight together
-            uint32_t qa[D / 16][4];
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int d0 = 16 * kk + 2 * t;
-                qa[kk][0] = valid[0] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[0] + d0)) : 0u;
-                qa[kk][1] = valid[1] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[1] + d0)) : 0u;
-                qa[kk][2] = valid[0] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[0] + d0 + 8)) : 0u;
-                qa[kk][3] = valid[1] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[1] + d0 + 8)) : 0u;
-            }
-            if (!waited) {
-                waited = true;
-                if (!dev::mbar_wait(&full[w], 0)) {
+            for (int kv = 0; kv < 2 && ok; ++kv) {
+                uint64_t *fr = kv ? vfree : kfree;
+                uint64_t *fl = kv ? vfull : kfull;
+                const CUtensorMap *map = kv ? &tv : &tk;
+                int got = 1;
+                if (lane == 0 && jv > 0) got = dev::mbar_wait(fr, (jv - 1) & 1) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
                     if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     ok = false;
                     break;
                 }
-                const int nvalid = len - key0;  // keys of this slot inside the sequence
-                if (nvalid < SUB) {
-                    // V rows past the sequence end hold stale or unloaded data: zero them so
-                    // that 0-probability keys contribute exactly 0 to P V
-                    for (int idx = lane; idx < C::HALVES * (SUB - nvalid) * 8; idx += 32) {
-                        const int hh = idx / ((SUB - nvalid) * 8);
-                        const int rem = idx % ((SUB - nvalid) * 8);
-                        const int key = nvalid + rem / 8, ch = rem % 8;
-                        *reinterpret_cast<uint4 *>(vslot + hh * SUB * 128 + key * 128 + ch * 16) =
-                            make_uint4(0, 0, 0, 0);
+                for (int w = 0; w < m.nsub; ++w) {
+                    const int key0 = m.kbeg + w * SUB;
+                    const int pg0 = key0 / PAGE;
+                    const int pg1 = min(pg0 + SUB / PAGE, pg_end);
+                    uint8_t *dst = smem + w * C::SLOT + kv * C::KV_BYTES;
+                    if (lane == 0)
+                        dev::mbar_arrive_expect_tx(&fl[w], (uint32_t)((pg1 - pg0) * C::HALVES * 2048));
+                    for (int pg = pg0; pg < pg1; ++pg) {
+                        const int phys = __shfl_sync(0xffffffffu, my_phys, pg - pg_first);
+                        if (lane == 0) {
+                            const int off = (pg - pg0) * 2048;
+#pragma unroll
+                            for (int hh = 0; hh < C::HALVES; ++hh)
+                                dev::tma_load_4d(dst + hh * SUB * 128 + off, map, hh * 64, 0, m.kvh, phys, &fl[w]);
+                        }
                     }
                 }
-                __syncwarp();
             }
-            // ---- S = Q K^T (16 rows x 64 keys) ----
-            float sc[8][4];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) sc[jj][0] = sc[jj][1] = sc[jj][2] = sc[jj][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t qa0 = qa[kk][0], qa1 = qa[kk][1], qa2 = qa[kk][2], qa3 = qa[kk][3];
-                const int hh = (16 * kk) / 64;
-                const int cbase = ((16 * kk) % 64) / 8;
-#pragma unroll
-                for (int jp = 0; jp < 4; ++jp) {
-                    const int mi = lane >> 3;
-                    const int key = 8 * (2 * jp + (mi >> 1)) + (lane & 7);
-                    const int ch = cbase + (mi & 1);
-                    uint32_t b0, b1, b2, b3;
-                    dev::ldmatrix_x4(b0, b1, b2, b3, kb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
-                    mma16<BF16>(sc[2 * jp], qa0, qa1, qa2, qa3, b0, b1, sc[2 * jp]);
-                    mma16<BF16>(sc[2 * jp + 1], qa0, qa1, qa2, qa3, b2, b3, sc[2 * jp + 1]);
-                }
-            }
-            // ---- mask, scale to log2 units, softmax within the sub-tile ----
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int h = e >> 1;
-                    const int key = key0 + 8 * jj + 2 * t + (e & 1);
-                    const bool vis = valid[h] && key <= pos[h];
-                    const float v = vis ? sc[jj][e] * scale_log2 : -INFINITY;
-                    sc[jj][e] = v;
-                    mx[h] = fmaxf(mx[h], v);
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-            }
-            float rs[2] = {0.f, 0.f};
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int h = e >> 1;
-                    const float p = (mx[h] == -INFINITY) ? 0.f : exp2f(sc[jj][e] - mx[h]);
-                    sc[jj][e] = p;
-                    rs[h] += p;
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 1);
-                rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 2);
-            }
-            // ---- O = P V with P = hi + lo ----
-            float o[D / 8][4];
-#pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < SUB / 16; ++kk) {
-                uint32_t ph[4], pl[4];
-                float r00, r01, r10, r11, r20, r21, r30, r31;
-                ph[0] = pack_hi<BF16>(sc[2 * kk][0], sc[2 * kk][1], r00, r01);
-                ph[1] = pack_hi<BF16>(sc[2 * kk][2], sc[2 * kk][3], r10, r11);
-                ph[2] = pack_hi<BF16>(sc[2 * kk + 1][0], sc[2 * kk + 1][1], r20, r21);
-                ph[3] = pack_hi<BF16>(sc[2 * kk + 1][2], sc[2 * kk + 1][3], r30, r31);
-                pl[0] = pack2<BF16>(r00, r01);
-                pl[1] = pack2<BF16>(r10, r11);
-                pl[2] = pack2<BF16>(r20, r21);
-                pl[3] = pack2<BF16>(r30, r31);
-#pragma unroll
-                for (int ndp = 0; ndp < D / 16; ++ndp) {
-                    const int mi = lane >> 3;
-                    const int key = 16 * kk + 8 * (mi & 1) + (lane & 7);
-                    const int dch = 2 * ndp + (mi >> 1);     // 8-wide d chunk
-                    const int hh = dch / 8, ch = dch % 8;
-                    uint32_t b0, b1, b2, b3;
-                    dev::ldmatrix_x4_trans(b0, b1, b2, b3, vb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
-                    mma16<BF16>(o[2 * ndp], ph[0], ph[1], ph[2], ph[3], b0, b1, o[2 * ndp]);
-                    mma16<BF16>(o[2 * ndp], pl[0], pl[1], pl[2], pl[3], b0, b1, o[2 * ndp]);
-                    mma16<BF16>(o[2 * ndp + 1], ph[0], ph[1], ph[2], ph[3], b2, b3, o[2 * ndp + 1]);
-                    mma16<BF16>(o[2 * ndp + 1], pl[0], pl[1], pl[2], pl[3], b2, b3, o[2 * ndp + 1]);
-                }
-            }
-            // ---- leave (m_w, l_w, o_w) of rows g, g + 8 in shared memory ----
-            uint8_t *pb = smem + C::PART_OFF + (j * NCONS + w) * C::PART;
-            float *po_s = reinterpret_cast<float *>(pb);
-            float2 *pml = reinterpret_cast<float2 *>(pb + 16 * C::OSTR * 4);
-#pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) {
-                *reinterpret_cast<float2 *>(po_s + g * C::OSTR + 8 * nd + 2 * t) = make_float2(o[nd][0], o[nd][1]);
-                *reinterpret_cast<float2 *>(po_s + (g + 8) * C::OSTR + 8 * nd + 2 * t) = make_float2(o[nd][2], o[nd][3]);
-            }
-            if (t == 0) {
-                pml[g] = make_float2(mx[0], rs[0]);
-                pml[g + 8] = make_float2(mx[1], rs[1]);
-            }
+            ++jv;
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(NCONS * 32) : "memory");
-        // ---- merge the sub-tiles of each row in ascending order, write the chunk partial ----
-        if (ok) {
-            constexpr int D4 = D / 4;
-            for (int e = threadIdx.x; e < C::MR * 16 * D4; e += NCONS * 32) {
-                const int j = e / (16 * D4), row = (e / D4) % 16, d4 = e % D4;
+        // every copy issued is waited for by its consumer warp before the CTA can exit
+        return;
+    }
+
+    // ---------------- consumers: warp w owns sub-tile w of every item ----------------
+    const int w = warp;
+    const int g = lane >> 2, t = lane & 3;
+    uint8_t *kslot = smem + w * C::SLOT;
+    uint8_t *vslot = kslot + C::KV_BYTES;
+    const uint32_t kb = dev::smem_u32(kslot), vb = dev::smem_u32(vslot);
+    bool ok = true;
+    int uses = 0;   // items in which this warp's slots were filled (their phase parity)
+    for (long long it = blockIdx.x; it < nitems; it += gridDim.x) {
+        Item itm;
+        if (!item(it, itm)) continue;
+        const int c = itm.c, kvh = itm.kvh, r0 = itm.r0, rows = itm.rows, ctx = itm.ctx, len = itm.len;
+        const int kbeg = itm.kbeg, nsub = itm.nsub;
+        const int i0 = max(0, kbeg - ctx);  // first row whose position reaches this chunk
+        const int mrows = (rows - i0) * G;
+        const int mtiles = (mrows + 15) / 16;
+        const int key0 = kbeg + w * SUB;
+        const bool has_sub = w < nsub;
+        const uint32_t par = (uint32_t)(uses & 1);
+        if (has_sub) ++uses;
+        bool kwaited = false, vwaited = false;
+        bool karrived = false, varrived = false;   // this warp's release of the item's K / V slots
+
+        for (int mt0 = 0; mt0 < mtiles; mt0 += C::MR) {
+            // ---- each warp: (m_w, l_w, o_w) of its sub-tile for up to MR M-tiles ----
+            const bool last_round = mt0 + C::MR >= mtiles;
+            for (int j = 0; j < C::MR && mt0 + j < mtiles && has_sub && ok; ++j) {
                 const int mt = mt0 + j;
-                const int m = mt * 16 + row;
-                if (mt >= mtiles || m >= mrows) continue;
-                const int i = i0 + m / G, gg = m % G;
-                const int p = ctx + i;
-                const int nw = min(nsub, (p - kbeg) / SUB + 1);   // sub-tiles whose first key is visible
-                const uint8_t *pb0 = smem + C::PART_OFF + (j * NCONS) * C::PART;
-                float mmax = -INFINITY;
-                for (int ww = 0; ww < nw; ++ww)
-                    mmax = fmaxf(mmax, reinterpret_cast<const float2 *>(pb0 + ww * C::PART + 16 * C::OSTR * 4)[row].x);
-                float l = 0.f;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int ww = 0; ww < nw; ++ww) {
-                    const uint8_t *pb = pb0 + ww * C::PART;
-                    const float2 ml = reinterpret_cast<const float2 *>(pb + 16 * C::OSTR * 4)[row];
-                    const float sc = exp2f(ml.x - mmax);
-                    l = fmaf(ml.y, sc, l);
-                    const float4 ov = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(pb) +
-                                                                        row * C::OSTR + 4 * d4);
-                    acc.x = fmaf(ov.x, sc, acc.x);
-                    acc.y = fmaf(ov.y, sc, acc.y);
-                    acc.z = fmaf(ov.z, sc, acc.z);
-                    acc.w = fmaf(ov.w, sc, acc.w);
+                const bool last_tile = last_round && (j == C::MR - 1 || mt0 + j + 1 == mtiles);
+                int pos[2];
+                bool valid[2];
+                size_t qoff[2];
+    #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int m = mt * 16 + g + 8 * h;
+                    valid[h] = m < mrows;
+                    const int i = i0 + (valid[h] ? m / G : 0);
+                    const int gg = valid[h] ? m % G : 0;
+                    pos[h] = ctx + i;
+                    qoff[h] = ((size_t)(r0 + i) * Hq + kvh * G + gg) * D;
                 }
-                const size_t pidx = ((size_t)(r0 + i) * Hq + kvh * G + gg) * nc_max + c;
-                *reinterpret_cast<float4 *>(part_o + pidx * D + 4 * d4) = acc;
-                if (d4 == 0) part_ml[pidx] = make_float2(mmax, l);
+                // Q fragments for all k-steps (A operand): row m0 / m1, d = 16 kk + 2t (+8), all loads in flight together
+                uint32_t qa[D / 16][4];
+    #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int d0 = 16 * kk + 2 * t;
+                    qa[kk][0] = valid[0] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[0] + d0)) : 0u;
+                    qa[kk][1] = valid[1] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[1] + d0)) : 0u;
+                    qa[kk][2] = valid[0] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[0] + d0 + 8)) : 0u;
+                    qa[kk][3] = valid[1] ? __ldg(reinterpret_cast<const unsigned int *>(q + qoff[1] + d0 + 8)) : 0u;
+                }
+                if (!kwaited) {
+                    kwaited = true;
+                    if (!dev::mbar_wait(&kfull[w], par)) {
+                        if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                }
+                // ---- S = Q K^T (16 rows x 64 keys) ----
+                float sc[8][4];
+    #pragma unroll
+                for (int jj = 0; jj < 8; ++jj) sc[jj][0] = sc[jj][1] = sc[jj][2] = sc[jj][3] = 0.f;
+    #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qa0 = qa[kk][0], qa1 = qa[kk][1], qa2 = qa[kk][2], qa3 = qa[kk][3];
+                    const int hh = (16 * kk) / 64;
+                    const int cbase = ((16 * kk) % 64) / 8;
+    #pragma unroll
+                    for (int jp = 0; jp < 4; ++jp) {
+                        const int mi = lane >> 3;
+                        const int key = 8 * (2 * jp + (mi >> 1)) + (lane & 7);
+                        const int ch = cbase + (mi & 1);
+                        uint32_t b0, b1, b2, b3;
+                        dev::ldmatrix_x4(b0, b1, b2, b3, kb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
+                        mma16<BF16>(sc[2 * jp], qa0, qa1, qa2, qa3, b0, b1, sc[2 * jp]);
+                        mma16<BF16>(sc[2 * jp + 1], qa0, qa1, qa2, qa3, b2, b3, sc[2 * jp + 1]);
+                    }
+                }
+                if (last_tile) {
+                    // the item's last S of this warp: its K slot may take the next item's keys
+                    __syncwarp();
+                    if (lane == 0) dev::mbar_arrive(kfree);
+                    karrived = true;
+                }
+                // ---- mask, scale to log2 units, softmax within the sub-tile ----
+                float mx[2] = {-INFINITY, -INFINITY};
+    #pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = e >> 1;
+                        const int key = key0 + 8 * jj + 2 * t + (e & 1);
+                        const bool vis = valid[h] && key <= pos[h];
+                        const float v = vis ? sc[jj][e] * scale_log2 : -INFINITY;
+                        sc[jj][e] = v;
+                        mx[h] = fmaxf(mx[h], v);
+                    }
+                }
+    #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                }
+                float rs[2] = {0.f, 0.f};
+    #pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = e >> 1;
+                        const float p = (mx[h] == -INFINITY) ? 0.f : exp2f(sc[jj][e] - mx[h]);
+                        sc[jj][e] = p;
+                        rs[h] += p;
+                    }
+                }
+    #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 1);
+                    rs[h] += __shfl_xor_sync(0xffffffffu, rs[h], 2);
+                }
+                if (!vwaited) {
+                    vwaited = true;
+                    if (!dev::mbar_wait(&vfull[w], par)) {
+                        if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    const int nvalid = len - key0;  // keys of this slot inside the sequence
+                    if (nvalid < SUB) {
+                        // V rows past the sequence end hold stale or unloaded data: zero them so
+                        // that 0-probability keys contribute exactly 0 to P V
+                        for (int idx = lane; idx < C::HALVES * (SUB - nvalid) * 8; idx += 32) {
+                            const int hh = idx / ((SUB - nvalid) * 8);
+                            const int rem = idx % ((SUB - nvalid) * 8);
+                            const int key = nvalid + rem / 8, ch = rem % 8;
+                            *reinterpret_cast<uint4 *>(vslot + hh * SUB * 128 + key * 128 + ch * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    __syncwarp();
+                }
+                // ---- O = P V with P = hi + lo ----
+                float o[D / 8][4];
+    #pragma unroll
+                for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    #pragma unroll
+                for (int kk = 0; kk < SUB / 16; ++kk) {
+                    uint32_t ph[4], pl[4];
+                    float r00, r01, r10, r11, r20, r21, r30, r31;
+                    ph[0] = pack_hi<BF16>(sc[2 * kk][0], sc[2 * kk][1], r00, r01);
+                    ph[1] = pack_hi<BF16>(sc[2 * kk][2], sc[2 * kk][3], r10, r11);
+                    ph[2] = pack_hi<BF16>(sc[2 * kk + 1][0], sc[2 * kk + 1][1], r20, r21);
+                    ph[3] = pack_hi<BF16>(sc[2 * kk + 1][2], sc[2 * kk + 1][3], r30, r31);
+                    pl[0] = pack2<BF16>(r00, r01);
+                    pl[1] = pack2<BF16>(r10, r11);
+                    pl[2] = pack2<BF16>(r20, r21);
+                    pl[3] = pack2<BF16>(r30, r31);
+    #pragma unroll
+                    for (int ndp = 0; ndp < D / 16; ++ndp) {
+                        const int mi = lane >> 3;
+                        const int key = 16 * kk + 8 * (mi & 1) + (lane & 7);
+                        const int dch = 2 * ndp + (mi >> 1);     // 8-wide d chunk
+                        const int hh = dch / 8, ch = dch % 8;
+                        uint32_t b0, b1, b2, b3;
+                        dev::ldmatrix_x4_trans(b0, b1, b2, b3, vb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
+                        mma16<BF16>(o[2 * ndp], ph[0], ph[1], ph[2], ph[3], b0, b1, o[2 * ndp]);
+                        mma16<BF16>(o[2 * ndp], pl[0], pl[1], pl[2], pl[3], b0, b1, o[2 * ndp]);
+                        mma16<BF16>(o[2 * ndp + 1], ph[0], ph[1], ph[2], ph[3], b2, b3, o[2 * ndp + 1]);
+                        mma16<BF16>(o[2 * ndp + 1], pl[0], pl[1], pl[2], pl[3], b2, b3, o[2 * ndp + 1]);
+                    }
+                }
+                if (last_tile) {
+                    // the item's last P V of this warp: its V slot may take the next item's values
+                    // (the zeroing above wrote it through the generic proxy: order that first)
+                    dev::fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) dev::mbar_arrive(vfree);
+                    varrived = true;
+                }
+                // ---- leave (m_w, l_w, o_w) of rows g, g + 8 in shared memory ----
+                uint8_t *pb = smem + C::PART_OFF + (j * NCONS + w) * C::PART;
+                float *po_s = reinterpret_cast<float *>(pb);
+                float2 *pml = reinterpret_cast<float2 *>(pb + 16 * C::OSTR * 4);
+    #pragma unroll
+                for (int nd = 0; nd < D / 8; ++nd) {
+                    *reinterpret_cast<float2 *>(po_s + g * C::OSTR + 8 * nd + 2 * t) = make_float2(o[nd][0], o[nd][1]);
+                    *reinterpret_cast<float2 *>(po_s + (g + 8) * C::OSTR + 8 * nd + 2 * t) = make_float2(o[nd][2], o[nd][3]);
+                }
+                if (t == 0) {
+                    pml[g] = make_float2(mx[0], rs[0]);
+                    pml[g + 8] = make_float2(mx[1], rs[1]);
+                }
             }
+            asm volatile("bar.sync 1, %0;" ::"n"(NCONS * 32) : "memory");
+            // ---- merge the sub-tiles of each row in ascending order, write the chunk partial ----
+            if (ok) {
+                constexpr int D4 = D / 4;
+                for (int e = threadIdx.x; e < C::MR * 16 * D4; e += NCONS * 32) {
+                    const int j = e / (16 * D4), row = (e / D4) % 16, d4 = e % D4;
+                    const int mt = mt0 + j;
+                    const int m = mt * 16 + row;
+                    if (mt >= mtiles || m >= mrows) continue;
+                    const int i = i0 + m / G, gg = m % G;
+                    const int p = ctx + i;
+                    const int nw = min(nsub, (p - kbeg) / SUB + 1);   // sub-tiles whose first key is visible
+                    const uint8_t *pb0 = smem + C::PART_OFF + (j * NCONS) * C::PART;
+                    float mmax = -INFINITY;
+                    for (int ww = 0; ww < nw; ++ww)
+                        mmax = fmaxf(mmax, reinterpret_cast<const float2 *>(pb0 + ww * C::PART + 16 * C::OSTR * 4)[row].x);
+                    float l = 0.f;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int ww = 0; ww < nw; ++ww) {
+                        const uint8_t *pb = pb0 + ww * C::PART;
+                        const float2 ml = reinterpret_cast<const float2 *>(pb + 16 * C::OSTR * 4)[row];
+                        const float sc = exp2f(ml.x - mmax);
+                        l = fmaf(ml.y, sc, l);
+                        const float4 ov = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(pb) +
+                                                                            row * C::OSTR + 4 * d4);
+                        acc.x = fmaf(ov.x, sc, acc.x);
+                        acc.y = fmaf(ov.y, sc, acc.y);
+                        acc.z = fmaf(ov.z, sc, acc.z);
+                        acc.w = fmaf(ov.w, sc, acc.w);
+                    }
+                    const size_t pidx = ((size_t)(r0 + i) * Hq + kvh * G + gg) * nc_max + c;
+                    *reinterpret_cast<float4 *>(part_o + pidx * D + 4 * d4) = acc;
+                    if (d4 == 0) part_ml[pidx] = make_float2(mmax, l);
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(NCONS * 32) : "memory");
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(NCONS * 32) : "memory");
+        // a warp without a sub-tile in this item (or after an error) still releases once
+        if (!karrived) {
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(kfree);
+        }
+        if (!varrived) {
+            dev::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(vfree);
+        }
     }
 }
 
@@ -471,10 +556,13 @@ spec_status launch_partial(const CUtensorMap &tk, const CUtensorMap &tv, const v
     static spec::SmemOptIn opt_in;
     spec_status so = spec::smem_opt_in(kern, C::SMEM, opt_in, "cudaFuncSetAttribute(attn smem)");
     if (so != SPEC_OK) return so;
-    dim3 grid(nc_max, Hkv, S);
-    cudaError_t le = spec::launch_pdl(kern, grid, dim3(THREADS), C::SMEM, st, tk, tv, reinterpret_cast<const uint16_t *>(q),
-                                      Hq, Hkv, scale * LOG2E, num_pages, bt, max_blocks, ctx, cu, R, max_kv_len, nc_max,
-                                      ml, po, dev_err);
+    // a resident grid: at most one CTA per SM (the shared memory of one), each walking every G-th item
+    const long long items = (long long)nc_max * Hkv * S;
+    const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
+    const int grid = (int)(items < sms ? items : sms);
+    cudaError_t le = spec::launch_pdl(kern, dim3(grid), dim3(THREADS), C::SMEM, st, tk, tv,
+                                      reinterpret_cast<const uint16_t *>(q), Hq, Hkv, scale * LOG2E, num_pages, bt,
+                                      max_blocks, ctx, cu, S, R, max_kv_len, nc_max, ml, po, dev_err);
     return spec::cuda_status(le, "attn partial launch");
 }
 
