@@ -120,6 +120,23 @@ spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
                          void *workspace, size_t ws_bytes,
                          int32_t *dev_err, spec_stream_t stream);
 
+/* The 80-column pass of spec_qmatmul with its activations already packed
+ * (the same arithmetic, bit for bit): `xpk` holds the packed form of up to 80
+ * activation columns (column c = row c of the producer) for every 256-k stage
+ * of K, spec_packed_activation_bytes(K) bytes, written by
+ * spec_add_rmsnorm_packed or spec_swiglu_packed; the call skips the packing
+ * kernel spec_qmatmul launches before such a pass.  17 <= n_cols <= 80 (one
+ * pass; columns from n_cols on are neither read for y nor written), K a
+ * multiple of 256, xpk 16-byte aligned; y, ldy, accumulate, workspace
+ * (spec_qmatmul_workspace(N, K, n_cols)) and dev_err as for spec_qmatmul.
+ * Source: ramgpt.org, "When Lossless Speculation Stops Being Lossless on
+ * Blackwell", section "Quantized Matrix Multiplication Shows the Same Class of
+ * Failure" (only the delivery of the activations changes). */
+size_t spec_packed_activation_bytes(int K);
+spec_status spec_qmatmul_packed(const uint8_t *wq, const uint16_t *ws, int N, int K, const void *xpk,
+                                int n_cols, void *y, spec_dtype y_dt, int ldy, int accumulate,
+                                void *workspace, size_t ws_bytes, int32_t *dev_err, spec_stream_t stream);
+
 /* The same product for a column count known only on the device: the first
  * c = min(n_cols, *dev_cols) columns of x when *dev_cols >= min_cols, else
  * nothing (y untouched).  dev_cols (device int32) is read after the preceding
@@ -344,6 +361,14 @@ spec_status spec_rope_append(const float *qkv, int R, int Hq, int Hkv, int D,
 
 /* out[r][i] = bf16(silu(gu[r][i]) * gu[r][F + i]); gu fp32 [R][2F]; out bf16 [R][F]. */
 spec_status spec_swiglu(const float *gu, int R, int F, uint16_t *out, spec_stream_t stream);
+
+/* spec_add_rmsnorm and spec_swiglu that also write their rows, as columns of
+ * an 80-column K1 pass, in the packed form spec_qmatmul_packed reads: xpk of
+ * spec_packed_activation_bytes(H or F) bytes, 16-byte aligned; R <= 80, H or F
+ * a multiple of 256.  out is written as by the plain calls. */
+spec_status spec_add_rmsnorm_packed(float *h, const float *delta, const float *w, int R, int H, float eps,
+                                    uint16_t *out, void *xpk, spec_stream_t stream);
+spec_status spec_swiglu_packed(const float *gu, int R, int F, uint16_t *out, void *xpk, spec_stream_t stream);
 
 /* out[i] = bf16(in[i]) for i < n (round to nearest even). */
 spec_status spec_cast_bf16(const float *in, size_t n, uint16_t *out, spec_stream_t stream);

@@ -52,6 +52,10 @@ _SIGS = {
     "spec_rope_append": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp,
                                 _i32, _vp, _vp, _vp, _vp]),
     "spec_swiglu": (_i32, [_vp, _i32, _i32, _vp, _vp]),
+    "spec_add_rmsnorm_packed": (_i32, [_vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp]),
+    "spec_swiglu_packed": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp]),
+    "spec_packed_activation_bytes": (_sz, [_i32]),
+    "spec_qmatmul_packed": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "spec_cast_bf16": (_i32, [_vp, _sz, _vp, _vp]),
     "spec_ngram_draft": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "spec_commit_accepted": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
@@ -251,6 +255,26 @@ def spec_rope_append(qkv, R, Hq, Hkv, D, rope_tab, max_pos, cu_rows, ctx_start, 
 
 def spec_swiglu(gu, R, F, out, stream=None):
     _check("spec_swiglu", load().spec_swiglu(_ptr(gu), R, F, _ptr(out), _stream(stream)))
+
+
+def spec_add_rmsnorm_packed(h, delta, w, R, H, eps, out, xpk, stream=None):
+    _check("spec_add_rmsnorm_packed", load().spec_add_rmsnorm_packed(_ptr(h), _ptr(delta), _ptr(w), R, H, float(eps),
+                                                                     _ptr(out), _ptr(xpk), _stream(stream)))
+
+
+def spec_swiglu_packed(gu, R, F, out, xpk, stream=None):
+    _check("spec_swiglu_packed", load().spec_swiglu_packed(_ptr(gu), R, F, _ptr(out), _ptr(xpk), _stream(stream)))
+
+
+def spec_packed_activation_bytes(K):
+    return int(load().spec_packed_activation_bytes(int(K)))
+
+
+def spec_qmatmul_packed(wq, ws, N, K, xpk, n_cols, y, y_dt, ldy, accumulate, workspace, ws_bytes, dev_err=None,
+                        stream=None):
+    _check("spec_qmatmul_packed", load().spec_qmatmul_packed(_ptr(wq), _ptr(ws), N, K, _ptr(xpk), n_cols, _ptr(y),
+                                                             int(y_dt), ldy, int(accumulate), _ptr(workspace),
+                                                             int(ws_bytes), _ptr(dev_err), _stream(stream)))
 
 
 def spec_cast_bf16(inp, n, out, stream=None):

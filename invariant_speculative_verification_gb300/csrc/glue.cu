@@ -1,7 +1,7 @@
 // Decoder glue and n-gram drafting for the end-to-end greedy generation
 // workload.  Every floating-point kernel here works on one row at a time with a
 // reduction order fixed by the row length, so it is width-invariant.
-#include "common.cuh"
+#include "qmm_shared.cuh"
 
 namespace {
 
@@ -31,7 +31,7 @@ __global__ void embed_kernel(const uint16_t *__restrict__ emb, int V, int H, con
 constexpr int NT_NORM = 256;
 __global__ void __launch_bounds__(NT_NORM)
 add_rmsnorm_kernel(float *__restrict__ h, const float *__restrict__ delta, const float *__restrict__ w, int H,
-                   float eps, uint16_t *__restrict__ out) {
+                   float eps, uint16_t *__restrict__ out, uint8_t *__restrict__ xpk) {
     dev::pdl_wait();
     dev::pdl_launch_dependents();
     const int r = blockIdx.x;
@@ -71,6 +71,11 @@ add_rmsnorm_kernel(float *__restrict__ h, const float *__restrict__ delta, const
         __nv_bfloat162 a = __floats2bfloat162_rn(v.x * inv * ww.x, v.y * inv * ww.y);
         __nv_bfloat162 b = __floats2bfloat162_rn(v.z * inv * ww.z, v.w * inv * ww.w);
         o2[i] = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+    }
+    if (xpk) {
+        // the row is column r of an 80-column K1 pass: write its packed blocks too
+        __syncthreads();   // the row's bf16 values, stored above by every thread, are visible to the block
+        for (int b = threadIdx.x; b < H / 32; b += NT_NORM) qmm::pack_wide_block(out + (size_t)r * H + 32 * b, 32 * b, r, xpk);
     }
 }
 
@@ -165,15 +170,17 @@ __device__ __forceinline__ uint16_t swiglu1(float x, float u) {
 
 // grid (ceil(F / 1024), R): each thread one group of four consecutive features
 // (16-byte loads when F % 4 == 0 and the buffers are aligned, one element at a time otherwise)
-__global__ void swiglu_kernel(const float *__restrict__ gu, int F, uint16_t *__restrict__ out, int vec) {
+__global__ void swiglu_kernel(const float *__restrict__ gu, int F, uint16_t *__restrict__ out, int vec,
+                              uint8_t *__restrict__ xpk) {
     dev::pdl_wait();
     dev::pdl_launch_dependents();
     const int r = blockIdx.y;
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    if (i >= F) return;
     const float *g = gu + (size_t)r * 2 * F;
     uint16_t *o = out + (size_t)r * F;
-    if (vec) {
+    if (i >= F) {
+        // nothing of this thread's own
+    } else if (vec) {
         const float4 x = *reinterpret_cast<const float4 *>(g + i);
         const float4 u = *reinterpret_cast<const float4 *>(g + F + i);
         const uint2 v = make_uint2((uint32_t)swiglu1(x.x, u.x) | ((uint32_t)swiglu1(x.y, u.y) << 16),
@@ -181,6 +188,15 @@ __global__ void swiglu_kernel(const float *__restrict__ gu, int F, uint16_t *__r
         *reinterpret_cast<uint2 *>(o + i) = v;
     } else {
         for (int e = i; e < i + 4 && e < F; ++e) o[e] = swiglu1(g[e], g[F + e]);
+    }
+    if (xpk) {
+        // the row is column r of an 80-column K1 pass: pack this CTA's 32-feature blocks too
+        __syncthreads();   // the CTA's bf16 values, stored above, are visible to the block
+        const int f0 = blockIdx.x * blockDim.x * 4;
+        for (int b = threadIdx.x; b < (int)blockDim.x / 8; b += blockDim.x) {
+            const int kb = f0 + 32 * b;
+            if (kb < F) qmm::pack_wide_block(o + kb, kb, r, xpk);
+        }
     }
 }
 
@@ -273,9 +289,25 @@ extern "C" spec_status spec_add_rmsnorm(float *h, const float *delta, const floa
     SPEC_CHECK_ARG(spec::aligned16(h) && spec::aligned16(delta) && spec::aligned16(w) && spec::aligned16(out),
                    "add_rmsnorm: pointers must be 16-byte aligned");
     if (R == 0) return SPEC_OK;
-    cudaError_t le = spec::launch_pdl(add_rmsnorm_kernel, dim3(R), dim3(NT_NORM), 0, (cudaStream_t)stream, h, delta, w, H, eps, out);
+    cudaError_t le = spec::launch_pdl(add_rmsnorm_kernel, dim3(R), dim3(NT_NORM), 0, (cudaStream_t)stream, h, delta, w, H, eps, out,
+                                      (uint8_t *)nullptr);
     if (le != cudaSuccess) return spec::cuda_status(le, "add_rmsnorm launch");
     return spec::cuda_status(cudaGetLastError(), "add_rmsnorm launch");
+}
+
+extern "C" spec_status spec_add_rmsnorm_packed(float *h, const float *delta, const float *w, int R, int H, float eps,
+                                               uint16_t *out, void *xpk, spec_stream_t stream) {
+    SPEC_CHECK_ARG(R >= 0 && R <= qmm::WIDE_COLS && H >= 256 && H % 256 == 0,
+                   "add_rmsnorm_packed: need R <= 80 and H a multiple of 256 (R=%d H=%d)", R, H);
+    SPEC_CHECK_ARG((h && w && out && xpk) || R == 0, "add_rmsnorm_packed: NULL pointer");
+    SPEC_CHECK_ARG(spec::aligned16(h) && spec::aligned16(delta) && spec::aligned16(w) && spec::aligned16(out) &&
+                       spec::aligned16(xpk),
+                   "add_rmsnorm_packed: pointers must be 16-byte aligned");
+    if (R == 0) return SPEC_OK;
+    cudaError_t le = spec::launch_pdl(add_rmsnorm_kernel, dim3(R), dim3(NT_NORM), 0, (cudaStream_t)stream, h, delta, w, H, eps, out,
+                                      reinterpret_cast<uint8_t *>(xpk));
+    if (le != cudaSuccess) return spec::cuda_status(le, "add_rmsnorm_packed launch");
+    return spec::cuda_status(cudaGetLastError(), "add_rmsnorm_packed launch");
 }
 
 extern "C" spec_status spec_rope_table(float *tab, int max_pos, int D, float theta, spec_stream_t stream) {
@@ -314,9 +346,22 @@ extern "C" spec_status spec_swiglu(const float *gu, int R, int F, uint16_t *out,
     SPEC_CHECK_ARG(R <= 65535, "swiglu: at most 65535 rows per call");
     const int vec = (F % 4 == 0) && spec::aligned16(gu) && (reinterpret_cast<uintptr_t>(out) % 8 == 0);
     cudaError_t le = spec::launch_pdl(swiglu_kernel, dim3((F + 1023) / 1024, R), dim3(256), 0, (cudaStream_t)stream,
-                                      gu, F, out, vec);
+                                      gu, F, out, vec, (uint8_t *)nullptr);
     if (le != cudaSuccess) return spec::cuda_status(le, "swiglu launch");
     return spec::cuda_status(cudaGetLastError(), "swiglu launch");
+}
+
+extern "C" spec_status spec_swiglu_packed(const float *gu, int R, int F, uint16_t *out, void *xpk, spec_stream_t stream) {
+    SPEC_CHECK_ARG(R >= 0 && R <= qmm::WIDE_COLS && F >= 256 && F % 256 == 0,
+                   "swiglu_packed: need R <= 80 and F a multiple of 256 (R=%d F=%d)", R, F);
+    SPEC_CHECK_ARG((gu && out && xpk) || R == 0, "swiglu_packed: NULL pointer");
+    SPEC_CHECK_ARG(spec::aligned16(gu) && spec::aligned16(out) && spec::aligned16(xpk),
+                   "swiglu_packed: pointers must be 16-byte aligned");
+    if (R == 0) return SPEC_OK;
+    cudaError_t le = spec::launch_pdl(swiglu_kernel, dim3((F + 1023) / 1024, R), dim3(256), 0, (cudaStream_t)stream,
+                                      gu, F, out, 1, reinterpret_cast<uint8_t *>(xpk));
+    if (le != cudaSuccess) return spec::cuda_status(le, "swiglu_packed launch");
+    return spec::cuda_status(cudaGetLastError(), "swiglu_packed launch");
 }
 
 extern "C" spec_status spec_cast_bf16(const float *in, size_t n, uint16_t *out, spec_stream_t stream) {

@@ -92,6 +92,10 @@ struct Cfg {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
+static_assert(Cfg<MAX_NT>::X_BYTES == SYNC_WIDE_X_BYTES && Cfg<MAX_NT>::XC_BYTES == WIDE_XC_BYTES &&
+                  Cfg<MAX_NT>::KS == WIDE_KS && MAX_NT == SYNC_WIDE_NT,
+              "the packed layout producers write (qmm_shared.cuh) is the 80-column pass's stage layout");
+
 // 32-k blocks per stage of a pass with nt column tiles (the scale box width)
 inline int stage_blocks(int nt) { return nt >= MAX_NT ? Cfg<MAX_NT>::NBLK : nt == 2 ? Cfg<2>::NBLK : Cfg<1>::NBLK; }
 
@@ -123,36 +127,6 @@ __device__ __forceinline__ void load_pair(uint4 (&v)[4], const uint16_t *__restr
     }
 }
 
-// Writes pair (blk, c) of a stage: the bf16 values in MMA B-fragment order into
-// the stage's activation area xs, and -136 x the block sum into ci (the block
-// sum is the four 8-k chunk sums, each summed in k order, added in chunk order).
-template <int NT>
-__device__ __forceinline__ void put_pair(const uint4 (&v)[4], int blk, int c, uint8_t *xs, float *ci) {
-    uint8_t *row = xs + (blk >> 1) * Cfg<NT>::X_BOX + c * 128;
-    float sum = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-        float cs = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            cs += __uint_as_float(w4[e] << 16);
-            cs += __uint_as_float(w4[e] & 0xFFFF0000u);
-        }
-        sum = (q == 0) ? cs : sum + cs;
-        uint4 o;
-        o.x = dev::prmt(w4[0], w4[2], 0x5410);   // (x0, x4)
-        o.y = dev::prmt(w4[0], w4[2], 0x7632);   // (x1, x5)
-        o.z = dev::prmt(w4[1], w4[3], 0x5410);   // (x2, x6)
-        o.w = dev::prmt(w4[1], w4[3], 0x7632);   // (x3, x7)
-        const int chunk = (((blk & 1) * 4 + q) ^ (c & 7)) << 4;
-        *reinterpret_cast<uint4 *>(row + chunk) = o;
-    }
-    // MMA column slot g carries activation column pi(g) = (g & 1) * 4 + g / 2
-    const int cc = c & 7, slot = (cc & 3) * 2 + (cc >> 2);
-    ci[blk * 8 * NT + (c & ~7) + slot] = -136.0f * sum;
-}
-
 // Packs the activations of one pass (columns col0 .. col0 + 8 NT - 1) for every
 // stage of K into out: stage st occupies out[st * XC_BYTES ...] in the byte
 // layout of a stage's activation and block-sum areas.
@@ -172,7 +146,7 @@ __global__ void __launch_bounds__(256) xpack_kernel(const uint16_t *__restrict__
     uint4 v[4];
     load_pair(v, x, ldx, K, n_cols, col0 + c, st * C::KS + 32 * blk);
     uint8_t *base = out + (size_t)st * C::XC_BYTES;
-    put_pair<NT>(v, blk, c, base, reinterpret_cast<float *>(base + C::X_BYTES));
+    pack_pair<NT>(v, blk, c, base, reinterpret_cast<float *>(base + C::X_BYTES));
 }
 
 __device__ __forceinline__ void named_sync_consumers() {
@@ -336,7 +310,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
 #pragma unroll
                 for (int jj = 0; jj < GROUP; ++jj) {
                     const int p = lane + 32 * (j0 + jj);
-                    put_pair<NT>(v[jj], p / (8 * NT), p % (8 * NT), xs, ci);
+                    pack_pair<NT>(v[jj], p / (8 * NT), p % (8 * NT), xs, ci);
                 }
             }
             int got = 1;
@@ -669,7 +643,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
 template <int NT, bool OUT_BF16, int FMT>
 spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N, int K,
                       int n_cols, int col0, void *y, int ldy, int accumulate, int seg512, void *workspace,
-                      int32_t *dev_err, const int32_t *dev_cols, int min_cols, cudaStream_t stream) {
+                      int32_t *dev_err, const int32_t *dev_cols, int min_cols, cudaStream_t stream,
+                      const uint8_t *xpk_in = nullptr) {
     using C = Cfg<NT, FMT>;
     auto kern = qmm_kernel<NT, OUT_BF16, FMT>;
     static spec::SmemOptIn opt_in;
@@ -680,8 +655,8 @@ spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16
     const WsLayout wl = ws_layout(workspace, sch.tiles, sch.ks, BM * 8 * NT);
     int *counters = wl.counters;
     float *prefix = wl.prefix, *segs = wl.segs;
-    const uint8_t *xpk = wl.xpk;
-    if constexpr (C::XPACK) {
+    const uint8_t *xpk = xpk_in ? xpk_in : wl.xpk;
+    if (C::XPACK && !xpk_in) {
         // this pass's activations, packed once for every CTA (into the workspace after the partial sums)
         const long long pairs = (long long)(K / C::KS) * C::NBLK * 8 * NT;
         cudaError_t e = spec::launch_pdl(xpack_kernel<NT>, dim3((unsigned)((pairs + 255) / 256)), dim3(256), 0, stream,
@@ -722,7 +697,7 @@ inline int super_pitch(int K) { return (K + 511) / 512 * 16; }
 spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
                     void *y, spec_dtype y_dt, int ldy, int accumulate, int seg512, int nt, void *workspace,
                     int32_t *dev_err, cudaStream_t stream, int fmt = SC_BLOCK, const int32_t *dev_cols = nullptr,
-                    int min_cols = 0, int wide = WIDE_AUTO) {
+                    int min_cols = 0, int wide = WIDE_AUTO, const uint8_t *xpk_in = nullptr) {
     CUtensorMap tw, ts;
     {
         uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)N};
@@ -754,9 +729,9 @@ spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint1
         spec_status st;
 #define SPEC_QMM_FMT(NTV, FMTV)                                                                                    \
     st = bf ? launch_nt<NTV, true, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err,    \
-                                         dev_cols, min_cols, stream)                                                  \
+                                         dev_cols, min_cols, stream, xpk_in)                                          \
             : launch_nt<NTV, false, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace,    \
-                                          dev_err, dev_cols, min_cols, stream)
+                                          dev_err, dev_cols, min_cols, stream, xpk_in)
 #define SPEC_QMM_CASE(NTV)                                                                                         \
     if (fmt == SC_BLOCK) {                                                                                         \
         SPEC_QMM_FMT(NTV, SC_BLOCK);                                                                              \
@@ -828,6 +803,29 @@ extern "C" spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N
     if (st != SPEC_OK) return st;
     return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, nt, workspace, dev_err,
                    (cudaStream_t)stream);
+}
+
+extern "C" size_t spec_packed_activation_bytes(int K) {
+    if (K < 256 || K % 256 != 0) return 0;
+    return (size_t)(K / WIDE_KS) * WIDE_XC_BYTES;
+}
+
+extern "C" spec_status spec_qmatmul_packed(const uint8_t *wq, const uint16_t *ws, int N, int K, const void *xpk,
+                                           int n_cols, void *y, spec_dtype y_dt, int ldy, int accumulate,
+                                           void *workspace, size_t ws_bytes, int32_t *dev_err, spec_stream_t stream) {
+    SPEC_CHECK_ARG(N >= 1 && K >= 256 && K % 256 == 0, "qmatmul_packed: need N >= 1 and K a multiple of 256 (N=%d K=%d)",
+                   N, K);
+    SPEC_CHECK_ARG(n_cols > 16 && n_cols <= WIDE_COLS, "qmatmul_packed: n_cols must be in 17..80 (n_cols=%d)", n_cols);
+    SPEC_CHECK_ARG(ldy >= N, "qmatmul_packed: ldy must be >= N (ldy=%d)", ldy);
+    SPEC_CHECK_ARG(wq && ws && xpk && y, "qmatmul_packed: NULL pointer");
+    SPEC_CHECK_ARG(spec::aligned16(wq) && spec::aligned16(ws) && spec::aligned16(xpk),
+                   "qmatmul_packed: wq, ws and xpk must be 16-byte aligned");
+    SPEC_CHECK_ARG(y_dt == SPEC_F32 || y_dt == SPEC_BF16, "qmatmul_packed: y_dt must be SPEC_F32 or SPEC_BF16");
+    SPEC_CHECK_ARG(!(accumulate && y_dt != SPEC_F32), "qmatmul_packed: accumulate needs SPEC_F32 output");
+    spec_status st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, MAX_NT, 1));
+    if (st != SPEC_OK) return st;
+    return qmm_run(wq, ws, N, K, nullptr, n_cols, K, y, y_dt, ldy, accumulate, 1, MAX_NT, workspace, dev_err,
+                   (cudaStream_t)stream, SC_BLOCK, nullptr, 0, WIDE_MMA_SYNC, reinterpret_cast<const uint8_t *>(xpk));
 }
 
 extern "C" spec_status spec_qmatmul_devcols(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,

@@ -26,6 +26,57 @@ constexpr int WIDE_COLS = 80;
 constexpr int WIDE_KS = 256;
 constexpr int WIDE_XC_BYTES = 4 * WIDE_COLS * 128 + 8 * WIDE_COLS * 4;
 
+// The mma.sync 80-column pass's packed activations (one 256-k stage: four
+// 64-k groups of 80 columns x 128 bytes in B-fragment order, then -136 x the
+// block sums, [8 blocks][80] fp32).  Producers of an 80-row K1 input may write
+// them directly (spec_add_rmsnorm_packed, spec_swiglu_packed) instead of
+// leaving it to the matmul's packing kernel; both go through pack_pair.
+constexpr int SYNC_WIDE_NT = 10;
+constexpr int SYNC_WIDE_X_BYTES = 4 * 8 * SYNC_WIDE_NT * 128;
+
+// Writes pair (blk, c) of a stage of a pass with NT column tiles: the bf16
+// values of column c at k = 32 blk .. 32 blk + 31 of the stage (v: 4 x 8 in k
+// order) in MMA B-fragment order into the stage's activation area xs, and
+// -136 x the block sum into ci (the block sum is the four 8-k chunk sums, each
+// summed in k order, added in chunk order).
+template <int NT>
+__device__ __forceinline__ void pack_pair(const uint4 (&v)[4], int blk, int c, uint8_t *xs, float *ci) {
+    constexpr int X_BOX = 8 * NT * 128;   // 64 k of the pass's columns
+    uint8_t *row = xs + (blk >> 1) * X_BOX + c * 128;
+    float sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+        float cs = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            cs += __uint_as_float(w4[e] << 16);
+            cs += __uint_as_float(w4[e] & 0xFFFF0000u);
+        }
+        sum = (q == 0) ? cs : sum + cs;
+        uint4 o;
+        o.x = dev::prmt(w4[0], w4[2], 0x5410);   // (x0, x4)
+        o.y = dev::prmt(w4[0], w4[2], 0x7632);   // (x1, x5)
+        o.z = dev::prmt(w4[1], w4[3], 0x5410);   // (x2, x6)
+        o.w = dev::prmt(w4[1], w4[3], 0x7632);   // (x3, x7)
+        const int chunk = (((blk & 1) * 4 + q) ^ (c & 7)) << 4;
+        *reinterpret_cast<uint4 *>(row + chunk) = o;
+    }
+    // MMA column slot g carries activation column pi(g) = (g & 1) * 4 + g / 2
+    const int cc = c & 7, slot = (cc & 3) * 2 + (cc >> 2);
+    ci[blk * 8 * NT + (c & ~7) + slot] = -136.0f * sum;
+}
+
+// Column c's 32 bf16 values at k = kb .. kb + 31 (kb a multiple of 32) into
+// the mma.sync 80-column pass's packed activations of all stages, xpk.
+__device__ __forceinline__ void pack_wide_block(const uint16_t *src, int kb, int c, uint8_t *xpk) {
+    uint4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const uint4 *>(src + 8 * q);
+    uint8_t *xs = xpk + (size_t)(kb / WIDE_KS) * WIDE_XC_BYTES;
+    pack_pair<SYNC_WIDE_NT>(v, (kb % WIDE_KS) / 32, c, xs, reinterpret_cast<float *>(xs + SYNC_WIDE_X_BYTES));
+}
+
 // Columns a call gated by a device-side count computes: none when the count is
 // below min_cols, else the first min(n_cols, count).
 __device__ __forceinline__ int gated_cols(int n_cols, const int32_t *dev_cols, int min_cols) {

@@ -90,6 +90,14 @@ class Decoder:
         shapes = [(self.nqkv, H), (H, self.Hq * self.D), (2 * F, H), (H, F), (self.V, H)]
         self.qws_bytes = max(L.spec_qmatmul_workspace(N, K, R) for N, K in shapes)
         self.qws = torch.zeros(self.qws_bytes // 4 + 64, dtype=torch.int32, device=d)   # zero once; calls keep it so
+        # an 80-column K1 pass's activations, packed by the producing kernel (RMSNorm, SwiGLU)
+        xpk_bytes = max(L.spec_packed_activation_bytes(H), L.spec_packed_activation_bytes(F))
+        self.xpk = torch.empty(xpk_bytes // 4 + 16, dtype=torch.int32, device=d)
+
+    @staticmethod
+    def _packed(R):
+        """Rows that make one 80-column K1 pass: their producers write the packed form."""
+        return 16 < R <= 80
 
     # ------------------------------------------------------------------
     def embed(self, tokens, R):
@@ -102,10 +110,10 @@ class Decoder:
         lay, H, F, D = self.layers[li], self.H, self.F, self.D
         max_kv_len = max_kv_len or self.max_len
         tr = trace or (lambda name: None)
-        L.spec_add_rmsnorm(self.h, None, lay["norm1"], R, H, self.cfg.eps, self.a)
+        pk = self._packed(R)
+        self._norm(lay["norm1"], R, pk)
         tr("norm1")
-        L.spec_qmatmul(lay["qkv"][0], lay["qkv"][1], self.nqkv, H, self.a, R, H, self.qkv, L.SPEC_F32,
-                       self.nqkv, 0, self.qws, self.qws_bytes, self.dev_err)
+        self._matmul(lay["qkv"], self.nqkv, H, self.a, R, self.qkv, 0, pk)
         tr("qkv")
         L.spec_rope_append(self.qkv, R, self.Hq, self.Hkv, D, self.rope, self.max_len, cu_rows, ctx, S, self.q,
                            self.k_cache[li], self.v_cache[li], self.pages, self.block_table, self.max_blocks,
@@ -118,16 +126,33 @@ class Decoder:
         L.spec_qmatmul(lay["o"][0], lay["o"][1], H, self.Hq * D, self.attn, R, self.Hq * D, self.h, L.SPEC_F32, H, 1,
                        self.qws, self.qws_bytes, self.dev_err)
         tr("o")
-        L.spec_add_rmsnorm(self.h, None, lay["norm2"], R, H, self.cfg.eps, self.a)
+        self._norm(lay["norm2"], R, pk)
         tr("norm2")
-        L.spec_qmatmul(lay["gu"][0], lay["gu"][1], 2 * F, H, self.a, R, H, self.gu, L.SPEC_F32, 2 * F,
-                       0, self.qws, self.qws_bytes, self.dev_err)
+        self._matmul(lay["gu"], 2 * F, H, self.a, R, self.gu, 0, pk)
         tr("gu")
-        L.spec_swiglu(self.gu, R, F, self.act)
+        if pk:
+            L.spec_swiglu_packed(self.gu, R, F, self.act, self.xpk)
+        else:
+            L.spec_swiglu(self.gu, R, F, self.act)
         tr("swiglu")
-        L.spec_qmatmul(lay["down"][0], lay["down"][1], H, F, self.act, R, F, self.h, L.SPEC_F32, H, 1,
-                       self.qws, self.qws_bytes, self.dev_err)
+        self._matmul(lay["down"], H, F, self.act, R, self.h, 1, pk)
         tr("down")
+
+    def _norm(self, w, R, pk):
+        """self.a = RMSNorm(self.h) * w (and its packed form when pk)."""
+        if pk:
+            L.spec_add_rmsnorm_packed(self.h, None, w, R, self.H, self.cfg.eps, self.a, self.xpk)
+        else:
+            L.spec_add_rmsnorm(self.h, None, w, R, self.H, self.cfg.eps, self.a)
+
+    def _matmul(self, wts, N, K, x, R, y, accumulate, pk):
+        """y (+)= W x over R rows; from the packed activations when pk (same bits)."""
+        if pk:
+            L.spec_qmatmul_packed(wts[0], wts[1], N, K, self.xpk, R, y, L.SPEC_F32, N, accumulate, self.qws,
+                                  self.qws_bytes, self.dev_err)
+        else:
+            L.spec_qmatmul(wts[0], wts[1], N, K, x, R, K, y, L.SPEC_F32, N, accumulate, self.qws, self.qws_bytes,
+                           self.dev_err)
 
     def enable_gate(self, capacity: int = 16):
         """Evaluate the LM head through the margin gate (tokenstrom.com, "'Lossless,'
@@ -150,12 +175,12 @@ class Decoder:
         self.gate = g
 
     def head(self, R, trace=None):
-        L.spec_add_rmsnorm(self.h, None, self.final_norm, R, self.H, self.cfg.eps, self.a)
+        pk = self._packed(R) and self.gate is None
+        self._norm(self.final_norm, R, pk)
         if trace:
             trace("final_norm")
         if self.gate is None:
-            L.spec_qmatmul(self.lm[0], self.lm[1], self.V, self.H, self.a, R, self.H, self.logits, L.SPEC_F32,
-                           self.V, 0, self.qws, self.qws_bytes, self.dev_err)
+            self._matmul(self.lm, self.V, self.H, self.a, R, self.logits, 0, pk)
             return
         g, H, V = self.gate, self.H, self.V
         L.spec_qmatmul_noninvariant(self.lm[0], self.lm[1], V, H, self.a, R, H, self.logits, V, 0, self.qws,

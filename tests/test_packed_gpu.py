@@ -1,0 +1,104 @@
+"""Activations packed by their producer for an 80-column K1 pass.
+
+spec_add_rmsnorm_packed / spec_swiglu_packed write the rows they produce both
+in the plain layout and in the packed stage layout of the 80-column pass;
+spec_qmatmul_packed runs that pass from the packed form.  Only the delivery of
+the activations changes (ramgpt.org, "When Lossless Speculation Stops Being
+Lossless on Blackwell", section "Quantized Matrix Multiplication Shows the
+Same Class of Failure"): the plain outputs and the products must equal the
+plain calls' bit for bit, and the product must match the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_util import TOL, bits_equal, dev, host, rel_err_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _L():
+    import invariant_speculative_verification_gb300 as L
+    return L
+
+
+def _matmul_pair(L, wq, ws, N, K, x, R, xpk, accumulate=0, y0=None):
+    """(plain spec_qmatmul, spec_qmatmul_packed) outputs [R][N] fp32."""
+    wsb = L.spec_qmatmul_workspace(N, K, R)
+    outs = []
+    for packed in (False, True):
+        wsp = torch.zeros(wsb // 4 + 64, dtype=torch.int32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        y = y0.clone() if y0 is not None else torch.zeros((R, N), dtype=torch.float32, device="cuda")
+        if packed:
+            L.spec_qmatmul_packed(wq, ws, N, K, xpk, R, y, L.SPEC_F32, N, accumulate, wsp, wsb, err)
+        else:
+            L.spec_qmatmul(wq, ws, N, K, x, R, K, y, L.SPEC_F32, N, accumulate, wsp, wsb, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append(y)
+    return outs
+
+
+@pytest.mark.parametrize("R", [17, 37, 80])
+def test_rmsnorm_packed_feeds_the_wide_pass_bit_for_bit(R):
+    L = _L()
+    g = np.random.default_rng(40 + R)
+    N, H = 3072, 2048
+    h = g.normal(0, 1, (R, H)).astype(np.float32)
+    w = g.normal(1, 0.1, H).astype(np.float32)
+    wq, ws = synth.qmatmul_weights(900 + R, N, H)
+    wqd, wsd = dev(wq), dev(ws)
+    plain = torch.zeros((R, H), dtype=torch.int16, device="cuda")
+    packed = torch.zeros((R, H), dtype=torch.int16, device="cuda")
+    xpk = torch.full((L.spec_packed_activation_bytes(H) // 4 + 16,), -1, dtype=torch.int32, device="cuda")
+    L.spec_add_rmsnorm(dev(h), None, dev(w), R, H, 1e-5, plain)
+    L.spec_add_rmsnorm_packed(dev(h), None, dev(w), R, H, 1e-5, packed, xpk)
+    torch.cuda.synchronize()
+    assert bits_equal(plain, packed)
+    y_plain, y_packed = _matmul_pair(L, wqd, wsd, N, H, plain, R, xpk)
+    assert bits_equal(y_plain, y_packed)
+    rows = [0, R // 2, R - 1]
+    ref = oracle.qmatmul(wq, ws, host(plain, np.uint16)[rows], N, H)
+    assert rel_err_rows(host(y_packed)[rows], ref) <= TOL
+
+
+@pytest.mark.parametrize("R", [23, 80])
+def test_swiglu_packed_feeds_the_wide_pass_bit_for_bit_with_accumulate(R):
+    L = _L()
+    g = np.random.default_rng(60 + R)
+    N, F = 2048, 5632
+    gu = g.normal(0, 2, (R, 2 * F)).astype(np.float32)
+    wq, ws = synth.qmatmul_weights(950 + R, N, F)
+    wqd, wsd = dev(wq), dev(ws)
+    plain = torch.zeros((R, F), dtype=torch.int16, device="cuda")
+    packed = torch.zeros((R, F), dtype=torch.int16, device="cuda")
+    xpk = torch.full((L.spec_packed_activation_bytes(F) // 4 + 16,), -1, dtype=torch.int32, device="cuda")
+    gud = dev(gu)
+    L.spec_swiglu(gud, R, F, plain)
+    L.spec_swiglu_packed(gud, R, F, packed, xpk)
+    torch.cuda.synchronize()
+    assert bits_equal(plain, packed)
+    y0 = torch.from_numpy(g.normal(0, 1, (R, N)).astype(np.float32)).cuda()
+    y_plain, y_packed = _matmul_pair(L, wqd, wsd, N, F, plain, R, xpk, accumulate=1, y0=y0)
+    assert bits_equal(y_plain, y_packed)
+
+
+def test_packed_arguments_are_checked():
+    L = _L()
+    xpk = torch.zeros(L.spec_packed_activation_bytes(2048) // 4 + 16, dtype=torch.int32, device="cuda")
+    wq, ws = synth.qmatmul_weights(7, 512, 2048)
+    y = torch.zeros((81, 512), dtype=torch.float32, device="cuda")
+    wsb = L.spec_qmatmul_workspace(512, 2048, 81)
+    wsp = torch.zeros(wsb // 4 + 64, dtype=torch.int32, device="cuda")
+    assert L.spec_packed_activation_bytes(1000) == 0
+    for n_cols in (16, 81):
+        with pytest.raises(L.SpecError):
+            L.spec_qmatmul_packed(dev(wq), dev(ws), 512, 2048, xpk, n_cols, y, L.SPEC_F32, 512, 0, wsp, wsb)
+    out = torch.zeros((81, 2048), dtype=torch.int16, device="cuda")
+    h = torch.zeros((81, 2048), dtype=torch.float32, device="cuda")
+    w = torch.ones(2048, dtype=torch.float32, device="cuda")
+    with pytest.raises(L.SpecError):
+        L.spec_add_rmsnorm_packed(h, None, w, 81, 2048, 1e-5, out, xpk)
