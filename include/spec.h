@@ -251,6 +251,18 @@ spec_status spec_flash_decode(const void *q, spec_dtype qkv_dt, int Hq, int Hkv,
                               void *workspace, size_t ws_bytes, int32_t *dev_err,
                               spec_stream_t stream);
 
+/* spec_flash_decode with bf16 output that also writes each output row r
+ * (Hq * D values), as column r of an 80-column K1 pass, in the packed form
+ * spec_qmatmul_packed reads (the o projection's input): xpk of
+ * spec_packed_activation_bytes(Hq * D) bytes, 16-byte aligned; R <= 80,
+ * Hq * D a multiple of 256.  out is written as by spec_flash_decode. */
+spec_status spec_flash_decode_packed(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, float scale,
+                                     const void *k_cache, const void *v_cache, int num_pages,
+                                     const int32_t *block_table, int max_blocks,
+                                     const int32_t *ctx_start, const int32_t *cu_rows, int S, int R,
+                                     int max_kv_len, void *out, void *workspace, size_t ws_bytes,
+                                     void *xpk, int32_t *dev_err, spec_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * K4  ragged greedy verification
  *

@@ -55,6 +55,8 @@ _SIGS = {
     "spec_add_rmsnorm_packed": (_i32, [_vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp]),
     "spec_swiglu_packed": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp]),
     "spec_packed_activation_bytes": (_sz, [_i32]),
+    "spec_flash_decode_packed": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32,
+                                        _i32, _i32, _vp, _vp, _sz, _vp, _vp, _vp]),
     "spec_qmatmul_packed": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "spec_cast_bf16": (_i32, [_vp, _sz, _vp, _vp]),
     "spec_ngram_draft": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
@@ -264,6 +266,15 @@ def spec_add_rmsnorm_packed(h, delta, w, R, H, eps, out, xpk, stream=None):
 
 def spec_swiglu_packed(gu, R, F, out, xpk, stream=None):
     _check("spec_swiglu_packed", load().spec_swiglu_packed(_ptr(gu), R, F, _ptr(out), _ptr(xpk), _stream(stream)))
+
+
+def spec_flash_decode_packed(q, qkv_dt, Hq, Hkv, D, scale, k_cache, v_cache, num_pages, block_table, max_blocks,
+                             ctx_start, cu_rows, S, R, max_kv_len, out, workspace, ws_bytes, xpk, dev_err=None,
+                             stream=None):
+    _check("spec_flash_decode_packed", load().spec_flash_decode_packed(
+        _ptr(q), qkv_dt, Hq, Hkv, D, float(scale), _ptr(k_cache), _ptr(v_cache), num_pages, _ptr(block_table),
+        max_blocks, _ptr(ctx_start), _ptr(cu_rows), S, R, max_kv_len, _ptr(out), _ptr(workspace), int(ws_bytes),
+        _ptr(xpk), _ptr(dev_err), _stream(stream)))
 
 
 def spec_packed_activation_bytes(K):

@@ -29,7 +29,7 @@
 // Which CTA computes an item, and when, is scheduling: an item's operations
 // are those of a CTA of its own.
 // K3 (attn_combine_kernel): one warp per (row, head).
-#include "common.cuh"
+#include "qmm_shared.cuh"
 
 namespace {
 
@@ -463,7 +463,7 @@ template <int D, bool OUT_BF16>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__restrict__ cu_rows, int S, int R, int Hq,
                     int nc_max, const float2 *__restrict__ part_ml, const float *__restrict__ part_o, void *out,
-                    int max_kv_len) {
+                    int max_kv_len, uint8_t *__restrict__ xpk) {
     dev::pdl_wait();
     dev::pdl_launch_dependents();
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -539,6 +539,15 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
         __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(out) + ob;
 #pragma unroll
         for (int e = 0; e < PER; ++e) o[e] = __float2bfloat16_rn(acc[e]);
+        if (xpk) {
+            // row r is column r of an 80-column K1 pass (the o projection): pack this
+            // head's 32-value blocks too, once the warp's stores are visible to it
+            __syncwarp();
+            if (lane < D / 32) {
+                const int kb = h * D + 32 * lane;
+                qmm::pack_wide_block(reinterpret_cast<const uint16_t *>(out) + (size_t)r * Hq * D + kb, kb, r, xpk);
+            }
+        }
     } else {
         float *o = reinterpret_cast<float *>(out) + ob;
 #pragma unroll
@@ -581,7 +590,8 @@ size_t attn_workspace_bytes(int R, int Hq, int D, int max_kv_len) {
 spec_status attn_run(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, float scale, const void *k_cache,
                      const void *v_cache, int num_pages, const int32_t *block_table, int max_blocks,
                      const int32_t *ctx_start, const int32_t *cu_rows, int S, int R, int max_kv_len, void *out,
-                     spec_dtype out_dt, void *workspace, int32_t *dev_err, cudaStream_t stream) {
+                     spec_dtype out_dt, void *workspace, int32_t *dev_err, cudaStream_t stream,
+                     uint8_t *xpk = nullptr) {
     const int nc_max = (max_kv_len + CHUNK - 1) / CHUNK;
     const size_t pairs = (size_t)R * Hq * nc_max;
     size_t mlb = (pairs * sizeof(float2) + 255) & ~size_t(255);
@@ -614,14 +624,14 @@ spec_status attn_run(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, f
     cudaError_t le;
     if (D == 128) {
         if (obf)
-            le = launch_pdl(attn_combine_kernel<128, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len);
+            le = launch_pdl(attn_combine_kernel<128, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, xpk);
         else
-            le = launch_pdl(attn_combine_kernel<128, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len);
+            le = launch_pdl(attn_combine_kernel<128, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, xpk);
     } else {
         if (obf)
-            le = launch_pdl(attn_combine_kernel<64, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len);
+            le = launch_pdl(attn_combine_kernel<64, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, xpk);
         else
-            le = launch_pdl(attn_combine_kernel<64, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len);
+            le = launch_pdl(attn_combine_kernel<64, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, xpk);
     }
     return cuda_status(le, "attn combine launch");
 }
@@ -668,4 +678,27 @@ extern "C" spec_status spec_flash_decode(const void *q, spec_dtype qkv_dt, int H
     return spec::attn_run(q, qkv_dt, Hq, Hkv, D, scale, k_cache, v_cache, num_pages, block_table, max_blocks,
                           ctx_start, cu_rows, S, R, max_kv_len, out, out_dt, workspace, dev_err,
                           (cudaStream_t)stream);
+}
+
+extern "C" spec_status spec_flash_decode_packed(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, float scale,
+                                                const void *k_cache, const void *v_cache, int num_pages,
+                                                const int32_t *block_table, int max_blocks, const int32_t *ctx_start,
+                                                const int32_t *cu_rows, int S, int R, int max_kv_len, void *out,
+                                                void *workspace, size_t ws_bytes, void *xpk, int32_t *dev_err,
+                                                spec_stream_t stream) {
+    spec_status st = spec::attn_check(q, qkv_dt, Hq, Hkv, D, k_cache, v_cache, num_pages, block_table, max_blocks,
+                                      ctx_start, cu_rows, S, R, max_kv_len, out, SPEC_BF16);
+    if (st != SPEC_OK) return st;
+    SPEC_CHECK_ARG(R <= qmm::WIDE_COLS && (Hq * D) % 256 == 0,
+                   "flash_decode_packed: need R <= 80 and Hq * D a multiple of 256 (R=%d Hq*D=%d)", R, Hq * D);
+    SPEC_CHECK_ARG(xpk && spec::aligned16(xpk) && spec::aligned16(out),
+                   "flash_decode_packed: xpk and out must be non-NULL and 16-byte aligned");
+    if (S == 0 || R == 0) return SPEC_OK;
+    const size_t need = spec::attn_workspace_bytes(R, Hq, D, max_kv_len);
+    if (!workspace || ws_bytes < need || !spec::aligned16(workspace))
+        return spec::fail(SPEC_ERR_WORKSPACE, "flash_decode_packed: workspace needs %zu bytes (16-byte aligned), got %zu",
+                          need, ws_bytes);
+    return spec::attn_run(q, qkv_dt, Hq, Hkv, D, scale, k_cache, v_cache, num_pages, block_table, max_blocks,
+                          ctx_start, cu_rows, S, R, max_kv_len, out, SPEC_BF16, workspace, dev_err,
+                          (cudaStream_t)stream, reinterpret_cast<uint8_t *>(xpk));
 }

@@ -91,7 +91,7 @@ class Decoder:
         self.qws_bytes = max(L.spec_qmatmul_workspace(N, K, R) for N, K in shapes)
         self.qws = torch.zeros(self.qws_bytes // 4 + 64, dtype=torch.int32, device=d)   # zero once; calls keep it so
         # an 80-column K1 pass's activations, packed by the producing kernel (RMSNorm, SwiGLU)
-        xpk_bytes = max(L.spec_packed_activation_bytes(H), L.spec_packed_activation_bytes(F))
+        xpk_bytes = max(L.spec_packed_activation_bytes(k) for k in (H, F, self.Hq * self.D))
         self.xpk = torch.empty(xpk_bytes // 4 + 16, dtype=torch.int32, device=d)
 
     @staticmethod
@@ -119,12 +119,17 @@ class Decoder:
                            self.k_cache[li], self.v_cache[li], self.pages, self.block_table, self.max_blocks,
                            None, None, self.dev_err)
         tr("rope")
-        L.spec_flash_decode(self.q, L.SPEC_BF16, self.Hq, self.Hkv, D, 1.0 / math.sqrt(D), self.k_cache[li],
-                            self.v_cache[li], self.pages, self.block_table, self.max_blocks, ctx, cu_rows, S, R,
-                            max_kv_len, self.attn, L.SPEC_BF16, self.attn_ws, self.ws_bytes, self.dev_err)
+        if pk:
+            L.spec_flash_decode_packed(self.q, L.SPEC_BF16, self.Hq, self.Hkv, D, 1.0 / math.sqrt(D),
+                                       self.k_cache[li], self.v_cache[li], self.pages, self.block_table,
+                                       self.max_blocks, ctx, cu_rows, S, R, max_kv_len, self.attn, self.attn_ws,
+                                       self.ws_bytes, self.xpk, self.dev_err)
+        else:
+            L.spec_flash_decode(self.q, L.SPEC_BF16, self.Hq, self.Hkv, D, 1.0 / math.sqrt(D), self.k_cache[li],
+                                self.v_cache[li], self.pages, self.block_table, self.max_blocks, ctx, cu_rows, S, R,
+                                max_kv_len, self.attn, L.SPEC_BF16, self.attn_ws, self.ws_bytes, self.dev_err)
         tr("attn")
-        L.spec_qmatmul(lay["o"][0], lay["o"][1], H, self.Hq * D, self.attn, R, self.Hq * D, self.h, L.SPEC_F32, H, 1,
-                       self.qws, self.qws_bytes, self.dev_err)
+        self._matmul(lay["o"], H, self.Hq * D, self.attn, R, self.h, 1, pk)
         tr("o")
         self._norm(lay["norm2"], R, pk)
         tr("norm2")

@@ -102,3 +102,38 @@ def test_packed_arguments_are_checked():
     w = torch.ones(2048, dtype=torch.float32, device="cuda")
     with pytest.raises(L.SpecError):
         L.spec_add_rmsnorm_packed(h, None, w, 81, 2048, 1e-5, out, xpk)
+
+
+def test_attention_packed_feeds_the_o_projection_bit_for_bit():
+    L = _L()
+    Hq, Hkv, D, S, W = 16, 4, 128, 16, 5
+    R = S * W
+    g = np.random.default_rng(77)
+    ctx = g.integers(100, 600, size=S).astype(np.int32)
+    c = synth.attention_case(78, rows=[W] * S, ctx=list(ctx), Hq=Hq, Hkv=Hkv, D=D, dt=synth.DT_BF16,
+                             q_std=1 / np.sqrt(D), scale=1.0)
+    max_len = int((ctx + W).max())
+    q, kc, vc, bt = dev(c.q), dev(c.k_cache), dev(c.v_cache), dev(c.block_table)
+    cs, cu = dev(c.ctx_start), dev(c.cu_rows)
+    wsb = L.spec_flash_decode_workspace(R, Hq, D, max_len)
+    xpk = torch.full((L.spec_packed_activation_bytes(Hq * D) // 4 + 16,), -1, dtype=torch.int32, device="cuda")
+    outs = []
+    for packed in (False, True):
+        ws = torch.empty(wsb // 4 + 64, dtype=torch.float32, device="cuda")
+        out = torch.zeros((R, Hq * D), dtype=torch.int16, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        args = (q, L.SPEC_BF16, Hq, Hkv, D, 1.0, kc, vc, c.k_cache.shape[0], bt, c.block_table.shape[1], cs, cu, S, R,
+                max_len, out)
+        if packed:
+            L.spec_flash_decode_packed(*args, ws, wsb, xpk, err)
+        else:
+            L.spec_flash_decode(*args, L.SPEC_BF16, ws, wsb, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append(out)
+    assert bits_equal(outs[0], outs[1])
+    N, K = 2048, Hq * D
+    wq, ws_ = synth.qmatmul_weights(79, N, K)
+    y0 = torch.from_numpy(g.normal(0, 1, (R, N)).astype(np.float32)).cuda()
+    y_plain, y_packed = _matmul_pair(L, dev(wq), dev(ws_), N, K, outs[0], R, xpk, accumulate=1, y0=y0)
+    assert bits_equal(y_plain, y_packed)
