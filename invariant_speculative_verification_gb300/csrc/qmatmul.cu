@@ -21,7 +21,8 @@
 // scheduling that may depend on the call; the arithmetic above never does.
 //
 // Execution: a persistent grid of one CTA per SM, each with eight consumer
-// warps (16 weight rows each, 128 rows per tile) and one TMA warp.  The
+// warps (128 rows per tile: 16 rows x all columns each in passes of up to 16
+// columns, 32 rows x 40 columns each in the 80-column pass) and one TMA warp.  The
 // (128-row tile x K-segment) units are dealt out in equal contiguous ranges
 // (stream-K), so every SM streams the same number of bytes; a matrix with
 // nearly one tile per SM gives each CTA one whole tile instead.  The TMA warp's
@@ -33,11 +34,12 @@
 // write them in MMA B-fragment order together with the block sums and hand the
 // stage on.  The 80-column pass uses 256-k stages (a segment is two stages;
 // only the delivery changes, not the arithmetic); its activations are packed
-// into that same layout once per call by xpack_kernel and copied in with the
+// into that same layout once per call by xpack_kernel (or beforehand by the
+// kernel that produced them: spec_qmatmul_packed) and copied in with the
 // stage by one cp.async.bulk.  Consumers issue only ldmatrix, 4 LOP3 + 3
 // shifts per 8 weights, lds, mma.sync and the FADD/FFMA of each block partial.
-// A tile covered by one CTA is folded in registers and written directly.  A tile shared by several CTAs: the CTAs
-// holding its later segments store their segment sums and count themselves
+// A tile covered by one CTA is folded in registers and written directly.  A
+// tile shared by several CTAs: the CTAs holding its later segments store their segment sums and count themselves
 // in, without waiting; the CTA holding the leading segments folds them in
 // segment order once all have arrived (the usual case when it gets there),
 // else leaves its prefix for whichever CTA arrives last.  No CTA waits for
