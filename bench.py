@@ -137,7 +137,7 @@ class ClockSampler:
 def count_launches(fn):
     """Number of kernels one call of fn launches (counted from the C-ABI calls it makes)."""
     from invariant_speculative_verification_gb300 import _lib as L
-    per_call = {"spec_flash_decode": 2, "spec_verify_greedy": 2}
+    per_call = {"spec_flash_decode": 2, "spec_flash_decode_packed": 2, "spec_verify_greedy": 2}
     counts = {}
     orig = {}
     for name in list(L._SIGS):
