@@ -511,6 +511,51 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                                 d_r8[rg] = super_scale(pi ? rec_r8[rg][1] : rec_r8[rg][0], blk & 7);
                             }
                         }
+                        if constexpr (NT >= MAX_NT) {
+                            // The 80-column pass: the ten chains of this warp (RG row groups x
+                            // CT column tiles) are issued together -- all first products, then
+                            // all second products, then the fmas -- so that no MMA waits on
+                            // the one just issued.  Every chain and every accumulator's
+                            // sequence of operations is the same as one chain at a time.
+                            uint32_t bq[CT][4];
+                            float cq[CT][2];
+#pragma unroll
+                            for (int ctl = 0; ctl < CT; ++ctl) {
+                                const int ct = ctb + ctl;
+                                const int xrow = ct * 8 + xcol;
+                                const int chunk = ((blk & 1) * 4 + t) ^ (xrow & 7);
+                                dev::lds128(bq[ctl][0], bq[ctl][1], bq[ctl][2], bq[ctl][3],
+                                            xbase + (blk >> 1) * C::X_BOX + xrow * 128 + (chunk << 4));
+                                asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                                             : "=f"(cq[ctl][0]), "=f"(cq[ctl][1])
+                                             : "r"(cbase + (blk * 8 * NT + ct * 8 + 2 * t) * 4));
+                            }
+                            const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+                            float pp[CT][RG][4];
+#pragma unroll
+                            for (int ctl = 0; ctl < CT; ++ctl)
+#pragma unroll
+                                for (int rg = 0; rg < RG; ++rg)
+                                    dev::mma_bf16(pp[ctl][rg], ar[rg][0], ar8[rg][0], ar[rg][1], ar8[rg][1], bq[ctl][0],
+                                                  bq[ctl][1], zero);
+#pragma unroll
+                            for (int ctl = 0; ctl < CT; ++ctl)
+#pragma unroll
+                                for (int rg = 0; rg < RG; ++rg)
+                                    dev::mma_bf16(pp[ctl][rg], ar[rg][2], ar8[rg][2], ar[rg][3], ar8[rg][3], bq[ctl][2],
+                                                  bq[ctl][3], pp[ctl][rg]);
+#pragma unroll
+                            for (int ctl = 0; ctl < CT; ++ctl)
+#pragma unroll
+                                for (int rg = 0; rg < RG; ++rg) {
+                                    float(&a4)[4] = acc[rg * CT + ctl];
+                                    dev::fma_add_f32x2(a4[0], a4[1], d_r[rg], pp[ctl][rg][0], pp[ctl][rg][1],
+                                                       cq[ctl][0], cq[ctl][1]);
+                                    dev::fma_add_f32x2(a4[2], a4[3], d_r8[rg], pp[ctl][rg][2], pp[ctl][rg][3],
+                                                       cq[ctl][0], cq[ctl][1]);
+                                }
+                            continue;
+                        }
 #pragma unroll
                         for (int ctl = 0; ctl < CT; ++ctl) {
                             const int ct = ctb + ctl;   // column tile of the pass
