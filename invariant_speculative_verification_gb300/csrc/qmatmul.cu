@@ -75,7 +75,10 @@ struct Cfg {
     static constexpr int NWBOX = KS / 256;                  // code boxes per stage
     static constexpr bool XPACK = NT >= 10;                 // activations pre-packed per call
     static constexpr int NXW = XPACK ? 0 : 2;               // activation warps
-    static constexpr int THREADS = (NCW + 1 + NXW) * 32;    // + TMA warp
+    // a TMA warp, except in the 80-column pass, where consumer warp 0 issues the
+    // copies: with eight warps a thread may hold 255 registers, with nine 168
+    static constexpr int NTMA = XPACK ? 0 : 1;
+    static constexpr int THREADS = (NCW + NTMA + NXW) * 32;
     static constexpr int W_BYTES = NWBOX * W_BOX;
     // scales of a stage: fp16 per block, or the row's 16-byte record pair holding the stage
     static constexpr int S_BYTES = FMT == SC_BLOCK ? BM * NBLK * 2 : BM * 16;
@@ -204,7 +207,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     // stage sequence of this CTA: units ua..ub-1, each 1 or 2 stages
     auto unit_stages = [&](long long u) { return min(seg_st, nst_total - (int)(u % ks) * seg_st); };
 
-    if (warp == NCW) {
+    if (!C::XPACK && warp == NCW) {
         // ============================ TMA warp ============================
         // lane 0 streams the codes (two 128-row x 128-byte boxes per 512-k stage)
         // and the scales of every stage of this CTA, NS stages ahead of the
@@ -214,20 +217,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             dev::prefetch_tmap(&ts);
             long long iu = ua;
             int ist = 0;
-            int k0s[C::NS];   // packed-activation pass: stages whose activations are still to be copied
-            bool x_sent = false;
-            int issued = 0;
-            for (; iu < ub; ++issued) {
+            for (int issued = 0; iu < ub; ++issued) {
                 const int s = issued % C::NS;
-                if (issued == C::NS && C::XPACK) {
-                    x_sent = true;
-                    // the first NS stages' weights are on their way; the packed activations
-                    // are written by the preceding kernel, so wait for it before copying them
-                    dev::pdl_wait();
-                    for (int j = 0; j < C::NS; ++j)
-                        dev::bulk_load(smem + j * C::STAGE + C::X_OFF, xpk + (size_t)(k0s[j] / C::KS) * C::XC_BYTES,
-                                       C::XC_BYTES, &full[j]);
-                }
                 if (issued >= C::NS && !dev::mbar_wait(&empty[s], ((issued / C::NS) - 1) & 1)) {
                     dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     break;
@@ -235,7 +226,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                 const int tile = (int)(iu / ks);
                 const int k0 = ((int)(iu % ks) * seg_st + ist) * C::KS;
                 uint8_t *base = smem + s * C::STAGE;
-                dev::mbar_arrive_expect_tx(&full[s], C::W_BYTES + C::S_BYTES + (C::XPACK ? C::XC_BYTES : 0));
+                dev::mbar_arrive_expect_tx(&full[s], C::W_BYTES + C::S_BYTES);
 #pragma unroll
                 for (int b = 0; b < C::NWBOX; ++b)
                     dev::tma_load_2d(base + b * W_BOX, &tw, k0 / 2 + 128 * b, tile * BM, &full[s]);
@@ -243,23 +234,10 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                     dev::tma_load_2d(base + C::S_OFF, &ts, k0 / 32, tile * BM, &full[s]);
                 else   // the 16-byte record pair holding this stage's super-block(s)
                     dev::tma_load_2d(base + C::S_OFF, &ts, (k0 / 512) * 16, tile * BM, &full[s]);
-                if (C::XPACK) {
-                    if (issued < C::NS)
-                        k0s[issued] = k0;
-                    else
-                        dev::bulk_load(base + C::X_OFF, xpk + (size_t)(k0 / C::KS) * C::XC_BYTES, C::XC_BYTES, &full[s]);
-                }
                 if (++ist == unit_stages(iu)) {
                     ist = 0;
                     ++iu;
                 }
-            }
-            if (C::XPACK && !x_sent) {
-                // no more stages than slots: copy the activations of all of them now
-                dev::pdl_wait();
-                for (int j = 0; j < issued; ++j)
-                    dev::bulk_load(smem + j * C::STAGE + C::X_OFF, xpk + (size_t)(k0s[j] / C::KS) * C::XC_BYTES,
-                                   C::XC_BYTES, &full[j]);
             }
         }
         return;
@@ -330,7 +308,57 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     }
 
     // ============================ consumers ============================
-    dev::pdl_wait();   // y (accumulate), the workspace and y writes follow the preceding kernel
+    // The 80-column pass: lane 0 of warp 0 issues the copies.  It sends the
+    // first NS stages' codes and scales at once (constant inputs), their packed
+    // activations once the preceding kernel has finished, and, at the start of
+    // each later stage i, stage i - 1 + NS into the slot that stage i - 1 has
+    // released.  The cursor is kept by every lane of warp 0, so that its
+    // decisions are warp-uniform.
+    int my_stages = 0, issued = 0;
+    long long p_iu = ua;
+    int p_ist = 0;
+    int k0s[C::NS];   // the first stages, whose activations are copied after pdl_wait
+    auto issue_stage = [&](bool with_x) {
+        const int s = issued % C::NS;
+        const int k0 = ((int)(p_iu % ks) * seg_st + p_ist) * C::KS;
+        if (lane == 0) {
+            const int tile = (int)(p_iu / ks);
+            uint8_t *base = smem + s * C::STAGE;
+            dev::mbar_arrive_expect_tx(&full[s], C::W_BYTES + C::S_BYTES + C::XC_BYTES);
+#pragma unroll
+            for (int b = 0; b < C::NWBOX; ++b)
+                dev::tma_load_2d(base + b * W_BOX, &tw, k0 / 2 + 128 * b, tile * BM, &full[s]);
+            if constexpr (FMT == SC_BLOCK)
+                dev::tma_load_2d(base + C::S_OFF, &ts, k0 / 32, tile * BM, &full[s]);
+            else
+                dev::tma_load_2d(base + C::S_OFF, &ts, (k0 / 512) * 16, tile * BM, &full[s]);
+            if (with_x)
+                dev::bulk_load(base + C::X_OFF, xpk + (size_t)(k0 / C::KS) * C::XC_BYTES, C::XC_BYTES, &full[s]);
+        }
+        if (!with_x) k0s[issued] = k0;
+        if (++p_ist == unit_stages(p_iu)) {
+            p_ist = 0;
+            ++p_iu;
+        }
+        ++issued;
+    };
+    if constexpr (C::XPACK) {
+        for (long long uu = ua; uu < ub; ++uu) my_stages += unit_stages(uu);
+        if (warp == 0) {
+            if (lane == 0) {
+                dev::prefetch_tmap(&tw);
+                dev::prefetch_tmap(&ts);
+            }
+            while (issued < my_stages && issued < C::NS) issue_stage(false);
+        }
+    }
+    dev::pdl_wait();   // y (accumulate), the workspace, y writes and the packed activations follow the preceding kernel
+    if constexpr (C::XPACK) {
+        if (warp == 0 && lane == 0)
+            for (int j = 0; j < issued; ++j)
+                dev::bulk_load(smem + j * C::STAGE + C::X_OFF, xpk + (size_t)(k0s[j] / C::KS) * C::XC_BYTES,
+                               C::XC_BYTES, &full[j]);
+    }
     const int r = lane >> 2, t = lane & 3;
     // A consumer warp owns RG 16-row groups x CT 8-column tiles (RG x CT = NT
     // fragments f = rg * CT + ctl).  Narrow passes: one row group, all columns.
@@ -446,6 +474,20 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
             for (int ct = 0; ct < NT; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
             for (int st = 0; st < nstg; ++st, ++i) {
                 const int s = i % C::NS;
+                if constexpr (C::XPACK) {
+                    // stage i - 1 + NS into the slot of stage i - 1, once every consumer warp released it
+                    if (warp == 0 && i >= 1 && issued < my_stages && ok) {
+                        int got = 1;
+                        if (lane == 0) got = dev::mbar_wait(&empty[issued % C::NS], ((issued / C::NS) - 1) & 1) ? 1 : 0;
+                        got = __shfl_sync(0xffffffffu, got, 0);
+                        if (got) {
+                            issue_stage(true);
+                        } else {
+                            if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
+                            ok = false;
+                        }
+                    }
+                }
                 if (ok && !dev::mbar_wait(C::XPACK ? &full[s] : &ready[s], (i / C::NS) & 1)) {
                     dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     ok = false;
@@ -554,8 +596,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                                     dev::fma_add_f32x2(a4[2], a4[3], d_r8[rg], pp[ctl][rg][2], pp[ctl][rg][3],
                                                        cq[ctl][0], cq[ctl][1]);
                                 }
-                            continue;
-                        }
+                        } else {
 #pragma unroll
                         for (int ctl = 0; ctl < CT; ++ctl) {
                             const int ct = ctb + ctl;   // column tile of the pass
@@ -577,6 +618,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                                 dev::fma_add_f32x2(a4[0], a4[1], d_r[rg], p[0], p[1], c0, c1);
                                 dev::fma_add_f32x2(a4[2], a4[3], d_r8[rg], p[2], p[3], c0, c1);
                             }
+                        }
                         }
                     }
                 }
@@ -683,6 +725,13 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
         fold_tile(tile, (int)(head_end - tile_u0));
 #pragma unroll
         for (int ct = 0; ct < NT; ++ct) clear_low(pp + ct * NCW * 128, fcol(ct) < n_cols);
+    }
+    if constexpr (C::XPACK) {
+        // after a timeout some issued stages may not have been waited for: their
+        // copies land before the CTA exits (bounded; at once otherwise)
+        if (warp == 0 && lane == 0)
+            for (int j = (issued > C::NS ? issued - C::NS : 0); j < issued; ++j)
+                if (!dev::mbar_wait(&full[j % C::NS], (j / C::NS) & 1)) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
     }
 }
 
