@@ -22,14 +22,16 @@
 //
 // Execution: a persistent grid of one CTA per SM, each with eight consumer
 // warps (128 rows per tile: 16 rows x all columns each in passes of up to 16
-// columns, 32 rows x 40 columns each in the 80-column pass) and one TMA warp.  The
-// (128-row tile x K-segment) units are dealt out in equal contiguous ranges
-// (stream-K), so every SM streams the same number of bytes; a matrix with
-// nearly one tile per SM gives each CTA one whole tile instead.  The TMA warp's
-// lane 0 issues cp.async.bulk.tensor copies of each stage -- the int4 codes
-// (128-row x 128-byte boxes, 128B swizzle) and the scales (fp16 per block, or
-// the super-block records of spec_qmatmul_sb) -- into a ring of
-// mbarrier-guarded stages.  Passes of up to 16 columns use 512-k stages and
+// columns, 32 rows x 40 columns each in the 80-column pass).  The (128-row tile
+// x K-segment) units are dealt out in equal contiguous ranges (stream-K), so
+// every SM streams the same number of bytes; a matrix with nearly one tile per
+// SM gives each CTA one whole tile instead.  One lane issues cp.async.bulk.tensor
+// copies of each stage -- the int4 codes (128-row x 128-byte boxes, 128B
+// swizzle) and the scales (fp16 per block, or the super-block records of
+// spec_qmatmul_sb) -- into a ring of mbarrier-guarded stages: lane 0 of a TMA
+// warp in the narrow passes, lane 0 of consumer warp 0 in the 80-column pass
+// (eight warps let a thread hold 255 registers, nine only 168; that pass's
+// consumers issue each warp's ten MMA chains together and need them).  Passes of up to 16 columns use 512-k stages and
 // two activation warps, which read the stage's activation columns from L2,
 // write them in MMA B-fragment order together with the block sums and hand the
 // stage on.  The 80-column pass uses 256-k stages (a segment is two stages;
