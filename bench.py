@@ -141,19 +141,26 @@ def count_launches(fn):
     counts = {}
     orig = {}
     for name in list(L._SIGS):
-        if not name.startswith("spec_") or name.endswith("_workspace") or name in ("spec_status_string",
-                                                                                  "spec_last_error"):
-            continue
+        if not name.startswith("spec_") or name.endswith("_workspace") or name in (
+                "spec_status_string", "spec_last_error", "spec_qmatmul_plan", "spec_packed_activation_bytes"):
+            continue   # host-only queries launch nothing
         if not hasattr(L, name):
             continue
         f = getattr(L, name)
         orig[name] = f
 
         def wrap(*a, _n=name, _f=f, **k):
-            if _n == "spec_qmatmul":   # one launch per pass of 8 or 16 columns, two (pack + matmul) per 80
-                nc = int(a[5])
-                per = 8 if nc <= 8 else (16 if nc <= 16 else 80)
-                counts[_n] = counts.get(_n, 0) + (nc + per - 1) // per * (2 if nc > 16 else 1)
+            if _n == "spec_qmatmul":
+                # up to 16 columns: one launch; 17 to 80: one launch of column groups, or
+                # pack + 80-column pass (spec_qmatmul_plan tells which); more: pack + pass per 80
+                N, K, nc = int(a[2]), int(a[3]), int(a[5])
+                if nc <= 16:
+                    n = 1
+                elif nc <= 80:
+                    n = 2 if L.spec_qmatmul_plan(N, K, nc, False) == 80 else 1
+                else:
+                    n = 2 * ((nc + 79) // 80)
+                counts[_n] = counts.get(_n, 0) + n
             else:
                 counts[_n] = counts.get(_n, 0) + 1
             return _f(*a, **k)

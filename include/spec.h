@@ -94,8 +94,9 @@ const char *spec_last_error(void);
  *        accumulate != 0 adds into y (SPEC_F32 only): y = fp32(y + result).
  *   workspace  at least spec_qmatmul_workspace(N, K, n_cols) bytes, 16-byte
  *        aligned, zero-filled before its first use (cudaMemset once).  A call
- *        keeps one arrival counter per 128 rows in the first 4 ceil(N/128)
- *        bytes; every call that returns SPEC_OK and reports no
+ *        keeps one arrival counter per 128 rows and column group (at most
+ *        10 groups, only while they fit in 64 KB) at the workspace's start;
+ *        every call that returns SPEC_OK and reports no
  *        SPEC_DEVERR_TIMEOUT leaves the first 64 KB zero again (counters reset,
  *        consumed partial sums cleared), so one workspace serves any sequence
  *        of calls of any shapes on one stream; calls that overlap on the GPU
@@ -112,6 +113,12 @@ const char *spec_last_error(void);
  * one chain of two m16n8k16 MMAs, scaled by its fp16 scale into an fp32
  * accumulator in ascending block order; segment partials are added in
  * ascending segment order.
+ *
+ * Passes: up to 8 columns run as one 8-column pass, up to 16 as one 16-column
+ * pass; 17 to 80 columns as the cheapest (by a fitted time estimate) of one
+ * 80-column pass and one launch of 16- or 8-column groups; more as 80-column
+ * passes.  The plan changes only
+ * which CTA computes a column, never its arithmetic.
  * ---------------------------------------------------------------------- */
 size_t spec_qmatmul_workspace(int N, int K, int n_cols);
 spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
@@ -133,6 +140,14 @@ spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
  * Blackwell", section "Quantized Matrix Multiplication Shows the Same Class of
  * Failure" (only the delivery of the activations changes). */
 size_t spec_packed_activation_bytes(int K);
+
+/* The pass width spec_qmatmul would take for n_cols columns of an N x K
+ * matrix: 8, 16 (column groups of that width in one launch) or 80 (the
+ * 80-column pass).  packed_input != 0 asks as for a caller that holds the
+ * packed activations of spec_qmatmul_packed (the 80-column pass then needs no
+ * packing launch): 80 means that entry point is the faster call, anything else
+ * that spec_qmatmul is.  0 for an empty or invalid shape.  Host only. */
+int spec_qmatmul_plan(int N, int K, int n_cols, int packed_input);
 spec_status spec_qmatmul_packed(const uint8_t *wq, const uint16_t *ws, int N, int K, const void *xpk,
                                 int n_cols, void *y, spec_dtype y_dt, int ldy, int accumulate,
                                 void *workspace, size_t ws_bytes, int32_t *dev_err, spec_stream_t stream);

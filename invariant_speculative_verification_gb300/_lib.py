@@ -55,6 +55,7 @@ _SIGS = {
     "spec_add_rmsnorm_packed": (_i32, [_vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp]),
     "spec_swiglu_packed": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp]),
     "spec_packed_activation_bytes": (_sz, [_i32]),
+    "spec_qmatmul_plan": (_i32, [_i32, _i32, _i32, _i32]),
     "spec_flash_decode_packed": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32,
                                         _i32, _i32, _vp, _vp, _sz, _vp, _vp, _vp]),
     "spec_qmatmul_packed": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
@@ -279,6 +280,10 @@ def spec_flash_decode_packed(q, qkv_dt, Hq, Hkv, D, scale, k_cache, v_cache, num
 
 def spec_packed_activation_bytes(K):
     return int(load().spec_packed_activation_bytes(int(K)))
+
+
+def spec_qmatmul_plan(N, K, n_cols, packed_input=False) -> int:
+    return int(load().spec_qmatmul_plan(int(N), int(K), int(n_cols), 1 if packed_input else 0))
 
 
 def spec_qmatmul_packed(wq, ws, N, K, xpk, n_cols, y, y_dt, ldy, accumulate, workspace, ws_bytes, dev_err=None,

@@ -225,7 +225,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                     dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     break;
                 }
-                const int tile = (int)(iu / ks);
+                const int tile = (int)(iu / ks) / sch.ncg;   // 128-row tile
                 const int k0 = ((int)(iu % ks) * seg_st + ist) * C::KS;
                 uint8_t *base = smem + s * C::STAGE;
                 dev::mbar_arrive_expect_tx(&full[s], C::W_BYTES + C::S_BYTES);
@@ -258,6 +258,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
         int pst = 0;
         for (int i = 0; pu < ub; ++i) {
             const int k0 = ((int)(pu % ks) * seg_st + pst) * C::KS;
+            const int cb = col0 + (int)((pu / ks) % sch.ncg) * 8 * NT;   // the unit's column group
             if (++pst == unit_stages(pu)) {
                 pst = 0;
                 ++pu;
@@ -277,7 +278,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
                 for (int jj = 0; jj < GROUP; ++jj) {
                     const int p = lane + 32 * (j0 + jj);
                     const int blk = p / (8 * NT), c = p % (8 * NT);
-                    load_pair(v[jj], x, ldx, K, n_cols, col0 + c, k0 + 32 * blk);
+                    load_pair(v[jj], x, ldx, K, n_cols, cb + c, k0 + 32 * blk);
                 }
                 if (!slot_free) {   // loads are in flight; now wait for the consumers' release
                     int got = 1;
@@ -324,7 +325,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
         const int s = issued % C::NS;
         const int k0 = ((int)(p_iu % ks) * seg_st + p_ist) * C::KS;
         if (lane == 0) {
-            const int tile = (int)(p_iu / ks);
+            const int tile = (int)(p_iu / ks) / sch.ncg;
             uint8_t *base = smem + s * C::STAGE;
             dev::mbar_arrive_expect_tx(&full[s], C::W_BYTES + C::S_BYTES + C::XC_BYTES);
 #pragma unroll
@@ -374,7 +375,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     static_assert(RG * CT == NT && RSLOTS * 16 * RG == BM, "consumer mapping");
     const int wrow0 = (warp % RSLOTS) * 16 * RG;         // row group rg starts at wrow0 + 16 rg
     const int ctb = (warp / RSLOTS) * CT;                 // first column tile of this warp
-    auto fcol = [&](int f) { return col0 + (ctb + f % CT) * 8; };   // first column of fragment f
+    int colb = col0;   // first column of the current tile's column group
+    auto fcol = [&](int f) { return colb + (ctb + f % CT) * 8; };   // first column of fragment f
     const int g = lane >> 2;
     const int xcol = (g & 1) * 4 + (g >> 1);   // activation column of this lane's B fragment
     float yrun[NT][4];
@@ -386,7 +388,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     // y for this thread's fragments of `tile` from yrun
     auto store_tile = [&](int tile) {
         auto store_y = [&](int c, int row, float v) {
-            const int col = col0 + c, n = tile * BM + row;
+            const int col = colb + c, n = (tile / sch.ncg) * BM + row;
             if (col < n_cols && n < N) {
                 if (OUT_BF16) {
                     reinterpret_cast<__nv_bfloat16 *>(y)[(size_t)col * ldy + n] = __float2bfloat16_rn(v);
@@ -462,6 +464,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
 
     while (u < ub) {
         const int tile = (int)(u / ks);
+        colb = col0 + (tile % sch.ncg) * 8 * NT;
         const long long tile_u0 = (long long)tile * ks;
         const long long u_end = min(ub, tile_u0 + ks);     // this CTA's units of this tile
         const bool head = (u == tile_u0);
@@ -713,6 +716,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     named_sync_consumers();
     if (flag[0]) {
         const int tile = flag[1];
+        colb = col0 + (tile % sch.ncg) * 8 * NT;
         const long long tile_u0 = (long long)tile * ks;
         const int head_cta = sch.cta_of(tile_u0);
         const long long head_end = min(sch.begin(head_cta + 1), tile_u0 + ks);
@@ -742,14 +746,14 @@ template <int NT, bool OUT_BF16, int FMT>
 spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N, int K,
                       int n_cols, int col0, void *y, int ldy, int accumulate, int seg512, void *workspace,
                       int32_t *dev_err, const int32_t *dev_cols, int min_cols, cudaStream_t stream,
-                      const uint8_t *xpk_in = nullptr) {
+                      const uint8_t *xpk_in = nullptr, int ncg = 1) {
     using C = Cfg<NT, FMT>;
     auto kern = qmm_kernel<NT, OUT_BF16, FMT>;
     static spec::SmemOptIn opt_in;
     spec_status so = spec::smem_opt_in(kern, C::SMEM, opt_in, "cudaFuncSetAttribute(qmm smem)");
     if (so != SPEC_OK) return so;
     const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
-    const Sched sch = make_sched(N, K, seg512, C::KS, sms);
+    const Sched sch = make_sched(N, K, seg512, C::KS, sms, C::XPACK ? 1 : ncg);
     const WsLayout wl = ws_layout(workspace, sch.tiles, sch.ks, BM * 8 * NT);
     int *counters = wl.counters;
     float *prefix = wl.prefix, *segs = wl.segs;
@@ -781,12 +785,78 @@ constexpr int WIDE_AUTO = 0, WIDE_TC = 1, WIDE_MMA_SYNC = 2;
 
 int pass_nt(int n_cols) { return n_cols <= 8 ? 1 : (n_cols <= 16 ? 2 : MAX_NT); }
 
-size_t ws_bytes_for(int N, int K, int nt, int seg512) {
-    const size_t tiles = (size_t)(N + BM - 1) / BM;
+// workspace of one launch of nt column tiles per column group, ncg column groups
+size_t ws_bytes_launch(int N, int K, int nt, int ncg, int seg512) {
+    const size_t tiles = (size_t)(N + BM - 1) / BM * ncg;
     const size_t cnt = ((tiles * sizeof(int)) + 255) & ~size_t(255);
     // the 80-column pass also keeps its packed activations: K / 256 stages of XC_BYTES
     const size_t packed = nt >= MAX_NT ? (size_t)(K / Cfg<MAX_NT>::KS) * Cfg<MAX_NT>::XC_BYTES : 0;
     return cnt + tiles * (1 + (size_t)n_segments(K, seg512 * SEG_K)) * BM * 8 * nt * sizeof(float) + packed;
+}
+
+// Column groups of one 16-column-pass launch that covers up to 80 columns.
+constexpr int MAX_NCG = MAX_NT / 2;
+
+size_t ws_bytes_for(int N, int K, int nt, int seg512) { return ws_bytes_launch(N, K, nt, 1, seg512); }
+
+// The passes of a call: nt column tiles per pass, ncg column groups per launch.
+// Every plan gives the same bits -- a column's arithmetic does not depend on the
+// pass that computes it -- so the plan decides only the time.
+struct Plan {
+    int nt, ncg;
+};
+
+// Estimated time (us) of a call planned as `p`: per launch a fixed cost plus,
+// for the CTA with the most units, its units x the time of one unit (512 k x
+// 128 rows of one column group).  Least-squares fit on GB300 over ten shapes
+// from 1024 x 4096 to 32000 x 2048 at 32 to 80 columns; the 80-column pass
+// also packs its activations in a launch of its own unless the caller's
+// producer did.
+double plan_cost(int N, int K, int n_cols, Plan p, bool packed_input) {
+    const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
+    const int per_launch = 8 * p.nt * (p.nt < MAX_NT ? p.ncg : 1);
+    const int launches = (n_cols + per_launch - 1) / per_launch;
+    const Sched sch = make_sched(N, K, 1, p.nt >= MAX_NT ? Cfg<MAX_NT>::KS : Cfg<1>::KS, sms, p.ncg);
+    const long long busiest = (sch.U + sch.G - 1) / sch.G;
+    double fixed, unit;
+    if (p.nt >= MAX_NT)
+        fixed = 6.9 + (packed_input ? 0.0 : 6.0), unit = 6.11;
+    else if (p.nt == 2)
+        fixed = 6.3, unit = 2.07;
+    else
+        fixed = 5.4, unit = 1.36;
+    return launches * (fixed + busiest * unit);
+}
+
+// Up to 8 columns: one 8-column pass; up to 16: one 16-column pass.  Up to
+// 80: the cheapest of the 80-column pass and one launch of 16- or 8-column
+// groups.  More: 80-column passes.
+Plan choose_plan(int N, int K, int n_cols, bool packed_input) {
+    if (n_cols <= 8) return {1, 1};
+    if (n_cols <= 16) return {2, 1};
+    if (n_cols > WIDE_COLS) return {MAX_NT, 1};
+    const size_t tiles = (size_t)(N + BM - 1) / BM;
+    Plan best = {2, 1};
+    double best_t = 1e30;
+    const Plan cands[3] = {{MAX_NT, 1}, {2, (n_cols + 15) / 16}, {1, (n_cols + 7) / 8}};
+    for (const Plan &p : cands) {
+        if (tiles * p.ncg * sizeof(int) > CNT_LIMIT) continue;
+        const double t = plan_cost(N, K, n_cols, p, packed_input);
+        if (t < best_t) best = p, best_t = t;
+    }
+    return best;
+}
+
+// Workspace for every plan a call of n_cols columns may take.
+size_t ws_bytes_cols(int N, int K, int n_cols) {
+    size_t need = ws_bytes_for(N, K, pass_nt(n_cols), 1);
+    if (n_cols > 16 && n_cols <= WIDE_COLS) {
+        const size_t g16 = ws_bytes_launch(N, K, 2, (n_cols + 15) / 16, 1);
+        const size_t g8 = ws_bytes_launch(N, K, 1, (n_cols + 7) / 8, 1);
+        need = need > g16 ? need : g16;
+        need = need > g8 ? need : g8;
+    }
+    return need;
 }
 
 // bytes of super-block scale records per weight row
@@ -795,7 +865,7 @@ inline int super_pitch(int K) { return (K + 511) / 512 * 16; }
 spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
                     void *y, spec_dtype y_dt, int ldy, int accumulate, int seg512, int nt, void *workspace,
                     int32_t *dev_err, cudaStream_t stream, int fmt = SC_BLOCK, const int32_t *dev_cols = nullptr,
-                    int min_cols = 0, int wide = WIDE_AUTO, const uint8_t *xpk_in = nullptr) {
+                    int min_cols = 0, int wide = WIDE_AUTO, const uint8_t *xpk_in = nullptr, int ncg = 1) {
     CUtensorMap tw, ts;
     {
         uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)N};
@@ -822,14 +892,19 @@ spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint1
             return SPEC_ERR_CUDA;
     }
     const bool bf = (y_dt == SPEC_BF16);
-    // one pass per group of 8 nt columns; passes run back to back on the stream
-    for (int col0 = 0; col0 < n_cols; col0 += 8 * nt) {
+    // column groups only while their arrival counters fit where counters may lie
+    if ((size_t)((N + BM - 1) / BM) * ncg * sizeof(int) > CNT_LIMIT) ncg = 1;
+    // One pass per group of 8 nt columns; passes run back to back on the stream.
+    // With ncg > 1 (narrow passes only), one launch covers ncg such groups.
+    const int step = 8 * nt * (nt < MAX_NT ? ncg : 1);
+    for (int col0 = 0; col0 < n_cols; col0 += step) {
         spec_status st;
+        const int g = nt < MAX_NT ? min(ncg, (n_cols - col0 + 8 * nt - 1) / (8 * nt)) : 1;
 #define SPEC_QMM_FMT(NTV, FMTV)                                                                                    \
     st = bf ? launch_nt<NTV, true, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err,    \
-                                         dev_cols, min_cols, stream, xpk_in)                                          \
+                                         dev_cols, min_cols, stream, xpk_in, g)                                       \
             : launch_nt<NTV, false, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace,    \
-                                          dev_err, dev_cols, min_cols, stream, xpk_in)
+                                          dev_err, dev_cols, min_cols, stream, xpk_in, g)
 #define SPEC_QMM_CASE(NTV)                                                                                         \
     if (fmt == SC_BLOCK) {                                                                                         \
         SPEC_QMM_FMT(NTV, SC_BLOCK);                                                                              \
@@ -884,8 +959,8 @@ spec_status check_ws(const void *workspace, size_t ws_bytes, size_t need) {
 
 extern "C" size_t spec_qmatmul_workspace(int N, int K, int n_cols) {
     if (N <= 0 || K < 256 || n_cols <= 0) return 0;
-    // the largest layout either entry point may use for this shape (one-stage segments)
-    return ws_bytes_for(N, K, pass_nt(n_cols), 1);
+    // the largest layout any plan of either entry point may use for this shape
+    return ws_bytes_cols(N, K, n_cols);
 }
 
 extern "C" spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K, const uint16_t *x,
@@ -896,11 +971,17 @@ extern "C" spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N
     SPEC_CHECK_ARG(y_dt == SPEC_F32 || y_dt == SPEC_BF16, "qmatmul: y_dt must be SPEC_F32 or SPEC_BF16");
     SPEC_CHECK_ARG(!(accumulate && y_dt != SPEC_F32), "qmatmul: accumulate needs SPEC_F32 output");
     if (n_cols == 0) return SPEC_OK;
-    const int nt = pass_nt(n_cols);
-    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
+    const Plan p = choose_plan(N, K, n_cols, false);
+    st = check_ws(workspace, ws_bytes, ws_bytes_launch(N, K, p.nt, p.ncg, 1));
     if (st != SPEC_OK) return st;
-    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, nt, workspace, dev_err,
-                   (cudaStream_t)stream);
+    return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, y_dt, ldy, accumulate, 1, p.nt, workspace, dev_err,
+                   (cudaStream_t)stream, SC_BLOCK, nullptr, 0, WIDE_AUTO, nullptr, p.ncg);
+}
+
+extern "C" int spec_qmatmul_plan(int N, int K, int n_cols, int packed_input) {
+    if (N <= 0 || K < 256 || n_cols <= 0) return 0;
+    const Plan p = choose_plan(N, K, n_cols, packed_input != 0);
+    return 8 * p.nt;
 }
 
 extern "C" size_t spec_packed_activation_bytes(int K) {
@@ -990,15 +1071,20 @@ extern "C" spec_status spec_qmatmul_debug_nt(const uint8_t *wq, const uint16_t *
                                              size_t ws_bytes, spec_stream_t stream) {
     spec_status st = check_args(wq, ws, N, K, x, n_cols, ldx, y, ldy);
     if (st != SPEC_OK) return st;
-    SPEC_CHECK_ARG(nt == 1 || nt == 2 || nt == MAX_NT || nt == MAX_NT + 1, "nt must be 1, 2, 10 or 11");
+    SPEC_CHECK_ARG(nt == 1 || nt == 2 || (nt >= MAX_NT && nt <= MAX_NT + 3), "nt must be 1, 2, 10, 11, 12 or 13");
     if (n_cols == 0) return SPEC_OK;
-    // 10: the 80-column pass on the mma.sync kernel, 11: on the tcgen05 kernel
+    // 10: the 80-column pass on the mma.sync kernel, 11: on the tcgen05 kernel;
+    // 12: 16-column passes, up to five column groups per launch; 13: 8-column
+    // passes, up to ten column groups per launch
     const int wide = nt == MAX_NT + 1 ? WIDE_TC : WIDE_MMA_SYNC;
-    nt = nt > MAX_NT ? MAX_NT : nt;
-    st = check_ws(workspace, ws_bytes, ws_bytes_for(N, K, nt, 1));
+    int ncg = 1;
+    if (nt == MAX_NT + 2) nt = 2, ncg = MAX_NCG;
+    else if (nt == MAX_NT + 3) nt = 1, ncg = 2 * MAX_NCG;
+    else nt = nt > MAX_NT ? MAX_NT : nt;
+    st = check_ws(workspace, ws_bytes, ws_bytes_launch(N, K, nt, ncg, 1));
     if (st != SPEC_OK) return st;
     return qmm_run(wq, ws, N, K, x, n_cols, ldx, y, SPEC_F32, ldy, 0, 1, nt, workspace, nullptr,
-                   (cudaStream_t)stream, SC_BLOCK, nullptr, 0, wide);
+                   (cudaStream_t)stream, SC_BLOCK, nullptr, 0, wide, nullptr, ncg);
 }
 
 // ---------------------------------------------------------------------------

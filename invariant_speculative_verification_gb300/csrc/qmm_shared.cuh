@@ -93,17 +93,22 @@ struct Sched {
     int G;          // CTAs
     long long U;    // units = tiles * ks
     int ks, tiles, seg_st;   // segments, tiles, stages per segment
+    // column groups of one launch: tile t is 128-row tile t / ncg of the
+    // matrix for column group t % ncg (the groups of a row tile are adjacent,
+    // so that its weights are read from DRAM once and then from L2)
+    int ncg;
     __device__ long long begin(int c) const { return (long long)c * U / G; }
     __device__ int cta_of(long long u) const { return (int)(((u + 1) * G - 1) / U); }
 };
 
 // The schedule of a call with 128-row tiles, segments of seg512 x 512 k and
-// stages of stage_k k on `sms` SMs.
-inline Sched make_sched(int N, int K, int seg512, int stage_k, int sms) {
+// stages of stage_k k on `sms` SMs, for ncg column groups.
+inline Sched make_sched(int N, int K, int seg512, int stage_k, int sms, int ncg = 1) {
     Sched sch;
     sch.seg_st = seg512 * (SEG_K / stage_k);
     sch.ks = n_segments(K, seg512 * SEG_K);
-    sch.tiles = (N + BM - 1) / BM;
+    sch.ncg = ncg;
+    sch.tiles = (N + BM - 1) / BM * ncg;
     sch.U = (long long)sch.tiles * sch.ks;
     sch.G = (int)(sch.U < sms ? sch.U : sms);
     // Nearly one tile per SM: one whole tile per CTA costs at most 15 % more work

@@ -93,6 +93,7 @@ class Decoder:
         # an 80-column K1 pass's activations, packed by the producing kernel (RMSNorm, SwiGLU)
         xpk_bytes = max(L.spec_packed_activation_bytes(k) for k in (H, F, self.Hq * self.D))
         self.xpk = torch.empty(xpk_bytes // 4 + 16, dtype=torch.int32, device=d)
+        self._plans = {}   # (N, K, rows) -> pass width of spec_qmatmul_plan
 
     @staticmethod
     def _packed(R):
@@ -151,7 +152,14 @@ class Decoder:
             L.spec_add_rmsnorm(self.h, None, w, R, self.H, self.cfg.eps, self.a)
 
     def _matmul(self, wts, N, K, x, R, y, accumulate, pk):
-        """y (+)= W x over R rows; from the packed activations when pk (same bits)."""
+        """y (+)= W x over R rows; from the packed activations when pk and the
+        80-column pass is the faster plan for this shape (every plan gives the
+        same bits)."""
+        if pk:
+            key = (N, K, R)
+            if key not in self._plans:
+                self._plans[key] = L.spec_qmatmul_plan(N, K, R, True)
+            pk = self._plans[key] == 80
         if pk:
             L.spec_qmatmul_packed(wts[0], wts[1], N, K, self.xpk, R, y, L.SPEC_F32, N, accumulate, self.qws,
                                   self.qws_bytes, self.dev_err)

@@ -52,9 +52,15 @@ def run(case_or_w, x_dev, n_cols, N, K, ldx=None, out_dt=0, y=None, accumulate=0
 
 def debug_nt_ws(N, K, nt):
     tiles = (N + 127) // 128
+    ncg = 1
+    if nt == 12:      # 16-column passes, up to five column groups in one launch
+        nt, ncg = 2, 5
+    elif nt == 13:    # 8-column passes, up to ten column groups in one launch
+        nt, ncg = 1, 10
     packed = (K // 256) * 43520 if nt >= 10 else 0   # the 80-column pass's packed activations
     nt = min(nt, 10)
-    return ((tiles * 4 + 255) // 256) * 256 + tiles * (1 + (K + 511) // 512) * 128 * 8 * nt * 4 + packed
+    t = tiles * ncg
+    return ((t * 4 + 255) // 256) * 256 + t * (1 + (K + 511) // 512) * 128 * 8 * nt * 4 + packed
 
 
 @pytest.fixture(scope="module")
@@ -102,7 +108,9 @@ def test_column_placement_and_tile_width_do_not_change_bits(tiny):
             xs[pos] = probe[0]
             y = run(w, xs, n_cols, 512, 512)
             assert bits_equal(y[pos], ref), (n_cols, pos)
-            for nt in (1, 2, 10, 11):   # 10: 80-column pass on mma.sync, 11: on tcgen05
+            # 10: 80-column pass on mma.sync, 11: on tcgen05; 12 / 13: 16- / 8-column
+            # passes, several column groups per launch
+            for nt in (1, 2, 10, 11, 12, 13):
                 yy = torch.zeros((n_cols, 512), dtype=torch.float32, device="cuda")
                 wsp = workspace(debug_nt_ws(512, 512, nt))
                 L.spec_qmatmul_debug_nt(w[0], w[1], 512, 512, xs, n_cols, 512, yy, 512, nt, wsp, wsp.numel() * 4)
@@ -199,6 +207,36 @@ def test_edge_shapes_and_pass_boundaries(N, K, n):
     assert rel_err_rows(host(y), oracle.qmatmul(case.wq, case.ws, case.x, N, K)) <= TOL
     for j in sorted({0, n // 2, n - 1}):
         assert bits_equal(run(w, x[j:j + 1], 1, N, K)[0], y[j]), j
+
+
+@pytest.mark.parametrize("N,K,n", [(2048, 5632, 80), (2048, 2048, 80), (3072, 2048, 48), (32000, 2048, 32),
+                                   (1000, 2304, 23)])
+def test_grouped_plans_parity_invariance_and_workspace(N, K, n):
+    """Shapes where spec_qmatmul runs its columns as one launch of 16- or
+    8-column groups: parity with the oracle on sampled columns, every sampled
+    column equal to its width-1 call and to the 80-column pass bit for bit, and
+    the workspace's counter area left zero."""
+    L = _lib()
+    plan = L.spec_qmatmul_plan(N, K, n)
+    assert plan in (8, 16, 80) and plan == L.spec_qmatmul_plan(N, K, n)
+    case = synth.qmatmul_case(9100 + n, N, K, n)
+    w, x = (dev(case.wq), dev(case.ws)), dev(case.x)
+    need = L.spec_qmatmul_workspace(N, K, n)
+    wsp = torch.zeros(need // 4 + 16, dtype=torch.int32, device="cuda")
+    y = torch.zeros((n, N), dtype=torch.float32, device="cuda")
+    L.spec_qmatmul(w[0], w[1], N, K, x, n, K, y, 0, N, 0, wsp, wsp.numel() * 4)
+    torch.cuda.synchronize()
+    assert int(wsp[:16384].abs().sum().item()) == 0
+    cols = sorted({0, 7, 8, 15, 16, n // 2, n - 1} & set(range(n)))
+    ref = oracle.qmatmul(case.wq, case.ws, case.x[cols], N, K)
+    assert rel_err_rows(host(y)[cols], ref) <= TOL
+    for j in cols[::2]:
+        assert bits_equal(run(w, x[j:j + 1], 1, N, K)[0], y[j]), j
+    y10 = torch.zeros((n, N), dtype=torch.float32, device="cuda")
+    w10 = workspace(debug_nt_ws(N, K, 10))
+    L.spec_qmatmul_debug_nt(w[0], w[1], N, K, x, n, K, y10, N, 10, w10, w10.numel() * 4)
+    torch.cuda.synchronize()
+    assert bits_equal(y10, y)
 
 
 def test_calls_of_different_tile_counts_share_one_workspace():
