@@ -93,7 +93,7 @@ class Decoder:
         # an 80-column K1 pass's activations, packed by the producing kernel (RMSNorm, SwiGLU)
         xpk_bytes = max(L.spec_packed_activation_bytes(k) for k in (H, F, self.Hq * self.D))
         self.xpk = torch.empty(xpk_bytes // 4 + 16, dtype=torch.int32, device=d)
-        self._plans = {}   # (N, K, rows) -> pass width of spec_qmatmul_plan
+        self._plans = {}   # (N, K, rows) -> the 80-column pass is the plan (spec_qmatmul_plan)
 
     @staticmethod
     def _packed(R):
@@ -112,15 +112,20 @@ class Decoder:
         max_kv_len = max_kv_len or self.max_len
         tr = trace or (lambda name: None)
         pk = self._packed(R)
-        self._norm(lay["norm1"], R, pk)
+        # which matmuls run the 80-column pass from packed activations (spec_qmatmul_plan)
+        pk_qkv = pk and self._plan80(self.nqkv, H, R)
+        pk_o = pk and self._plan80(H, self.Hq * D, R)
+        pk_gu = pk and self._plan80(2 * F, H, R)
+        pk_down = pk and self._plan80(H, F, R)
+        self._norm(lay["norm1"], R, pk_qkv)
         tr("norm1")
-        self._matmul(lay["qkv"], self.nqkv, H, self.a, R, self.qkv, 0, pk)
+        self._matmul(lay["qkv"], self.nqkv, H, self.a, R, self.qkv, 0, pk_qkv)
         tr("qkv")
         L.spec_rope_append(self.qkv, R, self.Hq, self.Hkv, D, self.rope, self.max_len, cu_rows, ctx, S, self.q,
                            self.k_cache[li], self.v_cache[li], self.pages, self.block_table, self.max_blocks,
                            None, None, self.dev_err)
         tr("rope")
-        if pk:
+        if pk_o:
             L.spec_flash_decode_packed(self.q, L.SPEC_BF16, self.Hq, self.Hkv, D, 1.0 / math.sqrt(D),
                                        self.k_cache[li], self.v_cache[li], self.pages, self.block_table,
                                        self.max_blocks, ctx, cu_rows, S, R, max_kv_len, self.attn, self.attn_ws,
@@ -130,18 +135,18 @@ class Decoder:
                                 self.v_cache[li], self.pages, self.block_table, self.max_blocks, ctx, cu_rows, S, R,
                                 max_kv_len, self.attn, L.SPEC_BF16, self.attn_ws, self.ws_bytes, self.dev_err)
         tr("attn")
-        self._matmul(lay["o"], H, self.Hq * D, self.attn, R, self.h, 1, pk)
+        self._matmul(lay["o"], H, self.Hq * D, self.attn, R, self.h, 1, pk_o)
         tr("o")
-        self._norm(lay["norm2"], R, pk)
+        self._norm(lay["norm2"], R, pk_gu)
         tr("norm2")
-        self._matmul(lay["gu"], 2 * F, H, self.a, R, self.gu, 0, pk)
+        self._matmul(lay["gu"], 2 * F, H, self.a, R, self.gu, 0, pk_gu)
         tr("gu")
-        if pk:
+        if pk_down:
             L.spec_swiglu_packed(self.gu, R, F, self.act, self.xpk)
         else:
             L.spec_swiglu(self.gu, R, F, self.act)
         tr("swiglu")
-        self._matmul(lay["down"], H, F, self.act, R, self.h, 1, pk)
+        self._matmul(lay["down"], H, F, self.act, R, self.h, 1, pk_down)
         tr("down")
 
     def _norm(self, w, R, pk):
@@ -151,15 +156,16 @@ class Decoder:
         else:
             L.spec_add_rmsnorm(self.h, None, w, R, self.H, self.cfg.eps, self.a)
 
+    def _plan80(self, N, K, R):
+        """True when the 80-column pass from packed activations is the faster plan
+        for an N x K matrix over R rows (every plan gives the same bits)."""
+        key = (N, K, R)
+        if key not in self._plans:
+            self._plans[key] = L.spec_qmatmul_plan(N, K, R, True) == 80
+        return self._plans[key]
+
     def _matmul(self, wts, N, K, x, R, y, accumulate, pk):
-        """y (+)= W x over R rows; from the packed activations when pk and the
-        80-column pass is the faster plan for this shape (every plan gives the
-        same bits)."""
-        if pk:
-            key = (N, K, R)
-            if key not in self._plans:
-                self._plans[key] = L.spec_qmatmul_plan(N, K, R, True)
-            pk = self._plans[key] == 80
+        """y (+)= W x over R rows; from the packed activations when pk."""
         if pk:
             L.spec_qmatmul_packed(wts[0], wts[1], N, K, self.xpk, R, y, L.SPEC_F32, N, accumulate, self.qws,
                                   self.qws_bytes, self.dev_err)
@@ -188,7 +194,7 @@ class Decoder:
         self.gate = g
 
     def head(self, R, trace=None):
-        pk = self._packed(R) and self.gate is None
+        pk = self._packed(R) and self.gate is None and self._plan80(self.V, self.H, R)
         self._norm(self.final_norm, R, pk)
         if trace:
             trace("final_norm")
