@@ -17,7 +17,9 @@
 //
 // K2 (attn_partial_kernel): a resident grid (at most one CTA per SM) walks
 // the (chunk, kv head, sequence) items, each CTA every G-th item.  A producer
-// warp copies an item's K pages and its V pages (4-D TMA boxes, 128B swizzle)
+// warp copies an item's K pages and its V pages (one TMA box per 16-key page:
+// the cache viewed as 5-D with the head dimension split into 64-wide halves,
+// so that each 128-byte row can be swizzled, 128B swizzle)
 // into four 64-key K slots and four V slots; consumer warp w owns sub-tile w
 // and, for each 16-row M-tile of (query row, grouped head) pairs, runs
 // S = Q K^T and O = P V on mma.sync m16n8k16 with fp32 accumulation (P enters
@@ -28,7 +30,8 @@
 // runs under this item's P V and merge, and its V copy under the next S.
 // Which CTA computes an item, and when, is scheduling: an item's operations
 // are those of a CTA of its own.
-// K3 (attn_combine_kernel): one warp per (row, head).
+// K3 (attn_combine_kernel): one warp per (row, head, 32-value block of the
+// head dimension), one value per lane.
 #include "qmm_shared.cuh"
 
 namespace {
@@ -54,6 +57,13 @@ struct ACfg {
     static constexpr int SMEM = 1024 + BAR_OFF + NBAR * 8;
     static_assert(SMEM <= 232448, "shared memory budget");
 };
+
+// Byte offset of (key, 64-wide half hh of the head dimension) in a sub-tile's
+// K or V slot: one 4 KB box per 16-key page, [page][half][key][128 B] (128-byte
+// swizzle within each 1024-byte atom, by key & 7).
+__device__ __forceinline__ uint32_t kv_off(int key, int hh, int halves) {
+    return (uint32_t)((key >> 4) * (halves * 2048) + hh * 2048 + (key & 15) * 128);
+}
 
 template <bool BF16>
 __device__ __forceinline__ void mma16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -200,12 +210,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                         dev::mbar_arrive_expect_tx(&fl[w], (uint32_t)((pg1 - pg0) * C::HALVES * 2048));
                     for (int pg = pg0; pg < pg1; ++pg) {
                         const int phys = __shfl_sync(0xffffffffu, my_phys, pg - pg_first);
-                        if (lane == 0) {
-                            const int off = (pg - pg0) * 2048;
-#pragma unroll
-                            for (int hh = 0; hh < C::HALVES; ++hh)
-                                dev::tma_load_4d(dst + hh * SUB * 128 + off, map, hh * 64, 0, m.kvh, phys, &fl[w]);
-                        }
+                        if (lane == 0)   // the page's keys, both halves of D in one box
+                            dev::tma_load_5d(dst + (pg - pg0) * C::HALVES * 2048, map, 0, 0, 0, m.kvh, phys, &fl[w]);
                     }
                 }
             }
@@ -289,7 +295,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                         const int key = 8 * (2 * jp + (mi >> 1)) + (lane & 7);
                         const int ch = cbase + (mi & 1);
                         uint32_t b0, b1, b2, b3;
-                        dev::ldmatrix_x4(b0, b1, b2, b3, kb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
+                        dev::ldmatrix_x4(b0, b1, b2, b3, kb + kv_off(key, hh, C::HALVES) + ((ch ^ (key & 7)) << 4));
                         mma16<BF16>(sc[2 * jp], qa0, qa1, qa2, qa3, b0, b1, sc[2 * jp]);
                         mma16<BF16>(sc[2 * jp + 1], qa0, qa1, qa2, qa3, b2, b3, sc[2 * jp + 1]);
                     }
@@ -350,7 +356,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                             const int hh = idx / ((SUB - nvalid) * 8);
                             const int rem = idx % ((SUB - nvalid) * 8);
                             const int key = nvalid + rem / 8, ch = rem % 8;
-                            *reinterpret_cast<uint4 *>(vslot + hh * SUB * 128 + key * 128 + ch * 16) =
+                            *reinterpret_cast<uint4 *>(vslot + kv_off(key, hh, C::HALVES) + ch * 16) =
                                 make_uint4(0, 0, 0, 0);
                         }
                     }
@@ -379,7 +385,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                         const int dch = 2 * ndp + (mi >> 1);     // 8-wide d chunk
                         const int hh = dch / 8, ch = dch % 8;
                         uint32_t b0, b1, b2, b3;
-                        dev::ldmatrix_x4_trans(b0, b1, b2, b3, vb + hh * SUB * 128 + key * 128 + ((ch ^ (key & 7)) << 4));
+                        dev::ldmatrix_x4_trans(b0, b1, b2, b3,
+                                               vb + kv_off(key, hh, C::HALVES) + ((ch ^ (key & 7)) << 4));
                         mma16<BF16>(o[2 * ndp], ph[0], ph[1], ph[2], ph[3], b0, b1, o[2 * ndp]);
                         mma16<BF16>(o[2 * ndp], pl[0], pl[1], pl[2], pl[3], b0, b1, o[2 * ndp]);
                         mma16<BF16>(o[2 * ndp + 1], ph[0], ph[1], ph[2], ph[3], b2, b3, o[2 * ndp + 1]);
@@ -458,7 +465,11 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     }
 }
 
-// K3: out = (sum_c o_c 2^(m_c - m)) / (sum_c l_c 2^(m_c - m)), c ascending
+// K3: out = (sum_c o_c 2^(m_c - m)) / (sum_c l_c 2^(m_c - m)), c ascending.
+// One warp per (row, head, 32-value block of the head dimension), one value
+// per lane: the chunk partials of 32 chunks are requested at once (the combine
+// is a chain of dependent loads otherwise), then added in ascending chunk
+// order.
 template <int D, bool OUT_BF16>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__restrict__ cu_rows, int S, int R, int Hq,
@@ -466,92 +477,67 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
                     int max_kv_len, uint8_t *__restrict__ xpk) {
     dev::pdl_wait();
     dev::pdl_launch_dependents();
+    constexpr int QB = D / 32;   // 32-value blocks of a head
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (wid >= R * Hq) return;
-    const int r = wid / Hq, h = wid % Hq;
+    if (wid >= R * Hq * QB) return;
+    const int qb = wid % QB, rh = wid / QB;
+    const int r = rh / Hq, h = rh % Hq;
     int lo = 0, hi = S;  // sequence of row r: largest s with cu_rows[s] <= r
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (cu_rows[mid] <= r) lo = mid; else hi = mid;
     }
     const int p = ctx_start[lo] + (r - cu_rows[lo]);
-    constexpr int PER = D / 32;
-    static_assert(PER == 2 || PER == 4, "head dimension 64 or 128");
-    float acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    const int d = qb * 32 + lane;
+    float acc = 0.f;
     if (p < 0 || p >= max_kv_len) {
         // the partial kernel rejected this sequence (length error); emit zeros
     } else {
         const int nc = p / CHUNK + 1;
-        const float2 *ml = part_ml + ((size_t)r * Hq + h) * nc_max;
-        const float *ob = part_o + ((size_t)r * Hq + h) * nc_max * D + lane * PER;
+        const float2 *ml = part_ml + (size_t)rh * nc_max;
+        const float *ob = part_o + (size_t)rh * nc_max * D + d;
         // m: max over the chunks (exact, any order); lane j holds chunks j, j + 32, ...
         float m = -INFINITY;
         for (int c = lane; c < nc; c += 32) m = fmaxf(m, ml[c].x);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        // l and the weighted values in ascending chunk order; the partials of
-        // eight chunks are loaded together
+        // l and the weighted values in ascending chunk order, 32 chunks' loads at a time
         float l = 0.f;
         for (int c0 = 0; c0 < nc; c0 += 32) {
             const int cl = c0 + lane;
             const float2 mlv = cl < nc ? ml[cl] : make_float2(-INFINITY, 0.f);
             const float wl = cl < nc ? exp2f(mlv.x - m) : 0.f;
             const int cn = min(32, nc - c0);
-            for (int j0 = 0; j0 < cn; j0 += 8) {
-                float ov[8][PER];
+            float ov[32];
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    if (j0 + jj < cn) {
-                        const float *src = ob + (size_t)(c0 + j0 + jj) * D;
-                        if constexpr (PER == 4) {
-                            const float4 v = *reinterpret_cast<const float4 *>(src);
-                            ov[jj][0] = v.x, ov[jj][1] = v.y, ov[jj][2] = v.z, ov[jj][3] = v.w;
-                        } else {
-                            const float2 v = *reinterpret_cast<const float2 *>(src);
-                            ov[jj][0] = v.x, ov[jj][1] = v.y;
-                        }
-                    } else {
+            for (int j = 0; j < 32; ++j) ov[j] = j < cn ? ob[(size_t)(c0 + j) * D] : 0.f;
 #pragma unroll
-                        for (int e = 0; e < PER; ++e) ov[jj][e] = 0.f;
-                    }
-                }
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const float w = __shfl_sync(0xffffffffu, wl, j0 + jj);
-                    const float lc = __shfl_sync(0xffffffffu, mlv.y, j0 + jj);
-                    if (j0 + jj < cn) {
-                        l = fmaf(lc, w, l);
-#pragma unroll
-                        for (int e = 0; e < PER; ++e) acc[e] = fmaf(ov[jj][e], w, acc[e]);
-                    }
+            for (int j = 0; j < 32; ++j) {
+                const float w = __shfl_sync(0xffffffffu, wl, j);
+                const float lc = __shfl_sync(0xffffffffu, mlv.y, j);
+                if (j < cn) {
+                    l = fmaf(lc, w, l);
+                    acc = fmaf(ov[j], w, acc);
                 }
             }
         }
-        const float inv = 1.0f / l;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] *= inv;
+        acc *= 1.0f / l;
     }
-    const size_t ob = ((size_t)r * Hq + h) * D + lane * PER;
+    const size_t oi = (size_t)rh * D + d;
     if (OUT_BF16) {
-        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(out) + ob;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) o[e] = __float2bfloat16_rn(acc[e]);
+        reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(acc);
         if (xpk) {
             // row r is column r of an 80-column K1 pass (the o projection): pack this
-            // head's 32-value blocks too, once the warp's stores are visible to it
+            // 32-value block too, once the warp's stores are visible to it
             __syncwarp();
-            if (lane < D / 32) {
-                const int kb = h * D + 32 * lane;
+            if (lane == 0) {
+                const int kb = h * D + 32 * qb;
                 qmm::pack_wide_block(reinterpret_cast<const uint16_t *>(out) + (size_t)r * Hq * D + kb, kb, r, xpk);
             }
         }
     } else {
-        float *o = reinterpret_cast<float *>(out) + ob;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) o[e] = acc[e];
+        reinterpret_cast<float *>(out)[oi] = acc;
     }
 }
 
@@ -598,12 +584,15 @@ spec_status attn_run(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, f
     float2 *ml = reinterpret_cast<float2 *>(workspace);
     float *po = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + mlb);
 
+    // The caches seen as (d within a 64-wide half, key, half, head, page): one box
+    // is a page's 16 keys of one head, both halves (128-byte rows for the swizzle)
     CUtensorMap tk, tv;
-    uint64_t dims[4] = {(uint64_t)D, (uint64_t)PAGE, (uint64_t)Hkv, (uint64_t)num_pages};
-    uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)PAGE * D * 2, (uint64_t)Hkv * PAGE * D * 2};
-    uint32_t box[4] = {64, PAGE, 1, 1};
-    if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, k_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, v_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t halves = (uint64_t)D / 64;
+    uint64_t dims[5] = {64, (uint64_t)PAGE, halves, (uint64_t)Hkv, (uint64_t)num_pages};
+    uint64_t strides[4] = {(uint64_t)D * 2, 128, (uint64_t)PAGE * D * 2, (uint64_t)Hkv * PAGE * D * 2};
+    uint32_t box[5] = {64, PAGE, (uint32_t)halves, 1, 1};
+    if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, k_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, v_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return SPEC_ERR_CUDA;
     const bool bf = (qkv_dt == SPEC_BF16);
     spec_status st;
@@ -618,7 +607,7 @@ spec_status attn_run(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, f
                 : launch_partial<64, false>(tk, tv, q, Hq, Hkv, scale, num_pages, block_table, max_blocks, ctx_start,
                                             cu_rows, S, R, max_kv_len, nc_max, ml, po, dev_err, stream);
     if (st != SPEC_OK) return st;
-    const int warps = R * Hq;
+    const int warps = R * Hq * (D / 32);
     dim3 grid((warps + 3) / 4);
     const bool obf = (out_dt == SPEC_BF16);
     cudaError_t le;
