@@ -16,18 +16,19 @@
 // row; sub-tiles past p are left out of the row's merge altogether.
 //
 // K2 (attn_partial_kernel): a resident grid (at most one CTA per SM) walks
-// the (chunk, kv head, sequence) items, each CTA every G-th item.  A producer
-// warp copies an item's K pages and its V pages (one TMA box per 16-key page:
-// the cache viewed as 5-D with the head dimension split into 64-wide halves,
-// so that each 128-byte row can be swizzled, 128B swizzle)
-// into four 64-key K slots and four V slots; consumer warp w owns sub-tile w
+// the (chunk, kv head, sequence) items, each CTA every G-th item, its K and V
+// staged through a ring of three (D = 128; four at D = 64) half-item buffers
+// in the order K0 V0 K1 V1 ..., so that up to 1.5 items' copies run ahead of
+// the math.  A producer warp copies an item's K pages and its V pages (one TMA
+// box per 16-key page: the cache viewed as 5-D with the head dimension split
+// into 64-wide halves, so that each 128-byte row takes the 128B swizzle) into
+// a buffer's four 64-key sub-tile slots; consumer warp w owns sub-tile w
 // and, for each 16-row M-tile of (query row, grouped head) pairs, runs
 // S = Q K^T and O = P V on mma.sync m16n8k16 with fp32 accumulation (P enters
 // the PV product as a hi + lo pair of 16-bit values, rounding error ~2^-17),
 // leaving its (m_w, l_w, o_w) in shared memory; the four warps then merge
 // them and write the chunk partials.  K and V are released separately (K
-// after the item's last S, V after its last P V), so the next item's K copy
-// runs under this item's P V and merge, and its V copy under the next S.
+// after the item's last S, V after its last P V).
 // Which CTA computes an item, and when, is scheduling: an item's operations
 // are those of a CTA of its own.
 // K3 (attn_combine_kernel): one warp per (row, head, 32-value block of the
@@ -43,18 +44,24 @@ constexpr int NCONS = CHUNK / SUB;   // one consumer warp per sub-tile
 constexpr int THREADS = (NCONS + 1) * 32;
 constexpr float LOG2E = 1.4426950408889634f;
 
+// Shared memory: a ring of NBUF buffers, each holding one half-item -- an
+// item's K or its V for all four sub-tiles -- in the order K0 V0 K1 V1 ...;
+// then the sub-tile partials of MR M-tiles for the merge.
 template <int D>
 struct ACfg {
     static constexpr int HALVES = D / 64;                 // 64-wide d boxes per key row
     static constexpr int KV_BYTES = HALVES * SUB * 128;   // one of K or V for a sub-tile
-    static constexpr int SLOT = 2 * KV_BYTES;
-    static constexpr int MR = D == 128 ? 2 : 4;           // M-tiles per round
+    static constexpr int BUF = NCONS * KV_BYTES;          // one half-item
+    static constexpr int MR = D == 128 ? 1 : 4;           // M-tiles per round
     static constexpr int OSTR = D + 4;                    // padded row stride of a sub-tile's o (floats)
     static constexpr int PART = 16 * OSTR * 4 + 16 * 8;   // o and (m, l) of one (M-tile, sub-tile)
-    static constexpr int PART_OFF = NCONS * SLOT;
-    static constexpr int BAR_OFF = PART_OFF + MR * NCONS * PART;
-    static constexpr int NBAR = 2 * NCONS + 2;              // kfull, vfull per slot; kfree, vfree
+    static constexpr int PARTS = MR * NCONS * PART;
+    static constexpr int NBUF = (232448 - 1024 - PARTS - 256) / BUF > 4 ? 4 : (232448 - 1024 - PARTS - 256) / BUF;
+    static constexpr int PART_OFF = NBUF * BUF;
+    static constexpr int BAR_OFF = PART_OFF + PARTS;
+    static constexpr int NBAR = NBUF * NCONS + NBUF;        // full per (buffer, sub-tile); free per buffer
     static constexpr int SMEM = 1024 + BAR_OFF + NBAR * 8;
+    static_assert(NBUF >= 3, "at least three half-items in the ring");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -116,22 +123,16 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     using C = ACfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *vfull = kfull + NCONS;
-    uint64_t *kfree = vfull + NCONS;   // every consumer warp is done with the item's K slots
-    uint64_t *vfree = kfree + 1;       // ... with its V slots
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);   // [buffer][sub-tile]
+    uint64_t *freeb = full + C::NBUF * NCONS;   // [buffer]: every consumer warp is done with it
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = Hq / Hkv;
     const long long nitems = (long long)nc_max * Hkv * S;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < NCONS; ++b) {
-            dev::mbar_init(&kfull[b], 1);
-            dev::mbar_init(&vfull[b], 1);
-        }
-        dev::mbar_init(kfree, NCONS);
-        dev::mbar_init(vfree, NCONS);
+        for (int b = 0; b < C::NBUF * NCONS; ++b) dev::mbar_init(&full[b], 1);
+        for (int b = 0; b < C::NBUF; ++b) dev::mbar_init(&freeb[b], NCONS);
         dev::fence_barrier_init();
     }
     __syncthreads();
@@ -167,10 +168,12 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     };
 
     if (warp == NCONS) {
-        // ---------------- producer: each item's K, then its V, into the slots ----------------
+        // ---------------- producer: each item's K, then its V, into the ring ----------------
         // An item's (at most 16) block-table entries are read by 16 lanes at once;
-        // lane 0 then issues every copy, K once the previous item's K slots are
-        // released, V once its V slots are.
+        // lane 0 then issues every copy of a half-item once its buffer's previous
+        // half-item is released.  Every sub-tile barrier of the buffer completes a
+        // phase per half-item (without bytes where the chunk has no such sub-tile),
+        // so a buffer's phase parity is the same for every consumer warp.
         if (lane == 0) {
             dev::prefetch_tmap(&tk);
             dev::prefetch_tmap(&tv);
@@ -191,21 +194,23 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 }
             }
             for (int kv = 0; kv < 2 && ok; ++kv) {
-                uint64_t *fr = kv ? vfree : kfree;
-                uint64_t *fl = kv ? vfull : kfull;
+                const int j = 2 * jv + kv, b = j % C::NBUF;   // half-item j of this CTA, its buffer
+                uint64_t *fl = full + b * NCONS;
                 const CUtensorMap *map = kv ? &tv : &tk;
                 int got = 1;
-                if (lane == 0 && jv > 0) got = dev::mbar_wait(fr, (jv - 1) & 1) ? 1 : 0;
+                if (lane == 0 && j >= C::NBUF) got = dev::mbar_wait(&freeb[b], ((j / C::NBUF) - 1) & 1) ? 1 : 0;
                 if (!__shfl_sync(0xffffffffu, got, 0)) {
                     if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                     ok = false;
                     break;
                 }
+                if (lane == 0)
+                    for (int w = m.nsub; w < NCONS; ++w) dev::mbar_arrive(&fl[w]);
                 for (int w = 0; w < m.nsub; ++w) {
                     const int key0 = m.kbeg + w * SUB;
                     const int pg0 = key0 / PAGE;
                     const int pg1 = min(pg0 + SUB / PAGE, pg_end);
-                    uint8_t *dst = smem + w * C::SLOT + kv * C::KV_BYTES;
+                    uint8_t *dst = smem + b * C::BUF + w * C::KV_BYTES;
                     if (lane == 0)
                         dev::mbar_arrive_expect_tx(&fl[w], (uint32_t)((pg1 - pg0) * C::HALVES * 2048));
                     for (int pg = pg0; pg < pg1; ++pg) {
@@ -224,11 +229,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     // ---------------- consumers: warp w owns sub-tile w of every item ----------------
     const int w = warp;
     const int g = lane >> 2, t = lane & 3;
-    uint8_t *kslot = smem + w * C::SLOT;
-    uint8_t *vslot = kslot + C::KV_BYTES;
-    const uint32_t kb = dev::smem_u32(kslot), vb = dev::smem_u32(vslot);
     bool ok = true;
-    int uses = 0;   // items in which this warp's slots were filled (their phase parity)
+    int vi = 0;   // valid items so far: item vi's K is half-item 2 vi, its V 2 vi + 1
     for (long long it = blockIdx.x; it < nitems; it += gridDim.x) {
         Item itm;
         if (!item(it, itm)) continue;
@@ -239,8 +241,12 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         const int mtiles = (mrows + 15) / 16;
         const int key0 = kbeg + w * SUB;
         const bool has_sub = w < nsub;
-        const uint32_t par = (uint32_t)(uses & 1);
-        if (has_sub) ++uses;
+        const int bk = (2 * vi) % C::NBUF, bv = (2 * vi + 1) % C::NBUF;
+        const uint32_t pk = (uint32_t)(((2 * vi) / C::NBUF) & 1), pv = (uint32_t)(((2 * vi + 1) / C::NBUF) & 1);
+        ++vi;
+        uint8_t *kslot = smem + bk * C::BUF + w * C::KV_BYTES;
+        uint8_t *vslot = smem + bv * C::BUF + w * C::KV_BYTES;
+        const uint32_t kb = dev::smem_u32(kslot), vb = dev::smem_u32(vslot);
         bool kwaited = false, vwaited = false;
         bool karrived = false, varrived = false;   // this warp's release of the item's K / V slots
 
@@ -274,7 +280,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 }
                 if (!kwaited) {
                     kwaited = true;
-                    if (!dev::mbar_wait(&kfull[w], par)) {
+                    if (!dev::mbar_wait(&full[bk * NCONS + w], pk)) {
                         if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                         ok = false;
                         break;
@@ -303,7 +309,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 if (last_tile) {
                     // the item's last S of this warp: its K slot may take the next item's keys
                     __syncwarp();
-                    if (lane == 0) dev::mbar_arrive(kfree);
+                    if (lane == 0) dev::mbar_arrive(&freeb[bk]);
                     karrived = true;
                 }
                 // ---- mask, scale to log2 units, softmax within the sub-tile ----
@@ -343,7 +349,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 }
                 if (!vwaited) {
                     vwaited = true;
-                    if (!dev::mbar_wait(&vfull[w], par)) {
+                    if (!dev::mbar_wait(&full[bv * NCONS + w], pv)) {
                         if (lane == 0) dev::report(dev_err, SPEC_DEVERR_TIMEOUT);
                         ok = false;
                         break;
@@ -398,7 +404,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                     // (the zeroing above wrote it through the generic proxy: order that first)
                     dev::fence_proxy_async();
                     __syncwarp();
-                    if (lane == 0) dev::mbar_arrive(vfree);
+                    if (lane == 0) dev::mbar_arrive(&freeb[bv]);
                     varrived = true;
                 }
                 // ---- leave (m_w, l_w, o_w) of rows g, g + 8 in shared memory ----
@@ -455,12 +461,12 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         // a warp without a sub-tile in this item (or after an error) still releases once
         if (!karrived) {
             __syncwarp();
-            if (lane == 0) dev::mbar_arrive(kfree);
+            if (lane == 0) dev::mbar_arrive(&freeb[bk]);
         }
         if (!varrived) {
             dev::fence_proxy_async();
             __syncwarp();
-            if (lane == 0) dev::mbar_arrive(vfree);
+            if (lane == 0) dev::mbar_arrive(&freeb[bv]);
         }
     }
 }
