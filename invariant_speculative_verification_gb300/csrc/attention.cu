@@ -489,11 +489,7 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
     if (wid >= R * Hq * QB) return;
     const int qb = wid % QB, rh = wid / QB;
     const int r = rh / Hq, h = rh % Hq;
-    int lo = 0, hi = S;  // sequence of row r: largest s with cu_rows[s] <= r
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cu_rows[mid] <= r) lo = mid; else hi = mid;
-    }
+    const int lo = dev::warp_seq_of_row(cu_rows, S, r);   // sequence of row r
     const int p = ctx_start[lo] + (r - cu_rows[lo]);
     const int d = qb * 32 + lane;
     float acc = 0.f;

@@ -160,6 +160,29 @@ __device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Sequence of row r from cu_rows[0..S] (non-decreasing, cu_rows[0] = 0): the
+// largest s < S with cu_rows[s] <= r, clamped to [0, S - 1].  Every lane of the
+// warp calls it; up to 128 sequences take one round of independent loads (a
+// binary search's loads depend on each other), more a binary search.
+__device__ __forceinline__ int warp_seq_of_row(const int32_t *cu_rows, int S, int r) {
+    const int lane = threadIdx.x & 31;
+    if (S <= 128) {
+        int cnt = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int t = lane + 32 * k;
+            cnt += __popc(__ballot_sync(0xffffffffu, t < S && cu_rows[t] <= r));
+        }
+        return cnt < 1 ? 0 : (cnt > S ? S - 1 : cnt - 1);
+    }
+    int lo = 0, hi = S;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu_rows[mid] <= r) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
 // Contiguous bulk copy global -> this CTA's shared memory, completion on `bar`
 // (both addresses 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

@@ -5,15 +5,6 @@
 
 namespace {
 
-__device__ __forceinline__ int seq_of_row(const int32_t *cu_rows, int S, int r) {
-    int lo = 0, hi = S;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cu_rows[mid] <= r) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
 __global__ void embed_kernel(const uint16_t *__restrict__ emb, int V, int H, const int32_t *__restrict__ tokens,
                              float *__restrict__ h, int32_t *dev_err) {
     dev::pdl_wait();
@@ -37,19 +28,41 @@ add_rmsnorm_kernel(float *__restrict__ h, const float *__restrict__ delta, const
     const int r = blockIdx.x;
     float4 *hr = reinterpret_cast<float4 *>(h + (size_t)r * H);
     const float4 *dr = delta ? reinterpret_cast<const float4 *>(delta + (size_t)r * H) : nullptr;
+    const float4 *w4 = reinterpret_cast<const float4 *>(w);
     const int n4 = H / 4;
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < n4; i += NT_NORM) {
-        float4 v = hr[i];
+    // up to NKEEP float4 of the row (and of w) stay in registers between the two
+    // passes, their loads all issued at once; a longer row reloads the rest
+    constexpr int NKEEP = 4;
+    float4 keep[NKEEP], wkeep[NKEEP];
+#pragma unroll
+    for (int k = 0; k < NKEEP; ++k) {
+        const int i = threadIdx.x + k * NT_NORM;
+        if (i < n4) {
+            keep[k] = hr[i];
+            wkeep[k] = w4[i];
+        }
+    }
+    // each thread's elements in index order: the kept ones, then the rest
+    auto add_sq = [&](float4 &v, int i, float &acc) {
         if (dr) {
             const float4 d = dr[i];
             v.x += d.x; v.y += d.y; v.z += d.z; v.w += d.w;
             hr[i] = v;
         }
-        ss += v.x * v.x;
-        ss += v.y * v.y;
-        ss += v.z * v.z;
-        ss += v.w * v.w;
+        acc += v.x * v.x;
+        acc += v.y * v.y;
+        acc += v.z * v.z;
+        acc += v.w * v.w;
+    };
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < NKEEP; ++k) {
+        const int i = threadIdx.x + k * NT_NORM;
+        if (i < n4) add_sq(keep[k], i, ss);
+    }
+    for (int i = threadIdx.x + NKEEP * NT_NORM; i < n4; i += NT_NORM) {
+        float4 v = hr[i];
+        add_sq(v, i, ss);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -64,14 +77,18 @@ add_rmsnorm_kernel(float *__restrict__ h, const float *__restrict__ delta, const
     }
     __syncthreads();
     const float inv = inv_s;
-    const float4 *w4 = reinterpret_cast<const float4 *>(w);
     uint2 *o2 = reinterpret_cast<uint2 *>(out + (size_t)r * H);
-    for (int i = threadIdx.x; i < n4; i += NT_NORM) {
-        const float4 v = hr[i], ww = w4[i];
+    auto emit = [&](const float4 &v, const float4 &ww, int i) {
         __nv_bfloat162 a = __floats2bfloat162_rn(v.x * inv * ww.x, v.y * inv * ww.y);
         __nv_bfloat162 b = __floats2bfloat162_rn(v.z * inv * ww.z, v.w * inv * ww.w);
         o2[i] = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+    };
+#pragma unroll
+    for (int k = 0; k < NKEEP; ++k) {
+        const int i = threadIdx.x + k * NT_NORM;
+        if (i < n4) emit(keep[k], wkeep[k], i);
     }
+    for (int i = threadIdx.x + NKEEP * NT_NORM; i < n4; i += NT_NORM) emit(hr[i], w4[i], i);
     if (xpk) {
         // the row is column r of an 80-column K1 pass: write its packed blocks too
         __syncthreads();   // the row's bf16 values, stored above by every thread, are visible to the block
@@ -101,7 +118,7 @@ __global__ void rope_append_kernel(const float *__restrict__ qkv, int Hq, int Hk
     dev::pdl_wait();
     dev::pdl_launch_dependents();
     const int r = blockIdx.x;
-    const int s = seq_of_row(cu_rows, S, r);
+    const int s = dev::warp_seq_of_row(cu_rows, S, r);
     const int pos = ctx_start[s] + (r - cu_rows[s]);
     const int half = D / 2;
     const float *row = qkv + (size_t)r * (Hq + 2 * Hkv) * D;
