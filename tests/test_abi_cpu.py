@@ -100,6 +100,28 @@ def test_qmatmul_workspace_is_checked_on_the_host():
     assert e.value.status == 3
 
 
+def test_qmatmul_plan_is_a_host_query_with_fixed_narrow_and_wide_widths():
+    """spec_qmatmul_plan: 8 columns -> one 8-column pass, 9-16 -> one 16-column
+    pass, more than 80 -> 80-column passes, 17-80 -> one of the three widths;
+    packed activations (no packing launch) never make the 80-column pass a
+    worse choice; invalid shapes answer 0."""
+    import invariant_speculative_verification_gb300 as L
+    shapes = [(2048, 2048), (3072, 2048), (2048, 5632), (11264, 2048), (32000, 2048), (17408, 5120), (5120, 17408)]
+    for N, K in shapes:
+        for n in (1, 8):
+            assert L.spec_qmatmul_plan(N, K, n) == 8
+        for n in (9, 16):
+            assert L.spec_qmatmul_plan(N, K, n) == 16
+        for n in (81, 161):
+            assert L.spec_qmatmul_plan(N, K, n) == 80
+        for n in (17, 33, 48, 64, 80):
+            plain, packed = L.spec_qmatmul_plan(N, K, n), L.spec_qmatmul_plan(N, K, n, True)
+            assert plain in (8, 16, 80) and packed in (8, 16, 80)
+            assert plain != 80 or packed == 80
+            assert L.spec_qmatmul_workspace(N, K, n) >= L.spec_qmatmul_workspace(N, K, 8)
+    assert L.spec_qmatmul_plan(0, 512, 8) == 0 and L.spec_qmatmul_plan(64, 512, 0) == 0
+
+
 def test_verify_and_compact_host_validation():
     import invariant_speculative_verification_gb300 as L
     with pytest.raises(L.SpecError, match="multiple of 8"):
