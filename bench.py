@@ -161,6 +161,12 @@ def count_launches(fn):
                 else:
                     n = 2 * ((nc + 79) // 80)
                 counts[_n] = counts.get(_n, 0) + n
+            elif _n == "spec_qmatmul_swiglu":
+                # one launch, plus a packing launch when an 80-column pass reads plain activations
+                N, K, xpk, nc = 2 * int(a[2]), int(a[3]), a[5], int(a[6])
+                packed = xpk is not None and 16 < nc <= 80
+                n = 2 if (not packed and L.spec_qmatmul_plan(N, K, nc, False) == 80) else 1
+                counts[_n] = counts.get(_n, 0) + n
             else:
                 counts[_n] = counts.get(_n, 0) + 1
             return _f(*a, **k)

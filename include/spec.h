@@ -141,6 +141,29 @@ spec_status spec_qmatmul(const uint8_t *wq, const uint16_t *ws, int N, int K,
  * Failure" (only the delivery of the activations changes). */
 size_t spec_packed_activation_bytes(int K);
 
+/* Gate/up matmul with the SwiGLU applied as each output is written:
+ *   act[j][f] = bf16(silu(g) * u),  silu(g) = g / (1 + e^-g) in fp32,
+ * g and u the invariant K1 products (spec_qmatmul's arithmetic) of column j with
+ * feature f's gate and up weight rows.  wq / ws hold the 2F rows of the gate/up
+ * matrix interleaved: rows 16i .. 16i+7 are the gate rows of features
+ * 8i .. 8i+7, rows 16i+8 .. 16i+15 their up rows (a row's result does not
+ * depend on where it sits, so act equals spec_swiglu of spec_qmatmul's [gate;
+ * up] output bit for bit).  F a positive multiple of 8; act bf16
+ * [n_cols][ld_act], ld_act >= F; x, ldx, K, workspace
+ * (spec_qmatmul_workspace(2F, K, n_cols)) and dev_err as for spec_qmatmul.
+ * xpk (optional, 16-byte aligned): the same activations packed as for
+ * spec_qmatmul_packed (17 <= n_cols <= 80); the call then plans as for a
+ * caller with packed activations and an 80-column pass reads them.
+ * The fp32 gate/up product is never written.  Source: the decoder's SwiGLU
+ * feed-forward of ramgpt.org, "When Lossless Speculation Stops Being Lossless
+ * on Blackwell" (the target model whose per-row results must not depend on
+ * the batch). */
+spec_status spec_qmatmul_swiglu(const uint8_t *wq, const uint16_t *ws, int F, int K,
+                                const uint16_t *x, const void *xpk, int n_cols, int ldx,
+                                uint16_t *act, int ld_act,
+                                void *workspace, size_t ws_bytes,
+                                int32_t *dev_err, spec_stream_t stream);
+
 /* The pass width spec_qmatmul would take for n_cols columns of an N x K
  * matrix: 8, 16 (column groups of that width in one launch) or 80 (the
  * 80-column pass).  packed_input != 0 asks as for a caller that holds the

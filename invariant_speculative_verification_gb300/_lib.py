@@ -56,6 +56,7 @@ _SIGS = {
     "spec_swiglu_packed": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp]),
     "spec_packed_activation_bytes": (_sz, [_i32]),
     "spec_qmatmul_plan": (_i32, [_i32, _i32, _i32, _i32]),
+    "spec_qmatmul_swiglu": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
     "spec_flash_decode_packed": (_i32, [_vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _i32, _vp, _i32, _vp, _vp, _i32,
                                         _i32, _i32, _vp, _vp, _sz, _vp, _vp, _vp]),
     "spec_qmatmul_packed": (_i32, [_vp, _vp, _i32, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
@@ -280,6 +281,13 @@ def spec_flash_decode_packed(q, qkv_dt, Hq, Hkv, D, scale, k_cache, v_cache, num
 
 def spec_packed_activation_bytes(K):
     return int(load().spec_packed_activation_bytes(int(K)))
+
+
+def spec_qmatmul_swiglu(wq, ws, F, K, x, xpk, n_cols, ldx, act, ld_act, workspace, ws_bytes, dev_err=None,
+                        stream=None):
+    _check("spec_qmatmul_swiglu", load().spec_qmatmul_swiglu(_ptr(wq), _ptr(ws), F, K, _ptr(x), _ptr(xpk), n_cols,
+                                                             ldx, _ptr(act), ld_act, _ptr(workspace), ws_bytes,
+                                                             _ptr(dev_err), _stream(stream)))
 
 
 def spec_qmatmul_plan(N, K, n_cols, packed_input=False) -> int:

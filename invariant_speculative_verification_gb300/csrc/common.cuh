@@ -160,6 +160,13 @@ __device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// SwiGLU of one feature: bf16(silu(g) * u), silu(g) = g / (1 + e^-g) in fp32
+// (the one expression the decoder uses, whichever kernel evaluates it).
+__device__ __forceinline__ uint16_t swiglu_bf16(float g, float u) {
+    const float silu = g / (1.0f + expf(-g));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(silu * u));
+}
+
 // Sequence of row r from cu_rows[0..S] (non-decreasing, cu_rows[0] = 0): the
 // largest s < S with cu_rows[s] <= r, clamped to [0, S - 1].  Every lane of the
 // warp calls it; up to 128 sequences take one round of independent loads (a

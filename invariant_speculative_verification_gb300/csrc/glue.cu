@@ -180,10 +180,7 @@ __global__ void rope_append_kernel(const float *__restrict__ qkv, int Hq, int Hk
     }
 }
 
-__device__ __forceinline__ uint16_t swiglu1(float x, float u) {
-    const float silu = x / (1.0f + expf(-x));
-    return __bfloat16_as_ushort(__float2bfloat16_rn(silu * u));
-}
+__device__ __forceinline__ uint16_t swiglu1(float x, float u) { return dev::swiglu_bf16(x, u); }
 
 // grid (ceil(F / 1024), R): each thread one group of four consecutive features
 // (16-byte loads when F % 4 == 0 and the buffers are aligned, one element at a time otherwise)

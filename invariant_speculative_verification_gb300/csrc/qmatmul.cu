@@ -60,6 +60,10 @@ namespace {
 using namespace qmm;
 
 constexpr int NCW = 8;                       // consumer warps (16 rows each)
+// what a pass writes: fp32 (optionally added into y), bf16, or for a gate/up
+// matrix whose rows come in groups of 8 gate rows and their 8 up rows, the
+// bf16 SwiGLU of each feature (spec_qmatmul_swiglu)
+constexpr int OUT_F32 = 0, OUT_BF16 = 1, OUT_SWIGLU = 2;
 constexpr int W_BOX = BM * 128;              // one 128-row x 128-byte code box (256 k)
 constexpr int MAX_NT = 10;                   // column tiles per pass (80 columns)
 
@@ -160,7 +164,7 @@ __device__ __forceinline__ void named_sync_consumers() {
     asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
 }
 
-template <int NT, bool OUT_BF16, int FMT>
+template <int NT, int OUTM, int FMT>
 __global__ void __launch_bounds__(Cfg<NT, FMT>::THREADS, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ts,
            const uint16_t *__restrict__ x, int ldx, int N, int K, int n_cols, int col0, void *__restrict__ y, int ldy,
@@ -387,10 +391,27 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
 
     // y for this thread's fragments of `tile` from yrun
     auto store_tile = [&](int tile) {
+        if constexpr (OUTM == OUT_SWIGLU) {
+            // a fragment's rows r and r + 8 of its 16-row group are a feature's gate
+            // and up rows: write that feature's SwiGLU for the fragment's two columns
+#pragma unroll
+            for (int f = 0; f < NT; ++f) {
+                const int c8 = (ctb + f % CT) * 8, wr = wrow0 + 16 * (f / CT);
+                const int n = (tile / sch.ncg) * BM + wr + r;   // the gate row
+                if (n < N) {
+                    const int feat = (n >> 4) * 8 + (n & 7);
+                    const int c0 = colb + c8 + t, c1 = c0 + 4;
+                    uint16_t *act = reinterpret_cast<uint16_t *>(y);
+                    if (c0 < n_cols) act[(size_t)c0 * ldy + feat] = dev::swiglu_bf16(yrun[f][0], yrun[f][2]);
+                    if (c1 < n_cols) act[(size_t)c1 * ldy + feat] = dev::swiglu_bf16(yrun[f][1], yrun[f][3]);
+                }
+            }
+            return;
+        }
         auto store_y = [&](int c, int row, float v) {
             const int col = colb + c, n = (tile / sch.ncg) * BM + row;
             if (col < n_cols && n < N) {
-                if (OUT_BF16) {
+                if (OUTM == OUT_BF16) {
                     reinterpret_cast<__nv_bfloat16 *>(y)[(size_t)col * ldy + n] = __float2bfloat16_rn(v);
                 } else {
                     float *yp = reinterpret_cast<float *>(y) + (size_t)col * ldy + n;
@@ -742,13 +763,13 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
 }
 
 // seg512: segment length in units of 512 k (1 for the invariant entry points)
-template <int NT, bool OUT_BF16, int FMT>
+template <int NT, int OUTM, int FMT>
 spec_status launch_nt(const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N, int K,
                       int n_cols, int col0, void *y, int ldy, int accumulate, int seg512, void *workspace,
                       int32_t *dev_err, const int32_t *dev_cols, int min_cols, cudaStream_t stream,
                       const uint8_t *xpk_in = nullptr, int ncg = 1) {
     using C = Cfg<NT, FMT>;
-    auto kern = qmm_kernel<NT, OUT_BF16, FMT>;
+    auto kern = qmm_kernel<NT, OUTM, FMT>;
     static spec::SmemOptIn opt_in;
     spec_status so = spec::smem_opt_in(kern, C::SMEM, opt_in, "cudaFuncSetAttribute(qmm smem)");
     if (so != SPEC_OK) return so;
@@ -862,10 +883,32 @@ size_t ws_bytes_cols(int N, int K, int n_cols) {
 // bytes of super-block scale records per weight row
 inline int super_pitch(int K) { return (K + 511) / 512 * 16; }
 
+// One launch of a pass with output mode outm (SwiGLU with block scales only).
+template <int NT, int FMT>
+spec_status launch_mode(int outm, const CUtensorMap &tw, const CUtensorMap &ts, const uint16_t *x, int ldx, int N,
+                        int K, int n_cols, int col0, void *y, int ldy, int accumulate, int seg512, void *workspace,
+                        int32_t *dev_err, const int32_t *dev_cols, int min_cols, cudaStream_t stream,
+                        const uint8_t *xpk_in, int ncg) {
+    if (outm == OUT_SWIGLU) {
+        if constexpr (FMT == SC_BLOCK)
+            return launch_nt<NT, OUT_SWIGLU, FMT>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace,
+                                                  dev_err, dev_cols, min_cols, stream, xpk_in, ncg);
+        return spec::fail(SPEC_ERR_UNSUPPORTED, "qmatmul: the SwiGLU output needs block scales");
+    }
+    if (outm == OUT_BF16)
+        return launch_nt<NT, OUT_BF16, FMT>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err,
+                                            dev_cols, min_cols, stream, xpk_in, ncg);
+    return launch_nt<NT, OUT_F32, FMT>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace,
+                                       dev_err, dev_cols, min_cols, stream, xpk_in, ncg);
+}
+
+// swiglu: y is the bf16 SwiGLU of a gate/up matrix of N = 2F interleaved rows
+// (8 gate rows, then their 8 up rows), [n_cols][ldy] with ldy >= F.
 spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint16_t *x, int n_cols, int ldx,
                     void *y, spec_dtype y_dt, int ldy, int accumulate, int seg512, int nt, void *workspace,
                     int32_t *dev_err, cudaStream_t stream, int fmt = SC_BLOCK, const int32_t *dev_cols = nullptr,
-                    int min_cols = 0, int wide = WIDE_AUTO, const uint8_t *xpk_in = nullptr, int ncg = 1) {
+                    int min_cols = 0, int wide = WIDE_AUTO, const uint8_t *xpk_in = nullptr, int ncg = 1,
+                    bool swiglu = false) {
     CUtensorMap tw, ts;
     {
         uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)N};
@@ -892,6 +935,7 @@ spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint1
             return SPEC_ERR_CUDA;
     }
     const bool bf = (y_dt == SPEC_BF16);
+    const int outm = swiglu ? OUT_SWIGLU : (bf ? OUT_BF16 : OUT_F32);
     // column groups only while their arrival counters fit where counters may lie
     if ((size_t)((N + BM - 1) / BM) * ncg * sizeof(int) > CNT_LIMIT) ncg = 1;
     // One pass per group of 8 nt columns; passes run back to back on the stream.
@@ -901,10 +945,8 @@ spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint1
         spec_status st;
         const int g = nt < MAX_NT ? min(ncg, (n_cols - col0 + 8 * nt - 1) / (8 * nt)) : 1;
 #define SPEC_QMM_FMT(NTV, FMTV)                                                                                    \
-    st = bf ? launch_nt<NTV, true, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, 0, seg512, workspace, dev_err,    \
-                                         dev_cols, min_cols, stream, xpk_in, g)                                       \
-            : launch_nt<NTV, false, FMTV>(tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace,    \
-                                          dev_err, dev_cols, min_cols, stream, xpk_in, g)
+    st = launch_mode<NTV, FMTV>(outm, tw, ts, x, ldx, N, K, n_cols, col0, y, ldy, accumulate, seg512, workspace,     \
+                                dev_err, dev_cols, min_cols, stream, xpk_in, g)
 #define SPEC_QMM_CASE(NTV)                                                                                         \
     if (fmt == SC_BLOCK) {                                                                                         \
         SPEC_QMM_FMT(NTV, SC_BLOCK);                                                                              \
@@ -919,7 +961,7 @@ spec_status qmm_run(const uint8_t *wq, const void *ws, int N, int K, const uint1
             // Both give the same bits; the tcgen05 kernel measured slower on every matrix of
             // the decoder (its per-block accumulator round trip through tensor memory, with
             // four accumulators in flight, sets its block rate), so it is not chosen by default.
-            if (fmt == SC_BLOCK && wide == WIDE_TC)
+            if (fmt == SC_BLOCK && wide == WIDE_TC && !swiglu)
                 st = tc_wide_pass(tw, ts, x, ldx, N, K, n_cols, col0, y, bf, ldy, accumulate, seg512, workspace,
                                   dev_err, dev_cols, min_cols, stream);
             else
@@ -982,6 +1024,25 @@ extern "C" int spec_qmatmul_plan(int N, int K, int n_cols, int packed_input) {
     if (N <= 0 || K < 256 || n_cols <= 0) return 0;
     const Plan p = choose_plan(N, K, n_cols, packed_input != 0);
     return 8 * p.nt;
+}
+
+extern "C" spec_status spec_qmatmul_swiglu(const uint8_t *wq, const uint16_t *ws, int F, int K, const uint16_t *x,
+                                           const void *xpk, int n_cols, int ldx, uint16_t *act, int ld_act,
+                                           void *workspace, size_t ws_bytes, int32_t *dev_err, spec_stream_t stream) {
+    SPEC_CHECK_ARG(F >= 8 && F % 8 == 0, "qmatmul_swiglu: F must be a positive multiple of 8 (F=%d)", F);
+    SPEC_CHECK_ARG(ld_act >= F, "qmatmul_swiglu: ld_act must be >= F (ld_act=%d F=%d)", ld_act, F);
+    SPEC_CHECK_ARG(!xpk || spec::aligned16(xpk), "qmatmul_swiglu: xpk must be 16-byte aligned");
+    spec_status st = check_args(wq, ws, 2 * F, K, x, n_cols, ldx, act, 2 * F);
+    if (st != SPEC_OK) return st;
+    if (n_cols == 0) return SPEC_OK;
+    // with packed activations the 80-column pass needs no packing launch
+    const bool packed = xpk && n_cols > 16 && n_cols <= WIDE_COLS;
+    const Plan p = choose_plan(2 * F, K, n_cols, packed);
+    st = check_ws(workspace, ws_bytes, ws_bytes_launch(2 * F, K, p.nt, p.ncg, 1));
+    if (st != SPEC_OK) return st;
+    return qmm_run(wq, ws, 2 * F, K, x, n_cols, ldx, act, SPEC_BF16, ld_act, 0, 1, p.nt, workspace, dev_err,
+                   (cudaStream_t)stream, SC_BLOCK, nullptr, 0, WIDE_AUTO,
+                   packed && p.nt >= MAX_NT ? reinterpret_cast<const uint8_t *>(xpk) : nullptr, p.ncg, true);
 }
 
 extern "C" size_t spec_packed_activation_bytes(int K) {

@@ -61,6 +61,15 @@ class Decoder:
         for lay in weights.layers:
             self.layers.append({k: (tuple(_dev(a, device) for a in v) if isinstance(v, tuple) else _dev(v, device))
                                 for k, v in lay.items()})
+        # the gate/up rows interleaved for spec_qmatmul_swiglu: per group of 8
+        # features its 8 gate rows, then their 8 up rows
+        F = self.F
+        if F % 8 == 0:
+            g = torch.arange(F // 8, device=device).view(-1, 1) * 8 + torch.arange(8, device=device).view(1, -1)
+            perm = torch.cat([g, g + F], dim=1).reshape(-1)
+            for lay in self.layers:
+                wq, ws = lay["gu"]
+                lay["gu_il"] = (wq.index_select(0, perm).contiguous(), ws.index_select(0, perm).contiguous())
         self.lm = tuple(_dev(a, device) for a in weights.lm)
         self.final_norm = _dev(weights.final_norm, device)
         self.block_table = torch.arange(self.pages, dtype=torch.int32, device=device).view(n_seqs, self.max_blocks)
@@ -139,12 +148,18 @@ class Decoder:
         tr("o")
         self._norm(lay["norm2"], R, pk_gu)
         tr("norm2")
-        self._matmul(lay["gu"], 2 * F, H, self.a, R, self.gu, 0, pk_gu)
-        tr("gu")
-        if pk_down:
-            L.spec_swiglu_packed(self.gu, R, F, self.act, self.xpk)
+        if trace is None and not pk_down and "gu_il" in lay:
+            # gate/up product and SwiGLU in one launch (the same bits as the two calls)
+            wq, ws = lay["gu_il"]
+            L.spec_qmatmul_swiglu(wq, ws, F, H, self.a, self.xpk if pk_gu else None, R, H, self.act, F, self.qws,
+                                  self.qws_bytes, self.dev_err)
         else:
-            L.spec_swiglu(self.gu, R, F, self.act)
+            self._matmul(lay["gu"], 2 * F, H, self.a, R, self.gu, 0, pk_gu)
+            tr("gu")
+            if pk_down:
+                L.spec_swiglu_packed(self.gu, R, F, self.act, self.xpk)
+            else:
+                L.spec_swiglu(self.gu, R, F, self.act)
         tr("swiglu")
         self._matmul(lay["down"], H, F, self.act, R, self.h, 1, pk_down)
         tr("down")

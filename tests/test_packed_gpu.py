@@ -137,3 +137,69 @@ def test_attention_packed_feeds_the_o_projection_bit_for_bit():
     y0 = torch.from_numpy(g.normal(0, 1, (R, N)).astype(np.float32)).cuda()
     y_plain, y_packed = _matmul_pair(L, dev(wq), dev(ws_), N, K, outs[0], R, xpk, accumulate=1, y0=y0)
     assert bits_equal(y_plain, y_packed)
+
+
+def _interleave_gate_up(wq, ws, F):
+    """Rows of a [gate; up] matrix reordered as spec_qmatmul_swiglu takes them:
+    per group of 8 features its 8 gate rows, then their 8 up rows."""
+    g = np.arange(F).reshape(-1, 8)
+    perm = np.concatenate([g, g + F], axis=1).reshape(-1)
+    return np.ascontiguousarray(wq[perm]), np.ascontiguousarray(ws[perm])
+
+
+@pytest.mark.parametrize("F,K,R", [(5632, 2048, 80), (5632, 2048, 33), (5632, 2048, 16), (5632, 2048, 5),
+                                   (40, 512, 23)])
+def test_fused_swiglu_equals_matmul_then_swiglu_bit_for_bit(F, K, R):
+    """spec_qmatmul_swiglu (interleaved gate/up rows) writes exactly what
+    spec_qmatmul on the [gate; up] rows followed by spec_swiglu writes, from
+    plain and (17-80 rows) from packed activations; sampled features agree with
+    the oracle's SwiGLU of the oracle's products."""
+    L = _L()
+    g = np.random.default_rng(70 + F + R)
+    h = g.normal(0, 1, (R, K)).astype(np.float32)
+    w = g.normal(1, 0.1, K).astype(np.float32)
+    wq, ws = synth.qmatmul_weights(950 + R, 2 * F, K)
+    wqi, wsi = _interleave_gate_up(wq, ws, F)
+    a = torch.zeros((R, K), dtype=torch.int16, device="cuda")
+    xpk = torch.full((L.spec_packed_activation_bytes(K) // 4 + 16,), -1, dtype=torch.int32, device="cuda")
+    L.spec_add_rmsnorm_packed(dev(h), None, dev(w), R, K, 1e-5, a, xpk)
+    wsb = L.spec_qmatmul_workspace(2 * F, K, R)
+    wsp = torch.zeros(wsb // 4 + 64, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gu = torch.zeros((R, 2 * F), dtype=torch.float32, device="cuda")
+    L.spec_qmatmul(dev(wq), dev(ws), 2 * F, K, a, R, K, gu, L.SPEC_F32, 2 * F, 0, wsp, wsb, err)
+    ref = torch.zeros((R, F), dtype=torch.int16, device="cuda")
+    L.spec_swiglu(gu, R, F, ref)
+    outs = []
+    for use_pk in ((False, True) if 16 < R <= 80 else (False,)):
+        act = torch.full((R, F), -1, dtype=torch.int16, device="cuda")
+        L.spec_qmatmul_swiglu(dev(wqi), dev(wsi), F, K, a, xpk if use_pk else None, R, K, act, F, wsp, wsb, err)
+        outs.append(act)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for act in outs:
+        assert bits_equal(act, ref)
+    assert int(wsp[:16384].abs().sum().item()) == 0
+    rows = sorted({0, R // 2, R - 1})
+    feats = sorted({0, 7, 8, F // 2, F - 1})
+    xa = host(a, np.uint16)[rows]
+    gate = oracle.qmatmul(wq[feats], ws[feats], xa, len(feats), K)
+    up = oracle.qmatmul(wq[[F + f for f in feats]], ws[[F + f for f in feats]], xa, len(feats), K)
+    want = np.array([[oracle.silu_mul(gate[i, j], up[i, j]) for j in range(len(feats))] for i in range(len(rows))])
+    got = synth.bf16_bits_to_f32(host(outs[0], np.uint16))[np.ix_(rows, feats)]
+    # bf16 rounding of the result plus the products' own tolerance; a swapped
+    # gate/up pair or a wrong feature row is off by O(1)
+    assert rel_err_rows(got, want) <= 2 ** -6
+
+
+def test_fused_swiglu_arguments_are_checked():
+    L = _L()
+    x = torch.zeros((4, 512), dtype=torch.int16, device="cuda")
+    w = torch.zeros(64 * 256, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(64 * 16, dtype=torch.int16, device="cuda")
+    act = torch.zeros((4, 32), dtype=torch.int16, device="cuda")
+    wsp = torch.zeros(1 << 16, dtype=torch.int32, device="cuda")
+    with pytest.raises(L.SpecError, match="multiple of 8"):
+        L.spec_qmatmul_swiglu(w, s, 30, 512, x, None, 4, 512, act, 32, wsp, wsp.numel() * 4)
+    with pytest.raises(L.SpecError, match="ld_act"):
+        L.spec_qmatmul_swiglu(w, s, 32, 512, x, None, 4, 512, act, 16, wsp, wsp.numel() * 4)
