@@ -441,43 +441,36 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
     };
     auto fold_tile = [&](int tile, int seg_from) {
         float *p0 = wsp_seg + (size_t)tile * ks * TILE_ELEMS + frag;
-        constexpr int SG = NT >= 8 ? 2 : (NT >= 2 ? 4 : 8);   // segments whose loads are in flight together
-        int sg = seg_from;
-        for (; sg + SG <= ks; sg += SG) {
+        // segments whose loads are in flight together (a short last group is
+        // predicated: no load and no add past the last segment)
+        constexpr int SG = NT >= 8 ? 2 : (NT >= 2 ? 8 : 16);
+        for (int sg = seg_from; sg < ks; sg += SG) {
             float4 l[SG][NT];
 #pragma unroll
             for (int q = 0; q < SG; ++q)
 #pragma unroll
                 for (int ct = 0; ct < NT; ++ct)
-                    l[q][ct] = (fcol(ct) < n_cols)
+                    l[q][ct] = (sg + q < ks && fcol(ct) < n_cols)
                                    ? __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)(sg + q) * TILE_ELEMS +
                                                                              ct * NCW * 128))
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < SG; ++q)
+                if (sg + q < ks) {
 #pragma unroll
-                for (int ct = 0; ct < NT; ++ct) {
-                    yrun[ct][0] += l[q][ct].x;
-                    yrun[ct][1] += l[q][ct].y;
-                    yrun[ct][2] += l[q][ct].z;
-                    yrun[ct][3] += l[q][ct].w;
+                    for (int ct = 0; ct < NT; ++ct) {
+                        yrun[ct][0] += l[q][ct].x;
+                        yrun[ct][1] += l[q][ct].y;
+                        yrun[ct][2] += l[q][ct].z;
+                        yrun[ct][3] += l[q][ct].w;
+                    }
                 }
-        }
-        for (; sg < ks; ++sg) {
-#pragma unroll
-            for (int ct = 0; ct < NT; ++ct) {
-                if (fcol(ct) < n_cols) {
-                    const float4 l = __ldcg(reinterpret_cast<const float4 *>(p0 + (size_t)sg * TILE_ELEMS +
-                                                                             ct * NCW * 128));
-                    yrun[ct][0] += l.x, yrun[ct][1] += l.y, yrun[ct][2] += l.z, yrun[ct][3] += l.w;
-                }
-            }
         }
         store_tile(tile);
         if (threadIdx.x == 0) counters[tile] = 0;
         // every sum is read: clear those a later call could take for counters
         // (after all loads, so none waits behind these stores)
-        for (sg = seg_from; sg < ks; ++sg)
+        for (int sg = seg_from; sg < ks; ++sg)
 #pragma unroll
             for (int ct = 0; ct < NT; ++ct)
                 clear_low(p0 + (size_t)sg * TILE_ELEMS + ct * NCW * 128, fcol(ct) < n_cols);
