@@ -443,7 +443,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUten
         float *p0 = wsp_seg + (size_t)tile * ks * TILE_ELEMS + frag;
         // segments whose loads are in flight together (a short last group is
         // predicated: no load and no add past the last segment)
-        constexpr int SG = NT >= 8 ? 2 : (NT >= 2 ? 8 : 16);
+        constexpr int SG = NT >= 8 ? 3 : (NT >= 2 ? 8 : 16);
         for (int sg = seg_from; sg < ks; sg += SG) {
             float4 l[SG][NT];
 #pragma unroll
