@@ -199,7 +199,10 @@ verify_finalize_kernel(const Best *__restrict__ part, int split, const int32_t *
 
 int argmax_split(int R, int V) {
     const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
-    int sp = (8 * sms + R - 1) / R;          // about eight CTAs per SM
+    // as many splits as fit in one wave of eight CTAs per SM: rounding up left
+    // a partial second wave (1312 CTAs for 1216 slots at 328 rows, 24.9 us
+    // against 22.1 us for three splits; every split gives the same argmax)
+    int sp = (8 * sms) / R;
     const int max_sp = V / 4096 > 0 ? V / 4096 : 1;  // at least 4096 logits per CTA
     if (sp > max_sp) sp = max_sp;
     if (sp < 1) sp = 1;
