@@ -169,8 +169,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 
     if (warp == NCONS) {
         // ---------------- producer: each item's K, then its V, into the ring ----------------
-        // An item's (at most 16) block-table entries are read by 16 lanes at once,
-        // and each of those lanes copies its page once the buffer's previous
+        // An item's (at most 16) block-table entries are read by 16 lanes at once;
+        // lane 0 then issues every copy of a half-item once its buffer's previous
         // half-item is released.  Every sub-tile barrier of the buffer completes a
         // phase per half-item (without bytes where the chunk has no such sub-tile),
         // so a buffer's phase parity is the same for every consumer warp.
@@ -206,17 +206,19 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 }
                 if (lane == 0)
                     for (int w = m.nsub; w < NCONS; ++w) dev::mbar_arrive(&fl[w]);
-                // lane w posts sub-tile w's bytes; then lane l copies the item's page l
-                // (sub-tile l / 4; both halves of D in one box), all in one instruction
-                if (lane < m.nsub) {
-                    const int pg0 = pg_first + lane * (SUB / PAGE), pg1 = min(pg0 + SUB / PAGE, pg_end);
-                    dev::mbar_arrive_expect_tx(&fl[lane], (uint32_t)((pg1 - pg0) * C::HALVES * 2048));
+                for (int w = 0; w < m.nsub; ++w) {
+                    const int key0 = m.kbeg + w * SUB;
+                    const int pg0 = key0 / PAGE;
+                    const int pg1 = min(pg0 + SUB / PAGE, pg_end);
+                    uint8_t *dst = smem + b * C::BUF + w * C::KV_BYTES;
+                    if (lane == 0)
+                        dev::mbar_arrive_expect_tx(&fl[w], (uint32_t)((pg1 - pg0) * C::HALVES * 2048));
+                    for (int pg = pg0; pg < pg1; ++pg) {
+                        const int phys = __shfl_sync(0xffffffffu, my_phys, pg - pg_first);
+                        if (lane == 0)   // the page's keys, both halves of D in one box
+                            dev::tma_load_5d(dst + (pg - pg0) * C::HALVES * 2048, map, 0, 0, 0, m.kvh, phys, &fl[w]);
+                    }
                 }
-                __syncwarp();
-                if (lane < pg_end - pg_first)
-                    dev::tma_load_5d(smem + b * C::BUF + (lane / (SUB / PAGE)) * C::KV_BYTES +
-                                         (lane % (SUB / PAGE)) * C::HALVES * 2048,
-                                     map, 0, 0, 0, m.kvh, my_phys, &fl[lane / (SUB / PAGE)]);
             }
             ++jv;
         }
