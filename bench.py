@@ -534,6 +534,9 @@ def run_ours(args):
         torch.cuda.empty_cache()
         return toks, gen_tokens / t, steps, err
 
+    # an untimed generation first: on a freshly started GPU machine the first ~4 s of
+    # graph replays in a process ran at a third of the later rate, on the host side
+    full_generation(WIDTH)
     spec_toks, spec_tps, spec_steps, err4 = full_generation(WIDTH)
     base_toks, base_tps, base_steps, err0 = full_generation(0)
     equal_seqs = int(sum(np.array_equal(spec_toks[s], base_toks[s]) for s in range(N_SEQ)))
