@@ -111,13 +111,14 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                     const uint16_t *__restrict__ q, int Hq, int Hkv, float scale_log2, int num_pages,
                     const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_start,
-                    const int32_t *__restrict__ cu_rows, int S, int R, int max_kv_len, int nc_max, int parts,
+                    const int32_t *__restrict__ cu_rows, int S, int R, int max_kv_len, int nc_max,
                     float2 *__restrict__ part_ml, float *__restrict__ part_o, int32_t *dev_err) {
+    constexpr int parts = SPLIT ? 2 : 1;   // items per chunk: halves of its M-tiles when SPLIT
     dev::pdl_wait();
     dev::pdl_launch_dependents();
     using C = ACfg<D>;
@@ -137,17 +138,17 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     }
     __syncthreads();
 
-    // Item `it` of the call: part `it % parts` of the M-tiles of chunk c of kv
-    // head kvh of sequence s (the parts of a chunk are neighbouring items, so
-    // they run at the same time and the later copies of the chunk come from
-    // L2).  Every warp derives the same geometry from the same inputs, so
-    // producer and consumers skip the same items.
+    // Item `it` of the call: chunk c of kv head kvh of sequence s, with SPLIT
+    // the lower or upper half of the chunk's M-tiles (the two halves are
+    // neighbouring items, so they run at the same time and the second copy of
+    // the chunk comes from L2).  Every warp derives the same geometry from the
+    // same inputs, so producer and consumers skip the same items.
     struct Item {
         int c, kvh, s, r0, rows, ctx, len, kbeg, kend, nsub, mt_lo, mt_hi;
     };
     auto item = [&](long long it, Item &m) -> bool {
-        const int part = (int)(it % parts);
-        it /= parts;
+        const int part = SPLIT ? (int)(it & 1) : 0;   // the parts of a chunk are neighbouring items
+        if (SPLIT) it >>= 1;
         m.c = (int)(it % nc_max);
         m.kvh = (int)((it / nc_max) % Hkv);
         m.s = (int)(it / ((long long)nc_max * Hkv));
@@ -168,11 +169,14 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         if (m.kbeg >= m.len) return false;
         m.kend = min(m.kbeg + CHUNK, m.len);
         m.nsub = (m.kend - m.kbeg + SUB - 1) / SUB;
-        // this part's M-tiles of the chunk, split as evenly as they go
-        const int mtiles = ((m.rows - max(0, m.kbeg - m.ctx)) * G + 15) / 16;
-        m.mt_lo = (int)((long long)mtiles * part / parts);
-        m.mt_hi = (int)((long long)mtiles * (part + 1) / parts);
-        return m.mt_lo < m.mt_hi;
+        if constexpr (SPLIT) {
+            // this part's M-tiles of the chunk: the lower or the upper half
+            const int mtiles = ((m.rows - max(0, m.kbeg - m.ctx)) * G + 15) / 16;
+            m.mt_lo = part ? mtiles / 2 : 0;
+            m.mt_hi = part ? mtiles : mtiles / 2;
+            return m.mt_lo < m.mt_hi;
+        }
+        return true;
     };
 
     if (warp == NCONS) {
@@ -246,7 +250,9 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         const int kbeg = itm.kbeg, nsub = itm.nsub;
         const int i0 = max(0, kbeg - ctx);  // first row whose position reaches this chunk
         const int mrows = (rows - i0) * G;
-        const int mtiles = itm.mt_hi;        // this item's M-tiles: itm.mt_lo .. mtiles - 1
+        // this item's M-tiles: mt_first .. mtiles - 1
+        const int mtiles = SPLIT ? itm.mt_hi : (mrows + 15) / 16;
+        const int mt_first = SPLIT ? itm.mt_lo : 0;
         const int key0 = kbeg + w * SUB;
         const bool has_sub = w < nsub;
         const int bk = (2 * vi) % C::NBUF, bv = (2 * vi + 1) % C::NBUF;
@@ -258,7 +264,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         bool kwaited = false, vwaited = false;
         bool karrived = false, varrived = false;   // this warp's release of the item's K / V slots
 
-        for (int mt0 = itm.mt_lo; mt0 < mtiles; mt0 += C::MR) {
+        for (int mt0 = mt_first; mt0 < mtiles; mt0 += C::MR) {
             // ---- each warp: (m_w, l_w, o_w) of its sub-tile for up to MR M-tiles ----
             const bool last_round = mt0 + C::MR >= mtiles;
             for (int j = 0; j < C::MR && mt0 + j < mtiles && has_sub && ok; ++j) {
@@ -556,24 +562,25 @@ spec_status launch_partial(const CUtensorMap &tk, const CUtensorMap &tv, const v
                            int num_pages, const int32_t *bt, int max_blocks, const int32_t *ctx, const int32_t *cu,
                            int S, int R, int max_kv_len, int nc_max, float2 *ml, float *po, int32_t *dev_err,
                            cudaStream_t st) {
+    using C = ACfg<D>;
     // Split a chunk's M-tiles over two items when sequences have more than one
     // M-tile on average and contexts are short (at most 8 chunks): there the
     // items alone leave SMs idle, while long contexts are bound by each SM's
     // copies, which a split would double.
     const int G = Hq / Hkv;
-    const int parts = (S > 0 && (long long)R * G > 16ll * S && nc_max <= 8) ? 2 : 1;
-    using C = ACfg<D>;
-    auto kern = attn_partial_kernel<D, BF16>;
-    static spec::SmemOptIn opt_in;
-    spec_status so = spec::smem_opt_in(kern, C::SMEM, opt_in, "cudaFuncSetAttribute(attn smem)");
+    const bool split = S > 0 && (long long)R * G > 16ll * S && nc_max <= 8;
+    const int parts = split ? 2 : 1;
+    auto kern = split ? attn_partial_kernel<D, BF16, true> : attn_partial_kernel<D, BF16, false>;
+    static spec::SmemOptIn opt_in[2];
+    spec_status so = spec::smem_opt_in(kern, C::SMEM, opt_in[split ? 1 : 0], "cudaFuncSetAttribute(attn smem)");
     if (so != SPEC_OK) return so;
-    // a resident grid: at most one CTA per SM (the shared memory of one), each walking every G-th item
+    // a resident grid: at most one CTA per SM (the shared memory of one), CTA b taking items b, b + grid, ...
     const long long items = (long long)nc_max * Hkv * S * parts;
     const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
     const int grid = (int)(items < sms ? items : sms);
     cudaError_t le = spec::launch_pdl(kern, dim3(grid), dim3(THREADS), C::SMEM, st, tk, tv,
                                       reinterpret_cast<const uint16_t *>(q), Hq, Hkv, scale * LOG2E, num_pages, bt,
-                                      max_blocks, ctx, cu, S, R, max_kv_len, nc_max, parts, ml, po, dev_err);
+                                      max_blocks, ctx, cu, S, R, max_kv_len, nc_max, ml, po, dev_err);
     return spec::cuda_status(le, "attn partial launch");
 }
 
