@@ -16,7 +16,10 @@
 // row; sub-tiles past p are left out of the row's merge altogether.
 //
 // K2 (attn_partial_kernel): a resident grid (at most one CTA per SM) walks
-// the (chunk, kv head, sequence) items, each CTA every G-th item, its K and V
+// the (chunk, kv head, sequence) items, CTA b taking items b, b + grid, ...
+// (when sequences average more than one M-tile, the chunks of sequences of at
+// most SPLIT_CHUNKS chunks are two neighbouring items each, the lower and the
+// upper half of the chunk's M-tiles), its K and V
 // staged through a ring of three (D = 128; four at D = 64) half-item buffers
 // in the order K0 V0 K1 V1 ..., so that up to 1.5 items' copies run ahead of
 // the math.  A producer warp copies an item's K pages and its V pages (one TMA
@@ -41,6 +44,7 @@ constexpr int CHUNK = 256;
 constexpr int SUB = 64;
 constexpr int PAGE = 16;
 constexpr int NCONS = CHUNK / SUB;   // one consumer warp per sub-tile
+constexpr int SPLIT_CHUNKS = 8;      // sequences of at most this many chunks have their M-tiles halved
 constexpr int THREADS = (NCONS + 1) * 32;
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -129,7 +133,6 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = Hq / Hkv;
-    const long long nitems = (long long)nc_max * Hkv * S * parts;
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < C::NBUF * NCONS; ++b) dev::mbar_init(&full[b], 1);
@@ -138,20 +141,52 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     }
     __syncthreads();
 
+    // The chunk index varies slowest over the items, so every item of a chunk
+    // no sequence reaches is empty: a warp's walk ends at the chunks the
+    // sequences reach (at most nc_max) instead of skipping the rest one by one.
+    // Every warp finds the same bound from the same inputs.
+    const long long per_chunk = (long long)Hkv * S * parts;
+    const long long nitems_all = (long long)nc_max * per_chunk;
+    auto chunks_reached = [&]() -> int {
+        int nc = 0;
+        for (int s = lane; s < S; s += 32) {
+            const int rows = cu_rows[s + 1] - cu_rows[s], ctx = ctx_start[s];
+            if (rows > 0 && ctx >= 0)
+                nc = max(nc, (int)min((long long)nc_max, ((long long)ctx + rows + CHUNK - 1) / CHUNK));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) nc = max(nc, __shfl_xor_sync(0xffffffffu, nc, o));
+        return nc;
+    };
+    // With SPLIT, an even grid and a sequence longer than SPLIT_CHUNKS chunks
+    // (whose second parts are empty), odd rounds take each item's partner
+    // (it ^ 1): a round covers whole chunk pairs (the grid and the bound are
+    // even), so every item is still taken once, the two halves of a chunk stay
+    // on CTAs 2j and 2j + 1 of the same round, and a CTA alternates first and
+    // second parts instead of half of the CTAs drawing only the empty ones.
+    // (With only short sequences the fixed parts measured faster.)
+    auto flip_of = [&](int nc) { return SPLIT && (gridDim.x % 2 == 0) && nc > SPLIT_CHUNKS; };
+    auto item_of = [&](long long it, long long round, bool flip) -> long long {
+        return (flip && (round & 1)) ? (it ^ 1) : it;
+    };
+
     // Item `it` of the call: chunk c of kv head kvh of sequence s, with SPLIT
     // the lower or upper half of the chunk's M-tiles (the two halves are
-    // neighbouring items, so they run at the same time and the second copy of
-    // the chunk comes from L2).  Every warp derives the same geometry from the
-    // same inputs, so producer and consumers skip the same items.
+    // neighbouring items, so they run at the same time on a CTA pair and the
+    // second copy of the chunk comes from L2).  Every warp derives the same
+    // geometry from the same inputs, so producer and consumers skip the same
+    // items.
     struct Item {
         int c, kvh, s, r0, rows, ctx, len, kbeg, kend, nsub, mt_lo, mt_hi;
     };
     auto item = [&](long long it, Item &m) -> bool {
         const int part = SPLIT ? (int)(it & 1) : 0;   // the parts of a chunk are neighbouring items
         if (SPLIT) it >>= 1;
-        m.c = (int)(it % nc_max);
-        m.kvh = (int)((it / nc_max) % Hkv);
-        m.s = (int)(it / ((long long)nc_max * Hkv));
+        // the chunk index varies slowest: whatever bound max_kv_len puts on the
+        // chunk count, the chunks that exist come first and spread evenly over the CTAs
+        m.kvh = (int)(it % Hkv);
+        m.s = (int)((it / Hkv) % S);
+        m.c = (int)(it / ((long long)Hkv * S));
         m.r0 = cu_rows[m.s];
         m.rows = cu_rows[m.s + 1] - m.r0;
         m.ctx = ctx_start[m.s];
@@ -170,10 +205,13 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         m.kend = min(m.kbeg + CHUNK, m.len);
         m.nsub = (m.kend - m.kbeg + SUB - 1) / SUB;
         if constexpr (SPLIT) {
-            // this part's M-tiles of the chunk: the lower or the upper half
+            // this part's M-tiles of the chunk: the lower or the upper half when
+            // the sequence spans at most SPLIT_CHUNKS chunks; a longer one keeps
+            // its chunks whole in the first part (its second parts are empty)
             const int mtiles = ((m.rows - max(0, m.kbeg - m.ctx)) * G + 15) / 16;
-            m.mt_lo = part ? mtiles / 2 : 0;
-            m.mt_hi = part ? mtiles : mtiles / 2;
+            const int half = (m.len + CHUNK - 1) / CHUNK <= SPLIT_CHUNKS ? mtiles / 2 : mtiles;
+            m.mt_lo = part ? half : 0;
+            m.mt_hi = part ? mtiles : half;
             return m.mt_lo < m.mt_hi;
         }
         return true;
@@ -192,9 +230,19 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         }
         bool ok = true;
         int jv = 0;   // valid items so far
-        for (long long it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+        // the first item's copies go out before the bound is known (an item past
+        // it is empty, so nothing is issued for it either way)
+        long long nitems = nitems_all;
+        bool flip = false;
+        for (long long it = blockIdx.x, rd = 0; it < nitems && ok; it += gridDim.x, ++rd) {
+            if (rd == 1) {
+                const int nc = chunks_reached();
+                nitems = min(nitems, (long long)nc * per_chunk);
+                flip = flip_of(nc);
+                if (it >= nitems) break;
+            }
             Item m;
-            if (!item(it, m)) continue;
+            if (!item(item_of(it, rd, flip), m)) continue;
             const int32_t *bt = block_table + (size_t)m.s * max_blocks;
             const int pg_first = m.kbeg / PAGE, pg_end = (m.kend + PAGE - 1) / PAGE;
             int my_phys = 0;
@@ -243,9 +291,12 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     const int g = lane >> 2, t = lane & 3;
     bool ok = true;
     int vi = 0;   // valid items so far: item vi's K is half-item 2 vi, its V 2 vi + 1
-    for (long long it = blockIdx.x; it < nitems; it += gridDim.x) {
+    const int nc_reached = chunks_reached();
+    const long long nitems = min(nitems_all, (long long)nc_reached * per_chunk);
+    const bool flip = flip_of(nc_reached);
+    for (long long it = blockIdx.x, rd = 0; it < nitems; it += gridDim.x, ++rd) {
         Item itm;
-        if (!item(it, itm)) continue;
+        if (!item(item_of(it, rd, flip), itm)) continue;
         const int c = itm.c, kvh = itm.kvh, r0 = itm.r0, rows = itm.rows, ctx = itm.ctx, len = itm.len;
         const int kbeg = itm.kbeg, nsub = itm.nsub;
         const int i0 = max(0, kbeg - ctx);  // first row whose position reaches this chunk
@@ -564,11 +615,13 @@ spec_status launch_partial(const CUtensorMap &tk, const CUtensorMap &tv, const v
                            cudaStream_t st) {
     using C = ACfg<D>;
     // Split a chunk's M-tiles over two items when sequences have more than one
-    // M-tile on average and contexts are short (at most 8 chunks): there the
-    // items alone leave SMs idle, while long contexts are bound by each SM's
-    // copies, which a split would double.
+    // M-tile on average.  The kernel halves only the chunks of sequences that
+    // are short (SPLIT_CHUNKS chunks at most, decided from each sequence's own
+    // length, since max_kv_len is only a bound): there the items alone leave
+    // SMs idle, while long contexts are bound by each SM's copies, which a
+    // split would double.
     const int G = Hq / Hkv;
-    const bool split = S > 0 && (long long)R * G > 16ll * S && nc_max <= 8;
+    const bool split = S > 0 && (long long)R * G > 16ll * S;
     const int parts = split ? 2 : 1;
     auto kern = split ? attn_partial_kernel<D, BF16, true> : attn_partial_kernel<D, BF16, false>;
     static spec::SmemOptIn opt_in[2];

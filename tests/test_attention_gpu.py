@@ -146,6 +146,25 @@ def test_bf16_output_and_larger_bound_do_not_change_values():
     assert bits_equal(d.call(max_kv_len=5000), out)
 
 
+def test_split_chunks_of_short_and_whole_chunks_of_long_sequences():
+    # Five rows per sequence (more than one M-tile on average): the chunks of
+    # sequences of at most 8 chunks are halved over two items, the 10-chunk
+    # one keeps whole chunks; a decoder-sized key bound (21 chunks, an odd
+    # grid of mostly empty items) gives the same bits as the tight one.
+    rows = [5] * 15 + [8]
+    ctx = [127, 300, 511, 1023, 0, 2040, 60, 700, 1500, 200, 900, 1200, 30, 400, 800, 2300]
+    case = synth.attention_case(5150, rows=rows, ctx=ctx, Hq=16, Hkv=4, D=128, dt=DT_BF16,
+                                scale=1 / math.sqrt(128))
+    d = Dev(case)
+    out = d.call()
+    assert rel_err_rows(host(out), oracle.attention(case)) <= TOL
+    assert bits_equal(d.call(max_kv_len=5277), out)
+    for s in (0, 4, 5, 15):
+        r0 = int(case.cu_rows[s])
+        assert bits_equal(d.sequence_alone(s), out[r0:r0 + rows[s]]), s
+        assert bits_equal(d.single_row(s, rows[s] - 1), out[r0 + rows[s] - 1]), s
+
+
 def test_prefill_block_many_rows():
     # 128-row block at position 0 (several M-tile rounds per CTA)
     case = synth.attention_case(91, rows=[128], ctx=[0], Hq=4, Hkv=1, D=64, dt=DT_BF16)
