@@ -219,8 +219,8 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 
     if (warp == NCONS) {
         // ---------------- producer: each item's K, then its V, into the ring ----------------
-        // An item's (at most 16) block-table entries are read by 16 lanes at once;
-        // lane 0 then issues every copy of a half-item once its buffer's previous
+        // An item's (at most 16) block-table entries are read by 16 lanes at once,
+        // and each of those lanes copies its page once the buffer's previous
         // half-item is released.  Every sub-tile barrier of the buffer completes a
         // phase per half-item (without bytes where the chunk has no such sub-tile),
         // so a buffer's phase parity is the same for every consumer warp.
@@ -241,13 +241,22 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 flip = flip_of(nc);
                 if (it >= nitems) break;
             }
+            const long long jt = item_of(it, rd, flip);
+            // the chunk's (at most 16) block-table entries, loaded together with the
+            // item's own geometry; an entry past the sequence's pages is not used
+            int bt_entry = -1;
+            {
+                const long long q = SPLIT ? (jt >> 1) : jt;
+                const int s = (int)((q / Hkv) % S), c = (int)(q / ((long long)Hkv * S));
+                const int e = c * (CHUNK / PAGE) + lane;
+                if (lane < CHUNK / PAGE && e < max_blocks) bt_entry = block_table[(size_t)s * max_blocks + e];
+            }
             Item m;
-            if (!item(item_of(it, rd, flip), m)) continue;
-            const int32_t *bt = block_table + (size_t)m.s * max_blocks;
+            if (!item(jt, m)) continue;
             const int pg_first = m.kbeg / PAGE, pg_end = (m.kend + PAGE - 1) / PAGE;
             int my_phys = 0;
             if (lane < pg_end - pg_first) {
-                my_phys = bt[pg_first + lane];
+                my_phys = bt_entry;
                 if (my_phys < 0 || my_phys >= num_pages) {
                     dev::report(dev_err, SPEC_DEVERR_BLOCK_TABLE);
                     my_phys = 0;
@@ -266,19 +275,17 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 }
                 if (lane == 0)
                     for (int w = m.nsub; w < NCONS; ++w) dev::mbar_arrive(&fl[w]);
-                for (int w = 0; w < m.nsub; ++w) {
-                    const int key0 = m.kbeg + w * SUB;
-                    const int pg0 = key0 / PAGE;
-                    const int pg1 = min(pg0 + SUB / PAGE, pg_end);
-                    uint8_t *dst = smem + b * C::BUF + w * C::KV_BYTES;
-                    if (lane == 0)
-                        dev::mbar_arrive_expect_tx(&fl[w], (uint32_t)((pg1 - pg0) * C::HALVES * 2048));
-                    for (int pg = pg0; pg < pg1; ++pg) {
-                        const int phys = __shfl_sync(0xffffffffu, my_phys, pg - pg_first);
-                        if (lane == 0)   // the page's keys, both halves of D in one box
-                            dev::tma_load_5d(dst + (pg - pg0) * C::HALVES * 2048, map, 0, 0, 0, m.kvh, phys, &fl[w]);
-                    }
+                // lane w posts sub-tile w's bytes; then lane l copies the item's page l
+                // (sub-tile l / 4; both halves of D in one box), all in one instruction
+                if (lane < m.nsub) {
+                    const int pg0 = pg_first + lane * (SUB / PAGE), pg1 = min(pg0 + SUB / PAGE, pg_end);
+                    dev::mbar_arrive_expect_tx(&fl[lane], (uint32_t)((pg1 - pg0) * C::HALVES * 2048));
                 }
+                __syncwarp();
+                if (lane < pg_end - pg_first)
+                    dev::tma_load_5d(smem + b * C::BUF + (lane / (SUB / PAGE)) * C::KV_BYTES +
+                                         (lane % (SUB / PAGE)) * C::HALVES * 2048,
+                                     map, 0, 0, 0, m.kvh, my_phys, &fl[lane / (SUB / PAGE)]);
             }
             ++jv;
         }
