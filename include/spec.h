@@ -275,7 +275,14 @@ spec_status spec_qmatmul_static_scratch(const uint8_t *wq, const uint16_t *ws, i
  *            own K/V must already be in the cache (positions ctx_start[s] ..
  *            ctx_start[s] + rows - 1).  Row i attends to keys 0 .. ctx_start+i.
  *   cu_rows  int32 [S+1]
- *   max_kv_len  host bound on ctx_start[s] + rows of s (sizes the grid)
+ *   max_kv_len  host bound on ctx_start[s] + rows of s: it sizes the
+ *            workspace and the item count; the kernel itself stops at the
+ *            chunks the sequences reach, so a loose bound (a graph captured
+ *            once for a whole generation) costs next to nothing.  A sequence
+ *            longer than the bound or than max_blocks * 16 keys is reported
+ *            (SPEC_DEVERR_LENGTH), one whose rows fall outside [0, R) as
+ *            SPEC_DEVERR_LAYOUT; the rows of such a sequence, and of one with
+ *            a negative ctx_start, are written as zeros.
  *   out      [R][Hq][D] of out_dt (SPEC_F32 or SPEC_BF16)
  *   scale    multiplies q.k before the softmax
  *   D in {64, 128}; Hq % Hkv == 0; Hq / Hkv <= 16.

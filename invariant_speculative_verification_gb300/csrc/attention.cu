@@ -36,6 +36,9 @@
 // are those of a CTA of its own.
 // K3 (attn_combine_kernel): one warp per (row, head, 32-value block of the
 // head dimension), one value per lane.
+#include <algorithm>
+#include <climits>
+
 #include "qmm_shared.cuh"
 
 namespace {
@@ -552,7 +555,7 @@ template <int D, bool OUT_BF16>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__restrict__ cu_rows, int S, int R, int Hq,
                     int nc_max, const float2 *__restrict__ part_ml, const float *__restrict__ part_o, void *out,
-                    int max_kv_len, uint8_t *__restrict__ xpk) {
+                    int max_kv_len, int kv_cap, uint8_t *__restrict__ xpk) {
     dev::pdl_wait();
     dev::pdl_launch_dependents();
     constexpr int QB = D / 32;   // 32-value blocks of a head
@@ -562,11 +565,15 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
     const int qb = wid % QB, rh = wid / QB;
     const int r = rh / Hq, h = rh % Hq;
     const int lo = dev::warp_seq_of_row(cu_rows, S, r);   // sequence of row r
-    const int p = ctx_start[lo] + (r - cu_rows[lo]);
+    const int r0 = cu_rows[lo], rows = cu_rows[lo + 1] - r0, ctx = ctx_start[lo];
+    const int p = ctx + (r - r0);
+    const long long len = (long long)ctx + rows;
+    // the partial kernel's rejections (layout or length), which leave no partials
+    const bool rejected = rows <= 0 || ctx < 0 || r0 < 0 || r0 + rows > R || len > max_kv_len || len > kv_cap;
     const int d = qb * 32 + lane;
     float acc = 0.f;
-    if (p < 0 || p >= max_kv_len) {
-        // the partial kernel rejected this sequence (length error); emit zeros
+    if (rejected || p < 0 || p >= max_kv_len) {
+        // a rejected sequence (reported by the partial kernel): emit zeros
     } else {
         const int nc = p / CHUNK + 1;
         const float2 *ml = part_ml + (size_t)rh * nc_max;
@@ -692,18 +699,19 @@ spec_status attn_run(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, f
     if (st != SPEC_OK) return st;
     const int warps = R * Hq * (D / 32);
     dim3 grid((warps + 3) / 4);
+    const int kv_cap = (int)std::min<long long>((long long)max_blocks * PAGE, INT_MAX);
     const bool obf = (out_dt == SPEC_BF16);
     cudaError_t le;
     if (D == 128) {
         if (obf)
-            le = launch_pdl(attn_combine_kernel<128, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, xpk);
+            le = launch_pdl(attn_combine_kernel<128, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, kv_cap, xpk);
         else
-            le = launch_pdl(attn_combine_kernel<128, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, xpk);
+            le = launch_pdl(attn_combine_kernel<128, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, kv_cap, xpk);
     } else {
         if (obf)
-            le = launch_pdl(attn_combine_kernel<64, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, xpk);
+            le = launch_pdl(attn_combine_kernel<64, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, kv_cap, xpk);
         else
-            le = launch_pdl(attn_combine_kernel<64, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, xpk);
+            le = launch_pdl(attn_combine_kernel<64, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, kv_cap, xpk);
     }
     return cuda_status(le, "attn combine launch");
 }

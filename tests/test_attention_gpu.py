@@ -195,6 +195,28 @@ def test_bad_block_table_is_reported_not_faulted():
                             dev(case.ctx_start), dev(case.cu_rows), 1, 2, 42, out, 0, ws, 16, err)
 
 
+def test_rows_of_a_sequence_longer_than_the_bound_are_zeros():
+    # Sequence 1 ends past max_kv_len (positions 198..201 against a bound of
+    # 200) although its first rows lie inside it: the partial kernel rejects
+    # the whole sequence and reports it, and the combine writes zeros for all
+    # of its rows instead of reading partials that were never written (the
+    # workspace starts as NaN).  Sequence 0 is unaffected.
+    import invariant_speculative_verification_gb300 as L
+    case = synth.attention_case(6, rows=[3, 4], ctx=[100, 198], Hq=8, Hkv=2, D=128, dt=DT_BF16)
+    d = Dev(case)
+    R, bound = 7, 200
+    ws_bytes = L.spec_flash_decode_workspace(R, 8, 128, bound)
+    ws = torch.full((ws_bytes // 4 + 64,), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.full((R, 8, 128), 7.0, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.spec_flash_decode(d.q, case.dt, 8, 2, 128, case.scale, d.k, d.v, d.pages, d.bt, case.block_table.shape[1],
+                        dev(case.ctx_start), dev(case.cu_rows), 2, R, bound, out, 0, ws, ws_bytes, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & L.DEVERR["LENGTH"]
+    assert torch.count_nonzero(out[3:]).item() == 0
+    assert bits_equal(out[:3], d.sequence_alone(0))
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_rows_across_subtile_and_chunk_edges(D):
     """Verify blocks whose rows cross the 64-key sub-tile and 256-key chunk edges:
