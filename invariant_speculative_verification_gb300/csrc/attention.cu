@@ -124,7 +124,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                     const uint16_t *__restrict__ q, int Hq, int Hkv, float scale_log2, int num_pages,
                     const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_start,
                     const int32_t *__restrict__ cu_rows, int S, int R, int max_kv_len, int nc_max,
-                    float2 *__restrict__ part_ml, float *__restrict__ part_o, int32_t *dev_err) {
+                    float2 *__restrict__ part_ml, float *__restrict__ part_o, int32_t *dev_err, int split_long) {
     constexpr int parts = SPLIT ? 2 : 1;   // items per chunk: halves of its M-tiles when SPLIT
     dev::pdl_wait();
     dev::pdl_launch_dependents();
@@ -209,10 +209,13 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         m.nsub = (m.kend - m.kbeg + SUB - 1) / SUB;
         if constexpr (SPLIT) {
             // this part's M-tiles of the chunk: the lower or the upper half when
-            // the sequence spans at most SPLIT_CHUNKS chunks; a longer one keeps
-            // its chunks whole in the first part (its second parts are empty)
+            // the sequence spans at most SPLIT_CHUNKS chunks or the call has
+            // items for several rounds of the grid (split_long, from the host);
+            // otherwise a longer sequence keeps its chunks whole in the first
+            // part (its second parts are empty)
             const int mtiles = ((m.rows - max(0, m.kbeg - m.ctx)) * G + 15) / 16;
-            const int half = (m.len + CHUNK - 1) / CHUNK <= SPLIT_CHUNKS ? mtiles / 2 : mtiles;
+            const int half =
+                ((m.len + CHUNK - 1) / CHUNK <= SPLIT_CHUNKS || split_long) ? mtiles / 2 : mtiles;
             m.mt_lo = part ? half : 0;
             m.mt_hi = part ? mtiles : half;
             return m.mt_lo < m.mt_hi;
@@ -645,9 +648,16 @@ spec_status launch_partial(const CUtensorMap &tk, const CUtensorMap &tv, const v
     const long long items = (long long)nc_max * Hkv * S * parts;
     const int sms = spec::num_sms() > 0 ? spec::num_sms() : 148;
     const int grid = (int)(items < sms ? items : sms);
+    // With items for three or more rounds of the grid (at the bound), long
+    // sequences' chunks are halved too: the finer items balance the CTAs'
+    // loads better than whole ones (16384 keys, one sequence, widths 4 and 8:
+    // 5 % faster), while with fewer items the doubled copies cost more
+    // (4096 keys at width 8, 8 % slower).
+    const bool split_long = split && (long long)nc_max * Hkv * S >= 3ll * grid;
     cudaError_t le = spec::launch_pdl(kern, dim3(grid), dim3(THREADS), C::SMEM, st, tk, tv,
                                       reinterpret_cast<const uint16_t *>(q), Hq, Hkv, scale * LOG2E, num_pages, bt,
-                                      max_blocks, ctx, cu, S, R, max_kv_len, nc_max, ml, po, dev_err);
+                                      max_blocks, ctx, cu, S, R, max_kv_len, nc_max, ml, po, dev_err,
+                                      split_long ? 1 : 0);
     return spec::cuda_status(le, "attn partial launch");
 }
 
