@@ -567,20 +567,32 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
     if (wid >= R * Hq * QB) return;
     const int qb = wid % QB, rh = wid / QB;
     const int r = rh / Hq, h = rh % Hq;
+    const int d = qb * 32 + lane;
+    const float2 *ml = part_ml + (size_t)rh * nc_max;
+    const float *ob = part_o + (size_t)rh * nc_max * D + d;
+    // chunk 0's partial (every row that is combined has one) is requested
+    // together with the row's position; it is only used for a valid row
+    const float2 ml0 = ml[0];
+    const float ov0 = ob[0];
     const int lo = dev::warp_seq_of_row(cu_rows, S, r);   // sequence of row r
     const int r0 = cu_rows[lo], rows = cu_rows[lo + 1] - r0, ctx = ctx_start[lo];
     const int p = ctx + (r - r0);
     const long long len = (long long)ctx + rows;
     // the partial kernel's rejections (layout or length), which leave no partials
     const bool rejected = rows <= 0 || ctx < 0 || r0 < 0 || r0 + rows > R || len > max_kv_len || len > kv_cap;
-    const int d = qb * 32 + lane;
     float acc = 0.f;
     if (rejected || p < 0 || p >= max_kv_len) {
         // a rejected sequence (reported by the partial kernel): emit zeros
+    } else if (p < CHUNK) {
+        // one chunk: the operations of the general path below with c = 0 alone
+        // (the other lanes' maxima are -inf, so m = fmaxf(-inf, m_0))
+        const float m = fmaxf(-INFINITY, ml0.x);
+        const float w = exp2f(ml0.x - m);
+        const float l = fmaf(ml0.y, w, 0.f);
+        acc = fmaf(ov0, w, 0.f);
+        acc *= 1.0f / l;
     } else {
         const int nc = p / CHUNK + 1;
-        const float2 *ml = part_ml + (size_t)rh * nc_max;
-        const float *ob = part_o + (size_t)rh * nc_max * D + d;
         // m: max over the chunks (exact, any order); lane j holds chunks j, j + 32, ...
         float m = -INFINITY;
         for (int c = lane; c < nc; c += 32) m = fmaxf(m, ml[c].x);
