@@ -591,6 +591,30 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
         const float l = fmaf(ml0.y, w, 0.f);
         acc = fmaf(ov0, w, 0.f);
         acc *= 1.0f / l;
+    } else if (p < 32 * CHUNK) {
+        // at most 32 chunks, one per lane: the operations of the general path
+        // below (a single group, c0 = 0), with the (m, l) pairs and the values
+        // requested together instead of the pairs first for the maximum
+        const int nc = p / CHUNK + 1;
+        const float2 mlv = lane < nc ? ml[lane] : make_float2(-INFINITY, 0.f);
+        float ov[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ov[j] = j < nc ? ob[(size_t)j * D] : 0.f;
+        float m = lane < nc ? fmaxf(-INFINITY, mlv.x) : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float wl = lane < nc ? exp2f(mlv.x - m) : 0.f;
+        float l = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wl, j);
+            const float lc = __shfl_sync(0xffffffffu, mlv.y, j);
+            if (j < nc) {
+                l = fmaf(lc, w, l);
+                acc = fmaf(ov[j], w, acc);
+            }
+        }
+        acc *= 1.0f / l;
     } else {
         const int nc = p / CHUNK + 1;
         // m: max over the chunks (exact, any order); lane j holds chunks j, j + 32, ...
