@@ -554,7 +554,7 @@ attn_partial_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 // per lane: the chunk partials of 32 chunks are requested at once (the combine
 // is a chain of dependent loads otherwise), then added in ascending chunk
 // order.
-template <int D, bool OUT_BF16>
+template <int D, bool OUT_BF16, bool SHORT>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__restrict__ cu_rows, int S, int R, int Hq,
                     int nc_max, const float2 *__restrict__ part_ml, const float *__restrict__ part_o, void *out,
@@ -568,12 +568,14 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
     const int qb = wid % QB, rh = wid / QB;
     const int r = rh / Hq, h = rh % Hq;
     const int d = qb * 32 + lane;
-    const float2 *ml = part_ml + (size_t)rh * nc_max;
-    const float *ob = part_o + (size_t)rh * nc_max * D + d;
-    // chunk 0's partial (every row that is combined has one) is requested
-    // together with the row's position; it is only used for a valid row
-    const float2 ml0 = ml[0];
-    const float ov0 = ob[0];
+    // SHORT (every row within 32 chunks): chunk 0's partial, which every row
+    // that is combined has, is requested together with the row's position
+    float2 ml0 = make_float2(0.f, 0.f);
+    float ov0 = 0.f;
+    if constexpr (SHORT) {
+        ml0 = part_ml[(size_t)rh * nc_max];
+        ov0 = part_o[(size_t)rh * nc_max * D + d];
+    }
     const int lo = dev::warp_seq_of_row(cu_rows, S, r);   // sequence of row r
     const int r0 = cu_rows[lo], rows = cu_rows[lo + 1] - r0, ctx = ctx_start[lo];
     const int p = ctx + (r - r0);
@@ -583,40 +585,46 @@ attn_combine_kernel(const int32_t *__restrict__ ctx_start, const int32_t *__rest
     float acc = 0.f;
     if (rejected || p < 0 || p >= max_kv_len) {
         // a rejected sequence (reported by the partial kernel): emit zeros
-    } else if (p < CHUNK) {
-        // one chunk: the operations of the general path below with c = 0 alone
-        // (the other lanes' maxima are -inf, so m = fmaxf(-inf, m_0))
-        const float m = fmaxf(-INFINITY, ml0.x);
-        const float w = exp2f(ml0.x - m);
-        const float l = fmaf(ml0.y, w, 0.f);
-        acc = fmaf(ov0, w, 0.f);
-        acc *= 1.0f / l;
-    } else if (p < 32 * CHUNK) {
-        // at most 32 chunks, one per lane: the operations of the general path
-        // below (a single group, c0 = 0), with the (m, l) pairs and the values
-        // requested together instead of the pairs first for the maximum
-        const int nc = p / CHUNK + 1;
-        const float2 mlv = lane < nc ? ml[lane] : make_float2(-INFINITY, 0.f);
-        float ov[32];
+    } else if constexpr (SHORT) {
+        const int nc = p / CHUNK + 1;   // at most 32
+        if (nc == 1) {
+            // one chunk: the general path's operations with c = 0 alone (the
+            // other lanes' maxima are -inf, so m = fmaxf(-inf, m_0))
+            const float m = fmaxf(-INFINITY, ml0.x);
+            const float w = exp2f(ml0.x - m);
+            const float l = fmaf(ml0.y, w, 0.f);
+            acc = fmaf(ov0, w, 0.f);
+            acc *= 1.0f / l;
+        } else {
+            // one chunk per lane: the general path's operations (a single group,
+            // c0 = 0), with the (m, l) pairs and the values requested together
+            // instead of the pairs first for the maximum
+            const float2 *ml = part_ml + (size_t)rh * nc_max;
+            const float *ob = part_o + (size_t)rh * nc_max * D + d;
+            const float2 mlv = lane < nc ? ml[lane] : make_float2(-INFINITY, 0.f);
+            float ov[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ov[j] = j < nc ? ob[(size_t)j * D] : 0.f;
-        float m = lane < nc ? fmaxf(-INFINITY, mlv.x) : -INFINITY;
+            for (int j = 0; j < 32; ++j) ov[j] = j < nc ? ob[(size_t)j * D] : 0.f;
+            float m = lane < nc ? fmaxf(-INFINITY, mlv.x) : -INFINITY;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float wl = lane < nc ? exp2f(mlv.x - m) : 0.f;
-        float l = 0.f;
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const float wl = lane < nc ? exp2f(mlv.x - m) : 0.f;
+            float l = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float w = __shfl_sync(0xffffffffu, wl, j);
-            const float lc = __shfl_sync(0xffffffffu, mlv.y, j);
-            if (j < nc) {
-                l = fmaf(lc, w, l);
-                acc = fmaf(ov[j], w, acc);
+            for (int j = 0; j < 32; ++j) {
+                const float w = __shfl_sync(0xffffffffu, wl, j);
+                const float lc = __shfl_sync(0xffffffffu, mlv.y, j);
+                if (j < nc) {
+                    l = fmaf(lc, w, l);
+                    acc = fmaf(ov[j], w, acc);
+                }
             }
+            acc *= 1.0f / l;
         }
-        acc *= 1.0f / l;
     } else {
         const int nc = p / CHUNK + 1;
+        const float2 *ml = part_ml + (size_t)rh * nc_max;
+        const float *ob = part_o + (size_t)rh * nc_max * D + d;
         // m: max over the chunks (exact, any order); lane j holds chunks j, j + 32, ...
         float m = -INFINITY;
         for (int c = lane; c < nc; c += 32) m = fmaxf(m, ml[c].x);
@@ -747,17 +755,27 @@ spec_status attn_run(const void *q, spec_dtype qkv_dt, int Hq, int Hkv, int D, f
     dim3 grid((warps + 3) / 4);
     const int kv_cap = (int)std::min<long long>((long long)max_blocks * PAGE, INT_MAX);
     const bool obf = (out_dt == SPEC_BF16);
+    // every row within 32 chunks (the bound says so): the short-row instance
+    const bool short_rows = max_kv_len <= 32 * CHUNK;
+    auto launch_combine = [&](auto kern) {
+        return launch_pdl(kern, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml,
+                          (const float *)po, out, max_kv_len, kv_cap, xpk);
+    };
     cudaError_t le;
     if (D == 128) {
         if (obf)
-            le = launch_pdl(attn_combine_kernel<128, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, kv_cap, xpk);
+            le = short_rows ? launch_combine(attn_combine_kernel<128, true, true>)
+                            : launch_combine(attn_combine_kernel<128, true, false>);
         else
-            le = launch_pdl(attn_combine_kernel<128, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, kv_cap, xpk);
+            le = short_rows ? launch_combine(attn_combine_kernel<128, false, true>)
+                            : launch_combine(attn_combine_kernel<128, false, false>);
     } else {
         if (obf)
-            le = launch_pdl(attn_combine_kernel<64, true>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, kv_cap, xpk);
+            le = short_rows ? launch_combine(attn_combine_kernel<64, true, true>)
+                            : launch_combine(attn_combine_kernel<64, true, false>);
         else
-            le = launch_pdl(attn_combine_kernel<64, false>, grid, dim3(128), 0, stream, ctx_start, cu_rows, S, R, Hq, nc_max, (const float2 *)ml, (const float *)po, out, max_kv_len, kv_cap, xpk);
+            le = short_rows ? launch_combine(attn_combine_kernel<64, false, true>)
+                            : launch_combine(attn_combine_kernel<64, false, false>);
     }
     return cuda_status(le, "attn combine launch");
 }
