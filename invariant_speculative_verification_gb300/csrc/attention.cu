@@ -16,10 +16,13 @@
 // row; sub-tiles past p are left out of the row's merge altogether.
 //
 // K2 (attn_partial_kernel): a resident grid (at most one CTA per SM) walks
-// the (chunk, kv head, sequence) items, CTA b taking items b, b + grid, ...
-// (when sequences average more than one M-tile, the chunks of sequences of at
-// most SPLIT_CHUNKS chunks are two neighbouring items each, the lower and the
-// upper half of the chunk's M-tiles), its K and V
+// the (chunk, kv head, sequence) items, CTA b taking items b, b + grid, ...,
+// the chunk index varying slowest so that each warp's walk ends at the chunks
+// the sequences reach, whatever bound max_kv_len puts on them.  When
+// sequences average more than one M-tile, a second instance makes each chunk
+// two neighbouring items, the lower and the upper half of its M-tiles: for
+// sequences of at most SPLIT_CHUNKS chunks, and for all of them when the call
+// has items for three or more rounds of the grid.  Each item's K and V are
 // staged through a ring of three (D = 128; four at D = 64) half-item buffers
 // in the order K0 V0 K1 V1 ..., so that up to 1.5 items' copies run ahead of
 // the math.  A producer warp copies an item's K pages and its V pages (one TMA
@@ -35,7 +38,9 @@
 // Which CTA computes an item, and when, is scheduling: an item's operations
 // are those of a CTA of its own.
 // K3 (attn_combine_kernel): one warp per (row, head, 32-value block of the
-// head dimension), one value per lane.
+// head dimension), one value per lane; when every row is within 32 chunks, an
+// instance that finishes a one-chunk row from an early request of chunk 0 and
+// loads up to 32 chunks' partials in one round (the same operations).
 #include <algorithm>
 #include <climits>
 
